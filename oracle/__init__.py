@@ -1,0 +1,166 @@
+"""The oracle for C = A.B with f16 operands (fp64 accumulation).
+
+TEST INFRASTRUCTURE, NOT PART OF THE PRODUCT.  Only ``tests/``, the smoke
+check in ``__graft_entry__`` and the CPU-baseline / reference legs of
+``bench.py`` may import this package.  It shares no code with the CUDA
+library (``tiled_staged_matmul_gb300``) and neither side imports the other.
+
+Two independent implementations live here:
+
+* ``gemm_f64`` / ``gemm_cells`` -- the C library ``oracle_gemm.c``: the plain
+  triple loop, fp64, ascending k (see the header of that file for the passage
+  it follows).
+* ``exact_gemm`` -- a pure-Python brute force over ``fractions.Fraction``
+  that decodes f16 through numpy's own float16 conversion.  It has no
+  rounding at all and is only for tiny shapes; the tests use it to pin the C
+  oracle.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from fractions import Fraction
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle_gemm.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle_gemm.so")
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``oracle_gemm.c`` with gcc into ``oracle/_build``.
+
+    No fast-math and no fused multiply-add contraction (every product of two
+    f16 values is exact in fp64 anyway, so contraction could not change a
+    result; it is off so that nobody has to take that on trust)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+           "-ffp-contract=off", "-fno-fast-math", "-Wall", "-Wextra",
+           _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    build()
+    lib = ctypes.CDLL(_LIB_PATH)
+    i64 = ctypes.c_int64
+    vp = ctypes.c_void_p
+    lib.oracle_f16_to_f64.restype = ctypes.c_double
+    lib.oracle_f16_to_f64.argtypes = [ctypes.c_uint16]
+    lib.oracle_gemm_f16_f64.restype = ctypes.c_int
+    lib.oracle_gemm_f16_f64.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64,
+                                        ctypes.c_int]
+    lib.oracle_gemm_f16_f64_cells.restype = ctypes.c_int
+    lib.oracle_gemm_f16_f64_cells.argtypes = [vp, vp, i64, i64, i64, i64, i64,
+                                              vp, vp, i64, vp, ctypes.c_int]
+    lib.oracle_threads.restype = ctypes.c_int
+    lib.oracle_threads.argtypes = [ctypes.c_int]
+    _lib = lib
+    return lib
+
+
+def _as_u16(x) -> np.ndarray:
+    """View an f16 array (numpy float16 / uint16, or a CPU torch tensor) as
+    its raw binary16 bit patterns, without copying when possible."""
+    if hasattr(x, "detach"):  # torch tensor on the CPU
+        x = x.detach().contiguous().view(dtype=__import__("torch").int16).numpy()
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.float16 or x.dtype == np.int16:
+        return x.view(np.uint16)
+    if x.dtype == np.uint16:
+        return x
+    raise TypeError(f"expected f16 bit patterns, got {x.dtype}")
+
+
+def f16_to_f64(bits: int) -> float:
+    """The oracle's own binary16 decoder (for pinning against numpy)."""
+    return _load().oracle_f16_to_f64(int(bits) & 0xFFFF)
+
+
+def threads(nthreads: int = 0) -> int:
+    """Threads the oracle uses for a request (0 = all OpenMP allows)."""
+    return _load().oracle_threads(int(nthreads))
+
+
+def gemm_f64(A, B, M: int, N: int, K: int, lda: int | None = None,
+             ldb: int | None = None, nthreads: int = 0) -> np.ndarray:
+    """C = A.B in fp64, ascending k, as an M x N float64 array.
+
+    ``A`` holds at least ``(M-1)*lda + K`` f16 values and ``B`` at least
+    ``(K-1)*ldb + N``, row-major (flattened or 2-D)."""
+    lda = K if lda is None else lda
+    ldb = N if ldb is None else ldb
+    a = _as_u16(A).reshape(-1)
+    b = _as_u16(B).reshape(-1)
+    if M > 0 and K > 0 and a.size < (M - 1) * lda + K:
+        raise ValueError("A is smaller than M, K and lda require")
+    if K > 0 and N > 0 and b.size < (K - 1) * ldb + N:
+        raise ValueError("B is smaller than K, N and ldb require")
+    C = np.empty((M, N), dtype=np.float64)
+    if M == 0 or N == 0:
+        return C
+    rc = _load().oracle_gemm_f16_f64(a.ctypes.data, b.ctypes.data, C.ctypes.data,
+                                     M, N, K, lda, ldb, N, int(nthreads))
+    if rc != 0:
+        raise RuntimeError("oracle_gemm_f16_f64 rejected its arguments")
+    return C
+
+
+def gemm_cells(A, B, M: int, N: int, K: int, rows, cols,
+               lda: int | None = None, ldb: int | None = None,
+               nthreads: int = 0) -> np.ndarray:
+    """The fp64 values of the selected cells C[rows[t], cols[t]]."""
+    lda = K if lda is None else lda
+    ldb = N if ldb is None else ldb
+    a = _as_u16(A).reshape(-1)
+    b = _as_u16(B).reshape(-1)
+    r = np.ascontiguousarray(rows, dtype=np.int64)
+    c = np.ascontiguousarray(cols, dtype=np.int64)
+    if r.shape != c.shape:
+        raise ValueError("rows and cols differ in length")
+    out = np.empty(r.size, dtype=np.float64)
+    rc = _load().oracle_gemm_f16_f64_cells(a.ctypes.data, b.ctypes.data, M, N, K,
+                                           lda, ldb, r.ctypes.data, c.ctypes.data,
+                                           r.size, out.ctypes.data, int(nthreads))
+    if rc != 0:
+        raise RuntimeError("oracle_gemm_f16_f64_cells rejected its arguments")
+    return out
+
+
+def exact_gemm(A, B, M: int, N: int, K: int, lda: int | None = None,
+               ldb: int | None = None) -> list[list[Fraction]]:
+    """Brute force with exact rationals: no rounding anywhere.
+
+    Each f16 value becomes ``Fraction(float(numpy.float16))`` -- numpy's own
+    conversion, independent of the C decoder -- and every sum is exact.
+    Pure-Python loops, so only for tiny shapes."""
+    lda = K if lda is None else lda
+    ldb = N if ldb is None else ldb
+    a = _as_u16(A).reshape(-1).view(np.float16)
+    b = _as_u16(B).reshape(-1).view(np.float16)
+    fa = [Fraction(float(v)) for v in a]
+    fb = [Fraction(float(v)) for v in b]
+    out = []
+    for i in range(M):
+        row = []
+        for j in range(N):
+            s = Fraction(0)
+            for k in range(K):
+                s += fa[i * lda + k] * fb[k * ldb + j]
+            row.append(s)
+        out.append(row)
+    return out
