@@ -1,0 +1,399 @@
+#!/usr/bin/env python3
+"""Throughput of the GB300 f16 x f16 -> f32 GEMM, one JSON line on stdout.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-cpu-baseline] [--no-e2e]
+
+A step is one call of the C ABI's GEMM on one synthetic, seeded workload
+(default: 8192 x 8192 x 8192, f16 N(0, 1/sqrt(K)) operands), inputs resident
+in HBM.  Each step is timed with CUDA events on the launching stream; the K
+steps sit between a barrier + device synchronisation on both sides and the
+slowest rank decides.  With N > 1 every rank runs an independent replica
+(the GEMM is single-GPU; the value is the sum over ranks: weak scaling).
+
+``--impl reference`` times the CPU oracle (fp64 triple loop) instead, on a
+bounded row sample of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "gemm_8192x8192x8192_normal_invsqrtk"
+METRIC = "GEMM TFLOP/s (f16 in, f32 acc) and % of GB300 dense-f16 / HBM roofline"
+L2_BYTES = 129 * 1024 * 1024
+KERNEL_SOURCES = ["tiled_staged_matmul_gb300/csrc/gemm_kernels.cu",
+                  "tiled_staged_matmul_gb300/csrc/ptx.cuh"]
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--e2e-steps", type=int, default=10)
+    return p.parse_args(argv)
+
+
+# ------------------------------------------------------------------ distributed helpers
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ peaks and roofline
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the GEMM kernel from an ncu capture, if one
+    was recorded for exactly the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if e and e.get("kernel_hash") == kernel_source_hash():
+        return e.get("dram_bytes_per_launch")
+    return None
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi sampled every 20 ms in the background; samples are kept
+    with their host time so that only those inside the timed region count."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        rows = [s for (t, s) in self.samples if t0 <= t <= t1]
+        if not rows:  # region shorter than the sampling period: nearest samples
+            rows = [s for (t, s) in sorted(self.samples, key=lambda ts: abs(ts[0] - (t0 + t1) / 2))[:3]]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            parts = [p.strip() for p in r.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, rank, local_rank, world):
+    import torch
+    from tiled_staged_matmul_gb300 import binding, synthetic
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = synthetic.WORKLOADS[args.workload]
+    A_h, B_h = synthetic.workload_operands(w)
+    A = A_h.to(dev)
+    B = B_h.to(dev)
+    C = torch.empty((w.M, w.N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    plan = binding.gemm_plan(w.M, w.N, w.K)
+    launches_per_call = 2 if plan["split_k"] > 1 else 1
+
+    working_set = 2 * w.M * w.K + 2 * w.K * w.N + 4 * w.M * w.N
+    flush = working_set < 2 * L2_BYTES
+    scrub = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+
+    def call():
+        binding.check(binding.gemm_f16_f32acc(A.data_ptr(), B.data_ptr(), C.data_ptr(),
+                                              w.M, w.N, w.K, w.K, w.N, w.N, stream.cuda_stream))
+
+    for _ in range(max(args.warmup, 3)):
+        if flush:
+            scrub.zero_()
+        call()
+    binding.check(binding.gemm_get_device_status(stream.cuda_stream))
+    torch.cuda.synchronize()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(args.steps):
+        if flush:
+            scrub.zero_()
+        starts[i].record(stream)
+        call()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t1 = time.time()
+    time.sleep(0.1)
+    sampler.stop()
+    binding.check(binding.gemm_get_device_status(stream.cuda_stream))
+
+    per_step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms_local = sum(per_step_ms) / len(per_step_ms)
+    ms = max_over_ranks(ms_local, world, dev)
+    value = world * w.flops / (ms * 1e-3) / 1e12
+
+    peaks = measured_peaks()
+    tflops_launch = w.flops / (ms_local * 1e-3) / 1e12
+    gbs_launch = w.algorithmic_bytes / (ms_local * 1e-3) / 1e9
+    t_tensor = w.flops / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = w.algorithmic_bytes / (peaks["hbm_gbs"] * 1e9)
+    if t_tensor >= t_hbm:
+        roofline = {"bound": "tensor", "achieved": round(tflops_launch, 2),
+                    "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": round(tflops_launch / peaks["bf16_tflops"], 4)}
+    else:
+        roofline = {"bound": "hbm", "achieved": round(gbs_launch, 1), "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": round(gbs_launch / peaks["hbm_gbs"], 4)}
+    roofline["traffic"] = recorded_traffic(args.workload)
+    roofline["peak_source"] = (f"{peaks['source']} (MEASURED_PEAKS.json bf16 burst; f16 dense "
+                               "rate taken equal to bf16, the nominal ratio)"
+                               if roofline["bound"] == "tensor" else
+                               f"{peaks['source']} (MEASURED_PEAKS.json copy bandwidth)")
+    roofline["kernel"] = "tsm_gemm_tcgen05_kernel" + (" + tsm_splitk_reduce_kernel"
+                                                      if launches_per_call > 1 else "")
+
+    result = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
+                   "dist": w.dist, "seed": w.seed, "accumulate": "f32",
+                   "tile_n": plan["tile_n"], "split_k": plan["split_k"],
+                   "stages": plan["stages"], "grid": plan["grid"],
+                   "l2": "flushed before every step" if flush else
+                         f"inputs+output {working_set / 2**20:.0f} MiB > L2, no flush",
+                   "parallelism": f"replicas x{world}"},
+        "gpu_launches": args.steps * launches_per_call,
+        "roofline": roofline,
+    }
+    clocks = sampler.summary(t0, t1)
+    result["clocks"] = {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")}
+
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(args, w, A_h, B_h, dev, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w, A_h, B_h, target_s=15.0)
+    return result
+
+
+def run_e2e(args, w, A_h, B_h, dev, world):
+    """Same metric through the public API from pinned host buffers: every step
+    copies A and B to the device, runs the GEMM and copies C back."""
+    import torch
+    from tiled_staged_matmul_gb300 import binding
+
+    A_p = A_h.pin_memory()
+    B_p = B_h.pin_memory()
+    C_p = torch.empty((w.M, w.N), dtype=torch.float32).pin_memory()
+    dA = torch.empty_like(A_p, device=dev)
+    dB = torch.empty_like(B_p, device=dev)
+    dC = torch.empty((w.M, w.N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(2):
+        binding.gemm_host(A_p, B_p, C_p, dA, dB, dC, stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(args.e2e_steps):
+        binding.gemm_host(A_p, B_p, C_p, dA, dB, dC, stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = start.elapsed_time(end) / args.e2e_steps
+    ms = max_over_ranks(ms, world, dev)
+    return {"value": round(world * w.flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": A_p.numel() * 2 + B_p.numel() * 2,
+            "d2h_bytes_per_step": C_p.numel() * 4}
+
+
+# ------------------------------------------------------------------ the oracle, timed
+
+def oracle_sample_rows(w, A_h, B_h, rows: int, seed: int = 0):
+    """Time the oracle on `rows` consecutive rows of C (a contiguous row
+    panel of A times all of B): flops = 2 * rows * N * K."""
+    import oracle
+    r0 = (seed * 7919) % max(1, w.M - rows + 1)
+    A_rows = A_h[r0:r0 + rows].contiguous()
+    t = time.perf_counter()
+    oracle.gemm_f64(A_rows, B_h, rows, w.N, w.K)
+    return time.perf_counter() - t
+
+
+def cpu_baseline(w, A_h, B_h, target_s: float):
+    import oracle
+    probe_rows = max(1, min(w.M, int(2e9 // (2 * w.N * w.K)) or 1))
+    dt = oracle_sample_rows(w, A_h, B_h, probe_rows)
+    rate = 2 * probe_rows * w.N * w.K / max(dt, 1e-9)
+    rows = max(1, min(w.M, int(rate * target_s / (2 * w.N * w.K))))
+    dt = oracle_sample_rows(w, A_h, B_h, rows, seed=1)
+    flops = 2 * rows * w.N * w.K
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.threads(),
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": f"{rows} of {w.M} rows of C ({rows} x {w.N} x {w.K}), fp64 triple loop, "
+                      f"OpenMP over rows"}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle, each step a bounded row sample."""
+    import oracle
+    from tiled_staged_matmul_gb300 import synthetic
+
+    w = synthetic.WORKLOADS[args.workload]
+    A_h, B_h = synthetic.workload_operands(w)
+    rows = max(1, min(w.M, int(4e9 // (2 * w.N * w.K)) or 1))
+    for i in range(max(args.warmup, 0)):
+        oracle_sample_rows(w, A_h, B_h, rows, seed=i)
+    times = [oracle_sample_rows(w, A_h, B_h, rows, seed=i) for i in range(args.steps)]
+    t = sum(times) / len(times)
+    flops = 2 * rows * w.N * w.K
+    value = flops / t / 1e12
+    sample = f"{rows} of {w.M} rows of C per step ({rows} x {w.N} x {w.K}), fp64 triple loop"
+    return {
+        "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "dist": w.dist,
+                   "seed": w.seed},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, local_rank, world = dist_env()
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return 0
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    result = run_ours(args, rank, local_rank, world)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,179 @@
+/*
+ * tsm_gemm.h -- C ABI of the GB300 (sm_103a) K-tiled, operand-staged GEMM.
+ *
+ *   C = A . B      A: M x K f16, B: K x N f16, C: M x N f32, f32 accumulation
+ *
+ * What the operation is, and where it is defined:
+ *
+ * - One output cell is the K-long dot product sum_k A[i][k] * B[k][j]
+ *   ("The PTSS Cliff: A Kernel That Won't Build", section "The Arithmetic of
+ *   'Fully Unrolled K'").  The library computes it the way that page's fix
+ *   does: operands staged in fast on-chip memory (here TMA into a
+ *   shared-memory ring), the K dimension walked in K_TILE chunks with the
+ *   accumulator carried across them (here 64-deep k-blocks into a TMEM
+ *   accumulator) -- sections "The Idea: Stage in SLM, Tile K" and "The Pass,
+ *   Step by Step".
+ * - The accumulator is f32 even though the operands are 16-bit ("A Dumb
+ *   Triton Runtime Error", section "Step 1": the chunk is converted to
+ *   float32 before it is summed, because 16-bit sums overflow or lose
+ *   precision).
+ * - Edge tiles read zeros past the matrix ("Intel XPU Backend for Triton",
+ *   section "Use Tensor Descriptors to load tl.dot arguments and save
+ *   results": the descriptor's shape masks out-of-bounds values to zero;
+ *   "A Dumb Triton Runtime Error", section "Step 2": masked lanes take
+ *   other=0, the additive identity).  No divisibility of M, N or K by any
+ *   tile size is required.  Stores are clipped to i < M, j < N.
+ * - Operands are row-major with strides in elements and a unit last stride
+ *   ("Intel XPU Backend for Triton", sections "Set last stride to 1" and
+ *   "Use Proper Type Annotations", whose GEMM signature takes M, N, K and a
+ *   row stride per matrix).  Offsets are computed in 64 bits (same page,
+ *   section "Avoid int32 Overflow").
+ * - C is overwritten (beta = 0): its previous contents are never read.  The
+ *   pages show that accumulating into an output left over from a previous
+ *   allocation gives wrong answers ("A Dumb Triton Runtime Error", section
+ *   "1. Atomics accumulate onto whatever is already in out"); the split-K
+ *   path below therefore uses no atomics on C and sums its partial products
+ *   in a fixed order.
+ *
+ * Memory and ownership.  A, B and C are DEVICE pointers on the current CUDA
+ * device, owned by the caller (for example torch tensors), and must stay
+ * valid until the work queued on `stream` has finished.  The library owns
+ * only its split-K workspace, taken from a private stream-ordered memory
+ * pool on `stream` and returned to it on the same stream, and a small
+ * per-device status word.
+ *
+ * Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ * default stream).  Argument errors are found on the host, before anything
+ * is queued, and return at once; nothing aborts, traps or prints.  Every
+ * device-side wait is bounded in time: if one runs out the kernel records
+ * GEMM_ERR_DEVICE_TIMEOUT in the status word and returns, and
+ * gemm_get_device_status() reports it.
+ *
+ * Requirements, each checked (the status returned is in brackets):
+ *   M, N, K >= 0 and < 2^31                          [INVALID_VALUE]
+ *   lda >= K, ldb >= N, ldc >= N (elements)          [INVALID_VALUE]
+ *   A, B, C 16-byte aligned; lda and ldb multiples
+ *   of 8, ldc a multiple of 4 (16-byte row pitch,
+ *   the tensor-memory-accelerator's rule)            [MISALIGNED]
+ *   A, B, C device memory of the current device,
+ *   each spanning the rows it is said to have        [INVALID_VALUE]
+ *   C's bytes overlap neither A's nor B's            [ALIAS]
+ *   a compute-capability 10.3 GPU (GB300)            [UNSUPPORTED_DEVICE]
+ * M == 0 or N == 0 (or batch == 0) queues nothing and returns GEMM_OK;
+ * K == 0 writes zeros into C (the empty sum).
+ */
+#ifndef TSM_GEMM_H
+#define TSM_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The same type as cudaStream_t, declared here so that this header needs no
+ * CUDA header. */
+typedef struct CUstream_st *gemm_stream_t;
+
+typedef enum gemm_status {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_VALUE = 1,      /* null pointer, bad size or stride, not device memory */
+    GEMM_ERR_MISALIGNED = 2,         /* base not 16-byte aligned, or row pitch not a multiple of 16 bytes */
+    GEMM_ERR_ALIAS = 3,              /* C overlaps A or B, or two batches of C overlap */
+    GEMM_ERR_UNSUPPORTED_DEVICE = 4, /* not a compute-capability 10.3 device */
+    GEMM_ERR_CUDA = 5,               /* a CUDA runtime or driver call failed; see gemm_last_error_string */
+    GEMM_ERR_DEVICE_TIMEOUT = 6      /* a bounded device-side wait ran out (reported by gemm_get_device_status) */
+} gemm_status_t;
+
+/* Tuning and test options.  Zero in every field means "the planner
+ * chooses"; a NULL pointer means the same. */
+typedef struct gemm_options {
+    int32_t split_k;    /* 0: planner's choice; S >= 1: split K into S contiguous ranges
+                           (clamped to the number of 64-deep k-blocks) */
+    int32_t tile_n;     /* 0: planner's choice; else 64, 128 or 256 output columns per tile */
+    int32_t timeout_ms; /* 0: default; else the limit of every device-side wait, in ms */
+    int32_t inject_stall; /* test hook, 0 in normal use; 1 makes the epilogue wait on a
+                             barrier that nothing signals, so that its bounded wait runs
+                             out and the call reports GEMM_ERR_DEVICE_TIMEOUT */
+} gemm_options_t;
+
+/* What the planner chose for a problem (see gemm_plan). */
+typedef struct gemm_plan_info {
+    int32_t tile_m;       /* rows of C per tile (128) */
+    int32_t tile_n;       /* columns of C per tile */
+    int32_t tile_k;       /* K depth of one staged k-block (64) */
+    int32_t stages;       /* k-blocks in flight in the shared-memory ring */
+    int32_t split_k;      /* number of K ranges (1 = no split) */
+    int32_t tiles_m;      /* ceil(M / tile_m) */
+    int32_t tiles_n;      /* ceil(N / tile_n) */
+    int32_t k_blocks;     /* ceil(K / tile_k) */
+    int64_t units;        /* batch * split_k * tiles_m * tiles_n work units */
+    int32_t grid;         /* persistent CTAs launched: min(units, SMs) */
+    int32_t group_m;      /* tiles of M walked together in the raster order */
+    int64_t stage_bytes;  /* shared memory of one k-block: A tile + B tile */
+    int64_t smem_bytes;   /* dynamic shared memory of one CTA */
+    int64_t workspace_bytes; /* split-K partials (0 when split_k == 1) */
+} gemm_plan_info_t;
+
+/* C = A . B for one matrix.
+ *   A    device, M rows of K f16 values (IEEE binary16 bit patterns), row stride lda
+ *   B    device, K rows of N f16 values, row stride ldb
+ *   C    device, M rows of N f32 values, row stride ldc; written, never read;
+ *        elements of a row past N (up to ldc) are left untouched
+ * Returns GEMM_OK once the work is queued on `stream`. */
+gemm_status_t gemm_f16_f32acc(const uint16_t *A, const uint16_t *B, float *C,
+                              int64_t M, int64_t N, int64_t K,
+                              int64_t lda, int64_t ldb, int64_t ldc,
+                              gemm_stream_t stream);
+
+/* C[b] = A[b] . B[b] for b < batch, the matrices of a batch `strideA`,
+ * `strideB` and `strideC` elements apart (int64; the pages' MoE example
+ * indexes a 3-D [E, M, K] tensor by expert with such a stride -- "Intel XPU
+ * Backend for Triton", section "Use Tensor Descriptors ...", the A[E, :M, :]
+ * slice, and section "Avoid int32 Overflow").  Strides must be multiples of 8
+ * (A, B) and 4 (C) elements; with batch > 1 they must be positive and the
+ * batches of C must not overlap. */
+gemm_status_t gemm_f16_f32acc_batched(const uint16_t *A, const uint16_t *B, float *C,
+                                      int64_t M, int64_t N, int64_t K,
+                                      int64_t lda, int64_t ldb, int64_t ldc,
+                                      int64_t strideA, int64_t strideB, int64_t strideC,
+                                      int64_t batch, gemm_stream_t stream);
+
+/* The batched call with explicit options (NULL = all defaults). */
+gemm_status_t gemm_f16_f32acc_opts(const uint16_t *A, const uint16_t *B, float *C,
+                                   int64_t M, int64_t N, int64_t K,
+                                   int64_t lda, int64_t ldb, int64_t ldc,
+                                   int64_t strideA, int64_t strideB, int64_t strideC,
+                                   int64_t batch, const gemm_options_t *opts,
+                                   gemm_stream_t stream);
+
+/* The plan the library would use, computed on the host only (no GPU is
+ * touched).  num_sms is the SM count to plan for (0 = the current device's).
+ * This is the analogue of the pages' footprint check and K_TILE choice
+ * ("The PTSS Cliff ...", sections "The SLM Footprint" and "Choosing
+ * K_TILE"): the ring holds as many A+B k-block stages as fit the shared
+ * memory budget, and at least two must fit. */
+gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int64_t batch,
+                        const gemm_options_t *opts, int32_t num_sms,
+                        gemm_plan_info_t *plan);
+
+/* Waits for `stream`, then reports and clears the current device's status
+ * word: GEMM_OK, or GEMM_ERR_DEVICE_TIMEOUT if a bounded wait of an earlier
+ * call ran out (that call's output is then incomplete), or GEMM_ERR_CUDA if
+ * the stream reported an error. */
+gemm_status_t gemm_get_device_status(gemm_stream_t stream);
+
+/* The message of the last failed call on this host thread ("" if none). */
+const char *gemm_last_error_string(void);
+
+/* A fixed name for a status code. */
+const char *gemm_status_string(gemm_status_t status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t gemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TSM_GEMM_H */

@@ -1,0 +1,162 @@
+"""The C ABI without a GPU: the library loads, exports every symbol the
+header declares, rejects bad arguments on the host before touching CUDA,
+and plans as the shared-memory budget dictates."""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+from tiled_staged_matmul_gb300.csrc import build as tsm_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tsm_gemm.h")
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="module")
+def b():
+    tsm_build.build()
+    from tiled_staged_matmul_gb300 import binding
+    return binding
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(gemm_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("gemm_f16_f32acc", "gemm_f16_f32acc_batched", "gemm_get_device_status",
+              "gemm_last_error_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(b):
+    lib = ctypes.CDLL(b.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_version_and_status_names(b):
+    assert b.gemm_version() >= 100
+    assert b.gemm_status_string(b.GEMM_ERR_ALIAS) == "GEMM_ERR_ALIAS"
+    assert b.gemm_status_string(99) == "GEMM_ERR_UNKNOWN"
+
+
+# Fake, never-dereferenced device addresses: every case below is rejected by
+# the host-side checks before any CUDA call is made.
+A0, B0, C0 = 0x7f0000000000, 0x7f0010000000, 0x7f0020000000
+
+
+@pytest.mark.parametrize("args,status", [
+    ((A0, B0, 0, 4, 4, 4, 8, 8, 4), "GEMM_ERR_INVALID_VALUE"),        # C NULL
+    ((A0, B0, C0, -1, 4, 4, 8, 8, 4), "GEMM_ERR_INVALID_VALUE"),      # negative M
+    ((A0, B0, C0, 4, 4, 2**31, 2**31, 8, 4), "GEMM_ERR_INVALID_VALUE"),  # K too large
+    ((A0, B0, C0, 4, 4, 16, 8, 8, 4), "GEMM_ERR_INVALID_VALUE"),      # lda < K
+    ((A0, B0, C0, 4, 16, 4, 8, 8, 16), "GEMM_ERR_INVALID_VALUE"),     # ldb < N
+    ((A0, B0, C0, 4, 8, 4, 8, 8, 4), "GEMM_ERR_INVALID_VALUE"),       # ldc < N
+    ((0, B0, C0, 4, 4, 4, 8, 8, 4), "GEMM_ERR_INVALID_VALUE"),        # A NULL
+    ((A0 + 2, B0, C0, 4, 4, 4, 8, 8, 4), "GEMM_ERR_MISALIGNED"),      # A not 16-byte aligned
+    ((A0, B0, C0 + 4, 4, 4, 4, 8, 8, 4), "GEMM_ERR_MISALIGNED"),      # C not 16-byte aligned
+    ((A0, B0, C0, 4, 4, 4, 12, 8, 4), "GEMM_ERR_MISALIGNED"),         # lda not a multiple of 8
+    ((A0, B0, C0, 4, 4, 4, 8, 12, 4), "GEMM_ERR_MISALIGNED"),         # ldb not a multiple of 8
+    ((A0, B0, C0, 4, 4, 4, 8, 8, 6), "GEMM_ERR_MISALIGNED"),          # ldc not a multiple of 4
+    ((A0, B0, A0 + 16, 4, 4, 4, 8, 8, 4), "GEMM_ERR_ALIAS"),          # C inside A
+    ((A0, B0, B0, 4, 4, 4, 8, 8, 4), "GEMM_ERR_ALIAS"),               # C on B
+])
+def test_host_rejects_bad_arguments(b, args, status):
+    st = b.gemm_f16_f32acc(*args, 0)
+    assert b.gemm_status_string(st) == status
+    assert b.gemm_last_error_string() != ""
+
+
+def test_empty_problems_need_no_gpu(b):
+    assert b.gemm_f16_f32acc(0, 0, 0, 0, 5, 7, 8, 8, 8, 0) == b.GEMM_OK
+    assert b.gemm_f16_f32acc(0, 0, 0, 5, 0, 7, 8, 8, 8, 0) == b.GEMM_OK
+    assert b.gemm_f16_f32acc_batched(A0, B0, C0, 4, 4, 4, 8, 8, 4, 0, 0, 0, 0, 0) == b.GEMM_OK
+
+
+def test_batched_strides_checked(b):
+    # overlapping batches of C
+    st = b.gemm_f16_f32acc_batched(A0, B0, C0, 4, 4, 4, 8, 8, 4, 32, 32, 8, 2, 0)
+    assert b.gemm_status_string(st) == "GEMM_ERR_ALIAS"
+    # non-positive stride with batch > 1
+    st = b.gemm_f16_f32acc_batched(A0, B0, C0, 4, 4, 4, 8, 8, 4, 0, 32, 16, 2, 0)
+    assert b.gemm_status_string(st) == "GEMM_ERR_INVALID_VALUE"
+    # stride not a multiple of 8 elements
+    st = b.gemm_f16_f32acc_batched(A0, B0, C0, 4, 4, 4, 8, 8, 4, 36, 32, 16, 2, 0)
+    assert b.gemm_status_string(st) == "GEMM_ERR_MISALIGNED"
+
+
+# ---------------------------------------------------------------- planner
+
+SMS = 152
+
+
+def test_stage_footprint_matches_the_pages_arithmetic(b):
+    """The pages stage a 64 x 128 f16 A tile (16384 B) and a 128 x 128 f16 B
+    tile (32768 B), 48 KiB in all.  The 128 x 256 x 64 k-block staged here
+    holds the same byte counts: a 128 x 64 A tile and a 64 x 256 B tile."""
+    g = json.load(open(os.path.join(GOLDEN, "slm_footprint.json")))
+    e = g["dtype_bytes"]
+    assert g["M"] * g["K"] * e == g["a_tile_bytes"]
+    assert g["K"] * g["N"] * e == g["b_tile_bytes"]
+    assert g["a_tile_bytes"] + g["b_tile_bytes"] == g["total_bytes"]
+    assert (g["total_bytes"] <= g["budget_bytes"]) == g["fits"]
+    p = b.gemm_plan(8192, 8192, 8192, 1, b._opts(tile_n=256), SMS)
+    assert p["tile_m"] * p["tile_k"] * e == g["a_tile_bytes"]
+    assert p["tile_k"] * p["tile_n"] * e == g["b_tile_bytes"]
+    assert p["stage_bytes"] == g["total_bytes"]
+
+
+@pytest.mark.parametrize("tile_n", [64, 128, 256])
+def test_ring_fills_the_shared_memory_budget(b, tile_n):
+    p = b.gemm_plan(4096, 4096, 4096, 1, b._opts(tile_n=tile_n), SMS)
+    assert p["stage_bytes"] == 2 * 128 * 64 + 2 * 64 * tile_n
+    assert p["stages"] >= 2
+    assert p["smem_bytes"] <= 232448
+    # one more stage would not fit
+    assert p["smem_bytes"] + p["stage_bytes"] > 232448 or p["stages"] == 8
+    # one CTA per SM, so the two TMEM accumulators (2 x tile_n columns) never contend
+    assert p["smem_bytes"] > 232448 // 2
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 128, 128), (1000, 1000, 1000), (4096, 4096, 4096),
+                                   (256, 256, 65536), (8192, 8192, 8192), (1, 1, 1),
+                                   (300, 7, 100000), (1, 5000, 64)])
+def test_plan_invariants(b, M, N, K):
+    p = b.gemm_plan(M, N, K, 1, None, SMS)
+    assert p["tiles_m"] == -(-M // 128)
+    assert p["tiles_n"] == -(-N // p["tile_n"])
+    assert p["k_blocks"] == -(-K // 64)
+    assert 1 <= p["split_k"] <= p["k_blocks"]
+    assert p["units"] == p["tiles_m"] * p["tiles_n"] * p["split_k"]
+    assert p["grid"] == min(p["units"], SMS)
+    ldw = -(-N // 4) * 4
+    assert p["workspace_bytes"] == (p["split_k"] * M * ldw * 4 if p["split_k"] > 1 else 0)
+
+
+def test_long_K_small_output_splits_K(b):
+    p = b.gemm_plan(256, 256, 65536, 1, None, SMS)
+    assert p["split_k"] > 1
+    assert p["units"] <= SMS
+    assert p["k_blocks"] // p["split_k"] >= 4
+
+
+def test_large_square_uses_wide_tiles_without_split(b):
+    p = b.gemm_plan(8192, 8192, 8192, 1, None, SMS)
+    assert p["tile_n"] == 256 and p["split_k"] == 1
+
+
+def test_forced_split_is_clamped_to_k_blocks(b):
+    p = b.gemm_plan(128, 128, 128, 1, b._opts(split_k=64), SMS)
+    assert p["split_k"] == 2
+
+
+def test_bad_options_rejected(b):
+    with pytest.raises(b.GemmError):
+        b.gemm_plan(128, 128, 128, 1, b._opts(tile_n=96), SMS)

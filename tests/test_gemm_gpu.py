@@ -1,0 +1,273 @@
+"""Parity of the CUDA path with the oracle, on a GB300.
+
+Every case runs through the C ABI on padded device buffers (NaN in every
+operand's padding and guard band, a sentinel around C) and compares with
+the fp64 oracle: bit for bit on small-integer inputs (exact in f32), within
+max |C - C_ref| <= 1e-3 sqrt(K) and relative Frobenius error <= 1e-4 on
+random inputs.  The shapes span several tiles and ragged tails; the five
+workload shapes run at full size (the 8192^3 one on sampled cells)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tiled_staged_matmul_gb300 import synthetic
+from tiled_staged_matmul_gb300.synthetic import WORKLOADS, integer_twin
+
+from gpu_util import check_exact, check_tolerance, run_gemm
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def b():
+    if not torch.cuda.is_available():
+        pytest.fail("the GPU tests need a CUDA device")
+    from tiled_staged_matmul_gb300 import binding
+    return binding
+
+
+def ref_of(A, B):
+    M, K = A.shape
+    N = B.shape[1]
+    return oracle.gemm_f64(A.contiguous(), B.contiguous(), M, N, K)
+
+
+# ---------------------------------------------------------------- the workload shapes
+
+def test_small_shape_integer_bit_exact(b):
+    w = WORKLOADS["gemm_64x128x128_int4"]
+    A, B = synthetic.workload_operands(w)
+    C, dC = run_gemm(b, A, B)
+    check_exact(C.numpy(), ref_of(A, B))
+    assert dC.outside_untouched()
+
+
+def test_small_shape_uniform(b):
+    w = WORKLOADS["gemm_64x128x128_uniform"]
+    A, B = synthetic.workload_operands(w)
+    C, dC = run_gemm(b, A, B)
+    check_tolerance(C.numpy(), ref_of(A, B), w.K)
+    assert dC.outside_untouched()
+
+
+def test_1000_cube_ragged_edges(b):
+    w = WORKLOADS["gemm_1000x1000x1000_normal"]
+    A, B = synthetic.workload_operands(w)
+    C, dC = run_gemm(b, A, B)
+    check_tolerance(C.numpy(), ref_of(A, B), w.K)
+    assert dC.outside_untouched()
+
+
+def test_1000_cube_integer_bit_exact(b):
+    w = integer_twin(WORKLOADS["gemm_1000x1000x1000_normal"])
+    A, B = synthetic.workload_operands(w)
+    C, _ = run_gemm(b, A, B)
+    check_exact(C.numpy(), ref_of(A, B))
+
+
+def test_4096_cube(b):
+    w = WORKLOADS["gemm_4096x4096x4096_normal_invsqrtk"]
+    A, B = synthetic.workload_operands(w)
+    C, dC = run_gemm(b, A, B)
+    check_tolerance(C.numpy(), ref_of(A, B), w.K)
+    assert dC.outside_untouched()
+
+
+def test_long_K_split(b):
+    w = WORKLOADS["gemm_256x256x65536_uniform"]
+    plan = b.gemm_plan(w.M, w.N, w.K)
+    assert plan["split_k"] > 1
+    A, B = synthetic.workload_operands(w)
+    C, dC = run_gemm(b, A, B)
+    check_tolerance(C.numpy(), ref_of(A, B), w.K)
+    assert dC.outside_untouched()
+    C2, _ = run_gemm(b, A, B)
+    assert torch.equal(C, C2), "split-K result is not reproducible run to run"
+
+
+def test_long_K_integer_bit_exact_for_every_split(b):
+    w = integer_twin(WORKLOADS["gemm_256x256x65536_uniform"])
+    A, B = synthetic.workload_operands(w)
+    ref = ref_of(A, B)
+    for s in (1, 2, 3, 7, 64, 0):
+        C, _ = run_gemm(b, A, B, split_k=s)
+        check_exact(C.numpy(), ref)
+
+
+def _sampled_cells(w, C, A, B, n=4096, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = rng.integers(0, w.M, n)
+    cols = rng.integers(0, w.N, n)
+    # always include the corners and the last row / column
+    rows[:4] = [0, 0, w.M - 1, w.M - 1]
+    cols[:4] = [0, w.N - 1, 0, w.N - 1]
+    ref = oracle.gemm_cells(A, B, w.M, w.N, w.K, rows, cols)
+    return C.numpy()[rows, cols], ref
+
+
+def test_8192_cube_sampled(b):
+    w = WORKLOADS["gemm_8192x8192x8192_normal_invsqrtk"]
+    A, B = synthetic.workload_operands(w)
+    C, dC = run_gemm(b, A, B)
+    got, ref = _sampled_cells(w, C, A, B)
+    check_tolerance(got, ref, w.K)
+    assert torch.isfinite(C).all()
+    assert dC.outside_untouched()
+
+
+def test_8192_cube_integer_sampled_and_transpose_identity(b):
+    w = integer_twin(WORKLOADS["gemm_8192x8192x8192_normal_invsqrtk"])
+    A, B = synthetic.workload_operands(w)
+    C, _ = run_gemm(b, A, B)
+    got, ref = _sampled_cells(w, C, A, B)
+    check_exact(got, ref)
+    # (A.B)^T == B^T.A^T exactly on integers: a second call with swapped operands
+    Ct, _ = run_gemm(b, B.t().contiguous(), A.t().contiguous())
+    assert torch.equal(C, Ct.t())
+
+
+# ---------------------------------------------------------------- ragged and edge cases
+
+RAGGED = [(1, 1, 1), (1, 8, 1), (7, 9, 63), (129, 257, 65), (130, 250, 1000),
+          (255, 129, 127), (128, 256, 64), (300, 1, 200), (1, 300, 200), (513, 77, 33)]
+
+
+@pytest.mark.parametrize("M,N,K", RAGGED)
+@pytest.mark.parametrize("tile_n", [64, 128, 256])
+def test_ragged_integer_bit_exact(b, M, N, K, tile_n):
+    A, B = synthetic.operands(M, N, K, "int4", seed=M * 7 + N * 13 + K)
+    C, dC = run_gemm(b, A, B, tile_n=tile_n)
+    check_exact(C.numpy(), ref_of(A, B))
+    assert dC.outside_untouched()
+
+
+@pytest.mark.parametrize("M,N,K", RAGGED)
+def test_ragged_random(b, M, N, K):
+    A, B = synthetic.operands(M, N, K, "normal", seed=M + N + K)
+    C, dC = run_gemm(b, A, B)
+    check_tolerance(C.numpy(), ref_of(A, B), K)
+    assert dC.outside_untouched()
+
+
+@pytest.mark.parametrize("pad", [(8, 0, 0), (0, 16, 4), (24, 8, 12)])
+def test_padded_leading_dimensions(b, pad):
+    M, N, K = 200, 136, 300
+    A, B = synthetic.operands(M, N, K, "int4", seed=5)
+    C, dC = run_gemm(b, A, B, lda=304 + pad[0], ldb=136 + pad[1], ldc=136 + pad[2])
+    check_exact(C.numpy(), ref_of(A, B))
+    assert dC.outside_untouched()
+
+
+def test_K_zero_writes_zeros(b):
+    M, N = 70, 90
+    A = torch.zeros((M, 0), dtype=torch.float16)
+    B = torch.zeros((0, N), dtype=torch.float16)
+    C, dC = run_gemm(b, A, B)
+    assert torch.equal(C, torch.zeros(M, N))
+    assert dC.outside_untouched()
+
+
+def test_identity_copies_B(b):
+    K, N = 256, 200
+    _, B = synthetic.operands(K, N, K, "normal", seed=77)
+    A = torch.eye(K, dtype=torch.float16)
+    C, _ = run_gemm(b, A, B)
+    assert torch.equal(C, B.float())
+
+
+def test_row_sum_special_case(b):
+    """N = 1 with B = ones: the pages' tiled row sum as a GEMM."""
+    M, K = 333, 1000
+    A, _ = synthetic.operands(M, 1, K, "uniform", seed=3)
+    B = torch.ones((K, 1), dtype=torch.float16)
+    C, _ = run_gemm(b, A, B)
+    check_tolerance(C.numpy(), ref_of(A, B), K)
+    x = torch.tensor([[1.0, 1.0, 1.0], [1.0, 1.0, 1.0]], dtype=torch.float16)
+    C, _ = run_gemm(b, x, torch.ones((3, 1), dtype=torch.float16))
+    assert C[:, 0].tolist() == [3.0, 3.0]
+
+
+def test_all_ones_give_K(b):
+    for (M, N, K) in [(64, 128, 128), (256, 256, 65536)]:
+        A = torch.ones((M, K), dtype=torch.float16)
+        B = torch.ones((K, N), dtype=torch.float16)
+        C, _ = run_gemm(b, A, B)
+        assert bool((C == K).all()), (M, N, K)
+
+
+def test_subnormal_inputs_are_not_flushed(b):
+    M = K = 128
+    N = 64
+    rng = np.random.default_rng(1)
+    bits = rng.integers(1, 1024, size=(M, K)).astype(np.uint16)
+    A = torch.from_numpy(bits.view(np.float16).copy())
+    B = torch.zeros((K, N), dtype=torch.float16)
+    B[:N, :N] = torch.eye(N, dtype=torch.float16)
+    C, _ = run_gemm(b, A, B)
+    assert torch.equal(C, A[:, :N].float())
+
+
+def test_batched(b):
+    for (M, N, K) in [(64, 128, 128), (1000, 1000, 1000)]:
+        batch = 3
+        A, B = synthetic.operands(M, N, K, "int4", seed=11, batch=batch)
+        lda, ldb, ldc = -(-K // 8) * 8, -(-N // 8) * 8, -(-N // 4) * 4
+        # gaps between batches (strides larger than one matrix)
+        C, dC = run_gemm(b, A, B, batch=batch, lda=lda, ldb=ldb, ldc=ldc,
+                         sA=M * lda + 64, sB=K * ldb + 128, sC=M * ldc + 36)
+        for i in range(batch):
+            check_exact(C[i].numpy(), ref_of(A[i], B[i]))
+        assert dC.outside_untouched()
+
+
+def test_batched_random_with_split(b):
+    M, N, K, batch = 256, 192, 8192, 2
+    A, B = synthetic.operands(M, N, K, "uniform", seed=12, batch=batch)
+    C, _ = run_gemm(b, A, B, batch=batch, split_k=5)
+    for i in range(batch):
+        check_tolerance(C[i].numpy(), ref_of(A[i], B[i]), K)
+
+
+def test_results_are_reproducible(b):
+    w = WORKLOADS["gemm_1000x1000x1000_normal"]
+    A, B = synthetic.workload_operands(w)
+    C1, _ = run_gemm(b, A, B)
+    C2, _ = run_gemm(b, A, B)
+    assert torch.equal(C1, C2)
+
+
+def test_non_default_stream(b):
+    A, B = synthetic.operands(300, 200, 500, "int4", seed=9)
+    s = torch.cuda.Stream()
+    C, _ = run_gemm(b, A, B, stream=s)
+    check_exact(C.numpy(), ref_of(A, B))
+
+
+def test_torch_convenience_wrapper(b):
+    A, B = synthetic.operands(190, 210, 330, "int4", seed=10)
+    out = b.gemm(A.cuda(), B.cuda())
+    torch.cuda.synchronize()
+    check_exact(out.cpu().numpy(), ref_of(A, B))
+
+
+# ---------------------------------------------------------------- device-side argument checks
+
+def test_host_pointer_rejected(b):
+    A = torch.zeros((64, 64), dtype=torch.float16)  # pageable host memory
+    dB = torch.zeros((64, 64), dtype=torch.float16, device="cuda")
+    dC = torch.zeros((64, 64), dtype=torch.float32, device="cuda")
+    st = b.gemm_f16_f32acc(A.data_ptr(), dB.data_ptr(), dC.data_ptr(), 64, 64, 64, 64, 64, 64, 0)
+    assert st == b.GEMM_ERR_INVALID_VALUE
+
+
+def test_allocation_too_small_rejected(b):
+    dA = torch.zeros((64 * 64,), dtype=torch.float16, device="cuda")
+    dB = torch.zeros((64 * 64,), dtype=torch.float16, device="cuda")
+    dC = torch.zeros((64 * 64,), dtype=torch.float32, device="cuda")
+    # claims 1 << 30 rows of A: far beyond the allocation
+    st = b.gemm_f16_f32acc(dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), 64, 64, 1 << 28, 1 << 28,
+                           64, 64, 0)
+    assert st == b.GEMM_ERR_INVALID_VALUE

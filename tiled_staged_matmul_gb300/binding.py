@@ -1,0 +1,201 @@
+"""ctypes binding of the C ABI in ``include/tsm_gemm.h``.
+
+Argument marshalling only: every step of the GEMM runs in ``libtsm_gemm.so``.
+Importing this module loads the library and raises ``ImportError`` when it
+has not been built -- there is no fallback path.
+
+The raw functions keep the C names (``gemm_f16_f32acc`` ...) and take device
+pointers as integers.  ``gemm`` and ``gemm_host`` are conveniences over torch
+tensors: torch only provides the memory and the stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .csrc import build as _build
+
+LIB_PATH = _build.LIB_PATH
+
+GEMM_OK = 0
+GEMM_ERR_INVALID_VALUE = 1
+GEMM_ERR_MISALIGNED = 2
+GEMM_ERR_ALIAS = 3
+GEMM_ERR_UNSUPPORTED_DEVICE = 4
+GEMM_ERR_CUDA = 5
+GEMM_ERR_DEVICE_TIMEOUT = 6
+
+
+class GemmOptions(ctypes.Structure):
+    _fields_ = [("split_k", ctypes.c_int32), ("tile_n", ctypes.c_int32),
+                ("timeout_ms", ctypes.c_int32), ("inject_stall", ctypes.c_int32)]
+
+
+class GemmPlanInfo(ctypes.Structure):
+    _fields_ = [("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32),
+                ("tile_k", ctypes.c_int32), ("stages", ctypes.c_int32),
+                ("split_k", ctypes.c_int32), ("tiles_m", ctypes.c_int32),
+                ("tiles_n", ctypes.c_int32), ("k_blocks", ctypes.c_int32),
+                ("units", ctypes.c_int64), ("grid", ctypes.c_int32),
+                ("group_m", ctypes.c_int32), ("stage_bytes", ctypes.c_int64),
+                ("smem_bytes", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64)]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{gemm_status_string(status)}: {message}")
+        self.status = status
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build the CUDA library first "
+            "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(LIB_PATH)
+    i64, i32, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
+    lib.gemm_f16_f32acc.restype = ctypes.c_int
+    lib.gemm_f16_f32acc.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, vp]
+    lib.gemm_f16_f32acc_batched.restype = ctypes.c_int
+    lib.gemm_f16_f32acc_batched.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64,
+                                            i64, i64, i64, i64, vp]
+    lib.gemm_f16_f32acc_opts.restype = ctypes.c_int
+    lib.gemm_f16_f32acc_opts.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64,
+                                         i64, i64, i64, i64, ctypes.POINTER(GemmOptions), vp]
+    lib.gemm_plan.restype = ctypes.c_int
+    lib.gemm_plan.argtypes = [i64, i64, i64, i64, ctypes.POINTER(GemmOptions), i32,
+                              ctypes.POINTER(GemmPlanInfo)]
+    lib.gemm_get_device_status.restype = ctypes.c_int
+    lib.gemm_get_device_status.argtypes = [vp]
+    lib.gemm_last_error_string.restype = ctypes.c_char_p
+    lib.gemm_last_error_string.argtypes = []
+    lib.gemm_status_string.restype = ctypes.c_char_p
+    lib.gemm_status_string.argtypes = [ctypes.c_int]
+    lib.gemm_version.restype = ctypes.c_int32
+    lib.gemm_version.argtypes = []
+    return lib
+
+
+_lib = _load()
+
+
+def _opts(split_k=0, tile_n=0, timeout_ms=0, inject_stall=0):
+    return GemmOptions(int(split_k), int(tile_n), int(timeout_ms), int(inject_stall))
+
+
+# ------------------------------------------------------------------ raw C names
+
+def gemm_f16_f32acc(A, B, C, M, N, K, lda, ldb, ldc, stream=0) -> int:
+    return _lib.gemm_f16_f32acc(A, B, C, M, N, K, lda, ldb, ldc, stream)
+
+
+def gemm_f16_f32acc_batched(A, B, C, M, N, K, lda, ldb, ldc, strideA, strideB, strideC,
+                            batch, stream=0) -> int:
+    return _lib.gemm_f16_f32acc_batched(A, B, C, M, N, K, lda, ldb, ldc, strideA, strideB,
+                                        strideC, batch, stream)
+
+
+def gemm_f16_f32acc_opts(A, B, C, M, N, K, lda, ldb, ldc, strideA, strideB, strideC, batch,
+                         opts: GemmOptions | None = None, stream=0) -> int:
+    p = ctypes.byref(opts) if opts is not None else None
+    return _lib.gemm_f16_f32acc_opts(A, B, C, M, N, K, lda, ldb, ldc, strideA, strideB,
+                                     strideC, batch, p, stream)
+
+
+def gemm_plan(M, N, K, batch=1, opts: GemmOptions | None = None, num_sms=0) -> dict:
+    info = GemmPlanInfo()
+    p = ctypes.byref(opts) if opts is not None else None
+    st = _lib.gemm_plan(M, N, K, batch, p, num_sms, ctypes.byref(info))
+    if st != GEMM_OK:
+        raise GemmError(st, gemm_last_error_string())
+    return info.as_dict()
+
+
+def gemm_get_device_status(stream=0) -> int:
+    return _lib.gemm_get_device_status(stream)
+
+
+def gemm_last_error_string() -> str:
+    return _lib.gemm_last_error_string().decode()
+
+
+def gemm_status_string(status: int) -> str:
+    return _lib.gemm_status_string(int(status)).decode()
+
+
+def gemm_version() -> int:
+    return _lib.gemm_version()
+
+
+def check(status: int) -> None:
+    if status != GEMM_OK:
+        raise GemmError(status, gemm_last_error_string())
+
+
+# ------------------------------------------------------------------ torch conveniences
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def gemm(A, B, out=None, *, split_k=0, tile_n=0, timeout_ms=0, inject_stall=0, stream=None):
+    """``out = A @ B`` for f16 CUDA tensors A (M x K) and B (K x N), f32 out.
+
+    3-D tensors (batch x M x K, batch x K x N) run as one batched call.  Rows
+    may be padded (``stride(-2) >= size(-1)``) but the last stride must be 1.
+    Returns ``out`` (allocated with ``torch.empty`` when not given)."""
+    import torch
+    if A.dtype != torch.float16 or B.dtype != torch.float16:
+        raise TypeError("A and B must be torch.float16")
+    batched = A.dim() == 3
+    if A.dim() != B.dim() or A.dim() not in (2, 3):
+        raise ValueError("A and B must both be 2-D or both 3-D")
+    M, K = A.shape[-2], A.shape[-1]
+    K2, N = B.shape[-2], B.shape[-1]
+    if K != K2:
+        raise ValueError(f"inner sizes differ: {K} vs {K2}")
+    batch = A.shape[0] if batched else 1
+    if batched and B.shape[0] != batch:
+        raise ValueError("batch sizes differ")
+    if out is None:
+        shape = (batch, M, N) if batched else (M, N)
+        out = torch.empty(shape, dtype=torch.float32, device=A.device)
+    if out.dtype != torch.float32:
+        raise TypeError("out must be torch.float32")
+    for t, name in ((A, "A"), (B, "B"), (out, "out")):
+        if t.numel() and t.stride(-1) != 1:
+            raise ValueError(f"{name} must have a unit last stride")
+    lda = A.stride(-2) if M > 1 else max(K, 1)
+    ldb = B.stride(-2) if K > 1 else max(N, 1)
+    ldc = out.stride(-2) if M > 1 else max(N, 1)
+    sA = A.stride(0) if batched else 0
+    sB = B.stride(0) if batched else 0
+    sC = out.stride(0) if batched else 0
+    opts = _opts(split_k, tile_n, timeout_ms, inject_stall)
+    st = gemm_f16_f32acc_opts(A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K, lda, ldb,
+                              ldc, sA, sB, sC, batch, opts, _stream_handle(stream))
+    check(st)
+    return out
+
+
+def gemm_host(A_host, B_host, C_host, dA, dB, dC, stream=None):
+    """End-to-end call from host memory: copy A and B (pinned CPU f16
+    tensors) into the device buffers dA and dB, run the GEMM into dC, copy dC
+    back into C_host (pinned CPU f32).  All on one stream, asynchronously;
+    synchronise the stream before reading C_host."""
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    with torch.cuda.stream(s):
+        dA.copy_(A_host, non_blocking=True)
+        dB.copy_(B_host, non_blocking=True)
+        gemm(dA, dB, dC, stream=s)
+        C_host.copy_(dC, non_blocking=True)
+    return C_host

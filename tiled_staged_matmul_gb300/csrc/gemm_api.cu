@@ -1,0 +1,551 @@
+// gemm_api.cu -- host side of the C ABI declared in include/tsm_gemm.h:
+// argument checks, the planner (tile width, ring depth, split-K factor,
+// grid), tensor-map encoding, the split-K workspace and the launches.
+//
+// The planner is the GB300 counterpart of the pages' footprint check and
+// K_TILE choice ("The PTSS Cliff: A Kernel That Won't Build", sections "The
+// SLM Footprint", "Choosing K_TILE" and "The Four Gates"): the K depth of a
+// staged block is fixed at 64 (one 128-byte swizzle row of f16), the ring
+// takes as many A+B blocks as fit the 227 KiB shared-memory budget next to
+// the epilogue's staging buffers, and the tile width and split factor are
+// chosen so that the persistent grid fills the SMs.  Unlike the pages' pass
+// there is no "decline" outcome: ragged K is handled by zero fill rather
+// than by a divisibility gate.
+#include "../../include/tsm_gemm.h"
+#include "gemm_internal.h"
+
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+namespace tsm {
+namespace {
+
+thread_local std::string g_last_error;
+
+gemm_status_t fail(gemm_status_t st, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+gemm_status_t fail_cuda(cudaError_t e, const char *what)
+{
+    return fail(GEMM_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kInt32Max = 2147483647;
+
+// ------------------------------------------------------------- driver entry points
+
+struct Driver {
+    PFN_cuTensorMapEncodeTiled_v12000 encode_tiled = nullptr;
+    PFN_cuMemGetAddressRange_v3020 get_address_range = nullptr;
+    bool loaded = false;
+    std::string error;
+};
+
+Driver &driver()
+{
+    static Driver d;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q1 = cudaDriverEntryPointSymbolNotFound;
+        cudaDriverEntryPointQueryResult q2 = cudaDriverEntryPointSymbolNotFound;
+        void *f1 = nullptr, *f2 = nullptr;
+        cudaError_t e1 =
+            cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f1, 12000, cudaEnableDefault, &q1);
+        cudaError_t e2 =
+            cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &f2, 12000, cudaEnableDefault, &q2);
+        if (e1 != cudaSuccess || q1 != cudaDriverEntryPointSuccess || !f1) {
+            d.error = "cuTensorMapEncodeTiled is not available from the driver";
+            return;
+        }
+        d.encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f1);
+        if (e2 == cudaSuccess && q2 == cudaDriverEntryPointSuccess && f2)
+            d.get_address_range = reinterpret_cast<PFN_cuMemGetAddressRange_v3020>(f2);
+        d.loaded = true;
+    });
+    return d;
+}
+
+// ------------------------------------------------------------- per-device state
+
+struct DeviceState {
+    bool ready = false;
+    int sms = 0;
+    int cc_major = 0, cc_minor = 0;
+    int smem_optin = 0;
+    bool attrs_set[3] = {false, false, false};  // tile_n 64, 128, 256
+    cudaMemPool_t pool = nullptr;
+    uint32_t *status = nullptr;
+};
+
+DeviceState g_devices[kMaxDevices];
+std::mutex g_device_mutex;
+
+gemm_status_t device_state(int dev, DeviceState **out)
+{
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(GEMM_ERR_INVALID_VALUE, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_device_mutex);
+    DeviceState &s = g_devices[dev];
+    if (!s.ready) {
+        cudaError_t e;
+        if ((e = cudaDeviceGetAttribute(&s.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return fail_cuda(e, "cudaDeviceGetAttribute(SM count)");
+        cudaDeviceGetAttribute(&s.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&s.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+        cudaDeviceGetAttribute(&s.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (s.cc_major != 10 || s.cc_minor != 3)
+            return fail(GEMM_ERR_UNSUPPORTED_DEVICE,
+                        "device %d has compute capability %d.%d; this library is built for 10.3 "
+                        "(GB300, sm_103a) only",
+                        dev, s.cc_major, s.cc_minor);
+        if ((e = device_status_word(&s.status)) != cudaSuccess)
+            return fail_cuda(e, "cudaGetSymbolAddress(status word)");
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        if ((e = cudaMemPoolCreate(&s.pool, &props)) != cudaSuccess)
+            return fail_cuda(e, "cudaMemPoolCreate(split-K workspace pool)");
+        uint64_t keep = UINT64_MAX;  // keep freed workspace for the next call
+        cudaMemPoolSetAttribute(s.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+        s.ready = true;
+    }
+    *out = &s;
+    return GEMM_OK;
+}
+
+int tile_index(int tile_n) { return tile_n == 64 ? 0 : tile_n == 128 ? 1 : 2; }
+
+// ------------------------------------------------------------- argument checks
+
+struct Problem {
+    const uint16_t *A;
+    const uint16_t *B;
+    float *C;
+    int64_t M, N, K, lda, ldb, ldc, sA, sB, sC, batch;
+};
+
+// Bytes spanned by `batch` matrices of `rows` x `cols` elements of `elem`
+// bytes, row stride `ld`, batch stride `stride` (all in elements).
+int64_t span_bytes(int64_t batch, int64_t stride, int64_t rows, int64_t ld, int64_t cols, int64_t elem)
+{
+    if (batch <= 0 || rows <= 0 || cols <= 0)
+        return 0;
+    return ((batch - 1) * stride + (rows - 1) * ld + cols) * elem;
+}
+
+bool overlaps(const void *p, int64_t pn, const void *q, int64_t qn)
+{
+    if (pn <= 0 || qn <= 0)
+        return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(p), a1 = a0 + uint64_t(pn);
+    const uintptr_t b0 = reinterpret_cast<uintptr_t>(q), b1 = b0 + uint64_t(qn);
+    return a0 < b1 && b0 < a1;
+}
+
+// Checks that need no GPU.  Sets *trivial when there is nothing to compute.
+gemm_status_t check_host(const Problem &pr, bool *trivial)
+{
+    *trivial = false;
+    if (pr.M < 0 || pr.N < 0 || pr.K < 0 || pr.batch < 0)
+        return fail(GEMM_ERR_INVALID_VALUE, "negative size: M=%lld N=%lld K=%lld batch=%lld",
+                    (long long)pr.M, (long long)pr.N, (long long)pr.K, (long long)pr.batch);
+    if (pr.M > kInt32Max || pr.N > kInt32Max || pr.K > kInt32Max || pr.batch > kInt32Max)
+        return fail(GEMM_ERR_INVALID_VALUE, "M, N, K and batch must be below 2^31");
+    if (pr.M == 0 || pr.N == 0 || pr.batch == 0) {
+        *trivial = true;
+        return GEMM_OK;
+    }
+    if (!pr.C)
+        return fail(GEMM_ERR_INVALID_VALUE, "C is NULL");
+    if (pr.ldc < pr.N)
+        return fail(GEMM_ERR_INVALID_VALUE, "ldc (%lld) < N (%lld)", (long long)pr.ldc, (long long)pr.N);
+    if (pr.K > 0) {
+        if (!pr.A || !pr.B)
+            return fail(GEMM_ERR_INVALID_VALUE, "A or B is NULL");
+        if (pr.lda < pr.K)
+            return fail(GEMM_ERR_INVALID_VALUE, "lda (%lld) < K (%lld)", (long long)pr.lda, (long long)pr.K);
+        if (pr.ldb < pr.N)
+            return fail(GEMM_ERR_INVALID_VALUE, "ldb (%lld) < N (%lld)", (long long)pr.ldb, (long long)pr.N);
+    }
+    if (pr.batch > 1 && (pr.sC <= 0 || (pr.K > 0 && (pr.sA <= 0 || pr.sB <= 0))))
+        return fail(GEMM_ERR_INVALID_VALUE, "batch strides must be positive when batch > 1");
+    // 16-byte rules of the tensor-memory accelerator: base address and every
+    // row / batch pitch.
+    if ((reinterpret_cast<uintptr_t>(pr.C) & 15u) || (pr.ldc % 4) || (pr.batch > 1 && pr.sC % 4))
+        return fail(GEMM_ERR_MISALIGNED,
+                    "C must be 16-byte aligned with ldc and strideC multiples of 4 elements");
+    if (pr.K > 0) {
+        if ((reinterpret_cast<uintptr_t>(pr.A) & 15u) || (pr.lda % 8) || (pr.batch > 1 && pr.sA % 8))
+            return fail(GEMM_ERR_MISALIGNED,
+                        "A must be 16-byte aligned with lda and strideA multiples of 8 elements");
+        if ((reinterpret_cast<uintptr_t>(pr.B) & 15u) || (pr.ldb % 8) || (pr.batch > 1 && pr.sB % 8))
+            return fail(GEMM_ERR_MISALIGNED,
+                        "B must be 16-byte aligned with ldb and strideB multiples of 8 elements");
+    }
+    if (pr.batch > 1 && pr.sC < (pr.M - 1) * pr.ldc + pr.N)
+        return fail(GEMM_ERR_ALIAS, "batches of C overlap (strideC too small)");
+    const int64_t bytesC = span_bytes(pr.batch, pr.sC, pr.M, pr.ldc, pr.N, 4);
+    if (pr.K > 0) {
+        const int64_t bytesA = span_bytes(pr.batch, pr.sA, pr.M, pr.lda, pr.K, 2);
+        const int64_t bytesB = span_bytes(pr.batch, pr.sB, pr.K, pr.ldb, pr.N, 2);
+        if (overlaps(pr.C, bytesC, pr.A, bytesA) || overlaps(pr.C, bytesC, pr.B, bytesB))
+            return fail(GEMM_ERR_ALIAS, "C overlaps A or B");
+    }
+    return GEMM_OK;
+}
+
+// The pointer is device memory of `dev` and its allocation covers `bytes`.
+gemm_status_t check_device_pointer(const void *p, int64_t bytes, int dev, const char *name)
+{
+    cudaPointerAttributes at = {};
+    cudaError_t e = cudaPointerGetAttributes(&at, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(GEMM_ERR_INVALID_VALUE, "%s is not a CUDA pointer (%s)", name, cudaGetErrorName(e));
+    }
+    if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged)
+        return fail(GEMM_ERR_INVALID_VALUE, "%s is not device memory", name);
+    if (at.device != dev)
+        return fail(GEMM_ERR_INVALID_VALUE, "%s lives on device %d, the current device is %d", name,
+                    at.device, dev);
+    Driver &d = driver();
+    if (d.get_address_range) {
+        CUdeviceptr base = 0;
+        size_t size = 0;
+        if (d.get_address_range(&base, &size, CUdeviceptr(reinterpret_cast<uintptr_t>(p))) == CUDA_SUCCESS) {
+            const uint64_t end = uint64_t(reinterpret_cast<uintptr_t>(p)) + uint64_t(bytes);
+            if (end > uint64_t(base) + uint64_t(size))
+                return fail(GEMM_ERR_INVALID_VALUE,
+                            "%s: the allocation ends %llu bytes before the last element", name,
+                            (unsigned long long)(end - (uint64_t(base) + uint64_t(size))));
+        }
+    }
+    return GEMM_OK;
+}
+
+// ------------------------------------------------------------- planner
+
+int ceil_div(int64_t a, int64_t b) { return int((a + b - 1) / b); }
+
+gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const gemm_options_t *o,
+                        int sms, gemm_plan_info_t *pl)
+{
+    if (sms <= 0)
+        return fail(GEMM_ERR_INVALID_VALUE, "SM count must be positive");
+    memset(pl, 0, sizeof *pl);
+    const int req_n = o ? o->tile_n : 0;
+    if (req_n != 0 && req_n != 64 && req_n != 128 && req_n != 256)
+        return fail(GEMM_ERR_INVALID_VALUE, "tile_n must be 0, 64, 128 or 256 (got %d)", req_n);
+    const int req_s = o ? o->split_k : 0;
+    if (req_s < 0)
+        return fail(GEMM_ERR_INVALID_VALUE, "split_k must be >= 0");
+    const int tiles_m = ceil_div(std::max<int64_t>(M, 1), kTileM);
+    const int k_blocks = ceil_div(std::max<int64_t>(K, 1), kTileK);
+    auto tiles_of = [&](int bn) { return int64_t(tiles_m) * ceil_div(std::max<int64_t>(N, 1), bn) * batch; };
+
+    int bn = req_n;
+    int split = 1;
+    if (bn == 0) {
+        // Long K on a small output: too few tiles to fill the SMs, so the K
+        // range is split (the pages' "long K" case; see the split rule below).
+        const bool long_k = tiles_of(256) * 2 <= sms && k_blocks >= 16;
+        if (long_k) {
+            bn = 128;
+        } else {
+            // Fewest waves of persistent CTAs, weighted by the relative cost of
+            // a narrow tile (more shared-memory traffic per flop).
+            double best = 0;
+            for (int cand : {256, 128, 64}) {
+                const double w = double((tiles_of(cand) + sms - 1) / sms) * cand *
+                                 (cand == 256 ? 1.0 : cand == 128 ? 1.1 : 1.3);
+                if (bn == 0 || w < best) {
+                    best = w;
+                    bn = cand;
+                }
+            }
+        }
+    }
+    const int64_t tiles = tiles_of(bn);
+    if (req_s > 0) {
+        split = std::min(req_s, k_blocks);
+    } else if (K > 0 && tiles < sms) {
+        // Enough K ranges to put one unit on every SM, at least 4 k-blocks each.
+        const int64_t by_sms = sms / tiles;
+        const int64_t by_depth = k_blocks / 4;
+        split = int(std::max<int64_t>(1, std::min(by_sms, by_depth)));
+    }
+    if (K == 0)
+        split = 1;
+    const SmemBudget sb = smem_budget(bn);
+    pl->tile_m = kTileM;
+    pl->tile_n = bn;
+    pl->tile_k = kTileK;
+    pl->stages = sb.stages;
+    pl->split_k = split;
+    pl->tiles_m = tiles_m;
+    pl->tiles_n = ceil_div(std::max<int64_t>(N, 1), bn);
+    pl->k_blocks = k_blocks;
+    pl->units = tiles * split;
+    if (pl->units > kInt32Max)
+        return fail(GEMM_ERR_INVALID_VALUE, "problem has too many tiles");
+    pl->grid = int(std::min<int64_t>(pl->units, sms));
+    pl->group_m = std::min(tiles_m, 8);
+    pl->stage_bytes = sb.stage_bytes;
+    pl->smem_bytes = sb.smem_bytes;
+    const int64_t ldw = (N + 3) / 4 * 4;
+    pl->workspace_bytes = split > 1 ? batch * int64_t(split) * M * ldw * 4 : 0;
+    return GEMM_OK;
+}
+
+// ------------------------------------------------------------- tensor maps
+
+gemm_status_t encode_3d(CUtensorMap *map, CUtensorMapDataType dt, int elem, const void *base,
+                        int64_t cols, int64_t rows, int64_t mats, int64_t ld, int64_t stride,
+                        uint32_t box_cols, uint32_t box_rows, CUtensorMapL2promotion promo,
+                        const char *name)
+{
+    Driver &d = driver();
+    if (!d.loaded)
+        return fail(GEMM_ERR_CUDA, "%s", d.error.c_str());
+    const cuuint64_t dims[3] = {cuuint64_t(cols), cuuint64_t(rows), cuuint64_t(mats)};
+    const cuuint64_t strides[2] = {cuuint64_t(ld) * elem, cuuint64_t(stride) * elem};
+    const cuuint32_t box[3] = {box_cols, box_rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = d.encode_tiled(map, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, promo,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(GEMM_ERR_INVALID_VALUE, "tensor map for %s rejected (CUresult %d)", name, int(r));
+    return GEMM_OK;
+}
+
+// ------------------------------------------------------------- the call
+
+int64_t timeout_ns_for(const gemm_options_t *o, const gemm_plan_info_t &pl)
+{
+    const int64_t base_ms = (o && o->timeout_ms > 0) ? o->timeout_ms : 2000;
+    const int64_t kb_per_unit = (pl.k_blocks + pl.split_k - 1) / pl.split_k;
+    return base_ms * 1000000ll + kb_per_unit * 10000ll;
+}
+
+gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t stream)
+{
+    bool trivial = false;
+    gemm_status_t st = check_host(pr, &trivial);
+    if (st != GEMM_OK || trivial)
+        return st;
+
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return fail_cuda(e, "cudaGetDevice");
+    DeviceState *ds = nullptr;
+    if ((st = device_state(dev, &ds)) != GEMM_OK)
+        return st;
+
+    const int64_t bytesC = span_bytes(pr.batch, pr.sC, pr.M, pr.ldc, pr.N, 4);
+    if ((st = check_device_pointer(pr.C, bytesC, dev, "C")) != GEMM_OK)
+        return st;
+    const int32_t M = int32_t(pr.M), N = int32_t(pr.N), batch = int32_t(pr.batch);
+    const int64_t sC = pr.batch > 1 ? pr.sC : int64_t(pr.M) * pr.ldc;
+
+    if (pr.K == 0) {
+        const int64_t total = int64_t(M) * N * batch;
+        const int grid = int(std::min<int64_t>((total + 255) / 256, int64_t(ds->sms) * 8));
+        if ((e = launch_zero_fill(pr.C, M, N, batch, pr.ldc, sC, grid, stream)) != cudaSuccess)
+            return fail_cuda(e, "zero-fill launch");
+        return GEMM_OK;
+    }
+
+    if ((st = check_device_pointer(pr.A, span_bytes(pr.batch, pr.sA, pr.M, pr.lda, pr.K, 2), dev, "A")) != GEMM_OK)
+        return st;
+    if ((st = check_device_pointer(pr.B, span_bytes(pr.batch, pr.sB, pr.K, pr.ldb, pr.N, 2), dev, "B")) != GEMM_OK)
+        return st;
+
+    gemm_plan_info_t pl;
+    if ((st = make_plan(pr.M, pr.N, pr.K, pr.batch, o, ds->sms, &pl)) != GEMM_OK)
+        return st;
+    if (ds->smem_optin < pl.smem_bytes)
+        return fail(GEMM_ERR_UNSUPPORTED_DEVICE, "device allows %d bytes of shared memory per block, the kernel needs %lld",
+                    ds->smem_optin, (long long)pl.smem_bytes);
+    const int ti = tile_index(pl.tile_n);
+    if (!ds->attrs_set[ti]) {
+        if ((e = set_kernel_attributes(pl.tile_n)) != cudaSuccess)
+            return fail_cuda(e, "cudaFuncSetAttribute(max dynamic shared memory)");
+        ds->attrs_set[ti] = true;
+    }
+
+    const int64_t sA = pr.batch > 1 ? pr.sA : int64_t(pr.M) * pr.lda;
+    const int64_t sB = pr.batch > 1 ? pr.sB : int64_t(pr.K) * pr.ldb;
+    alignas(64) CUtensorMap map_a, map_b, map_out;
+    if ((st = encode_3d(&map_a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, pr.A, pr.K, pr.M, pr.batch,
+                        pr.lda, sA, kTileK, kTileM, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "A")) != GEMM_OK)
+        return st;
+    if ((st = encode_3d(&map_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, pr.B, pr.N, pr.K, pr.batch,
+                        pr.ldb, sB, 64, kTileK, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "B")) != GEMM_OK)
+        return st;
+
+    KernelParams kp = {};
+    kp.M = M;
+    kp.N = N;
+    kp.K = int32_t(pr.K);
+    kp.tiles_m = pl.tiles_m;
+    kp.tiles_n = pl.tiles_n;
+    kp.k_blocks = pl.k_blocks;
+    kp.split_k = pl.split_k;
+    kp.batch = batch;
+    kp.group_m = pl.group_m;
+    kp.inject_stall = (o && o->inject_stall) ? 1 : 0;
+    kp.num_units = pl.units;
+    kp.timeout_ns = uint64_t(timeout_ns_for(o, pl));
+    kp.status = ds->status;
+
+    if (pl.split_k == 1) {
+        if ((st = encode_3d(&map_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pr.C, pr.N, pr.M, pr.batch,
+                            pr.ldc, sC, 32, 32, CU_TENSOR_MAP_L2_PROMOTION_NONE, "C")) != GEMM_OK)
+            return st;
+        if ((e = launch_tcgen05_gemm(pl.tile_n, map_a, map_b, map_out, kp, pl.grid, stream)) != cudaSuccess)
+            return fail_cuda(e, "GEMM kernel launch");
+        return GEMM_OK;
+    }
+
+    // Split-K: partials W[b*S + s] (M x ldw f32 each), then the fixed-order sum.
+    const int64_t ldw = (pr.N + 3) / 4 * 4;
+    void *ws = nullptr;
+    if ((e = cudaMallocFromPoolAsync(&ws, size_t(pl.workspace_bytes), ds->pool, stream)) != cudaSuccess)
+        return fail_cuda(e, "split-K workspace allocation");
+    st = encode_3d(&map_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ws, pr.N, pr.M,
+                   pr.batch * pl.split_k, ldw, int64_t(pr.M) * ldw, 32, 32,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, "split-K workspace");
+    if (st == GEMM_OK) {
+        if ((e = launch_tcgen05_gemm(pl.tile_n, map_a, map_b, map_out, kp, pl.grid, stream)) != cudaSuccess)
+            st = fail_cuda(e, "GEMM kernel launch");
+    }
+    if (st == GEMM_OK) {
+        const int64_t threads = int64_t(M) * ((N + 3) / 4) * batch;
+        const int grid = int(std::min<int64_t>((threads + 255) / 256, int64_t(ds->sms) * 8));
+        if ((e = launch_splitk_reduce(static_cast<const float *>(ws), pr.C, M, N, pl.split_k, batch,
+                                      ldw, pr.ldc, sC, grid, stream)) != cudaSuccess)
+            st = fail_cuda(e, "split-K reduce launch");
+    }
+    cudaFreeAsync(ws, stream);
+    return st;
+}
+
+}  // namespace
+}  // namespace tsm
+
+using namespace tsm;
+
+extern "C" {
+
+gemm_status_t gemm_f16_f32acc(const uint16_t *A, const uint16_t *B, float *C, int64_t M, int64_t N,
+                              int64_t K, int64_t lda, int64_t ldb, int64_t ldc, gemm_stream_t stream)
+{
+    g_last_error.clear();
+    Problem pr{A, B, C, M, N, K, lda, ldb, ldc, 0, 0, 0, 1};
+    return run(pr, nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_f16_f32acc_batched(const uint16_t *A, const uint16_t *B, float *C, int64_t M,
+                                      int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                                      int64_t strideA, int64_t strideB, int64_t strideC,
+                                      int64_t batch, gemm_stream_t stream)
+{
+    g_last_error.clear();
+    Problem pr{A, B, C, M, N, K, lda, ldb, ldc, strideA, strideB, strideC, batch};
+    return run(pr, nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_f16_f32acc_opts(const uint16_t *A, const uint16_t *B, float *C, int64_t M,
+                                   int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                                   int64_t strideA, int64_t strideB, int64_t strideC, int64_t batch,
+                                   const gemm_options_t *opts, gemm_stream_t stream)
+{
+    g_last_error.clear();
+    Problem pr{A, B, C, M, N, K, lda, ldb, ldc, strideA, strideB, strideC, batch};
+    return run(pr, opts, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const gemm_options_t *opts,
+                        int32_t num_sms, gemm_plan_info_t *plan)
+{
+    g_last_error.clear();
+    if (!plan)
+        return fail(GEMM_ERR_INVALID_VALUE, "plan is NULL");
+    if (M < 0 || N < 0 || K < 0 || batch < 0 || M > kInt32Max || N > kInt32Max || K > kInt32Max ||
+        batch > kInt32Max)
+        return fail(GEMM_ERR_INVALID_VALUE, "sizes must be in [0, 2^31)");
+    int sms = num_sms;
+    if (sms <= 0) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess)
+            return fail_cuda(e, "cudaGetDevice");
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return fail_cuda(e, "cudaDeviceGetAttribute(SM count)");
+    }
+    return make_plan(M, N, K, std::max<int64_t>(batch, 1), opts, sms, plan);
+}
+
+gemm_status_t gemm_get_device_status(gemm_stream_t stream)
+{
+    g_last_error.clear();
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return fail_cuda(e, "cudaStreamSynchronize");
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess)
+        return fail_cuda(e, "cudaGetDevice");
+    DeviceState *ds = nullptr;
+    gemm_status_t st = device_state(dev, &ds);
+    if (st != GEMM_OK)
+        return st;
+    uint32_t word = 0;
+    if ((e = cudaMemcpy(&word, ds->status, sizeof word, cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return fail_cuda(e, "reading the status word");
+    if (word == 0)
+        return GEMM_OK;
+    const uint32_t zero = 0;
+    cudaMemcpy(ds->status, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    return fail(GEMM_ERR_DEVICE_TIMEOUT,
+                "a bounded device-side wait ran out (roles: %s%s%s%s); the output of that call is incomplete",
+                (word & kStatusProducer) ? "producer " : "", (word & kStatusMma) ? "mma " : "",
+                (word & kStatusEpilogue) ? "epilogue " : "", (word & kStatusDrain) ? "drain" : "");
+}
+
+const char *gemm_last_error_string(void) { return g_last_error.c_str(); }
+
+const char *gemm_status_string(gemm_status_t s)
+{
+    switch (s) {
+    case GEMM_OK: return "GEMM_OK";
+    case GEMM_ERR_INVALID_VALUE: return "GEMM_ERR_INVALID_VALUE";
+    case GEMM_ERR_MISALIGNED: return "GEMM_ERR_MISALIGNED";
+    case GEMM_ERR_ALIAS: return "GEMM_ERR_ALIAS";
+    case GEMM_ERR_UNSUPPORTED_DEVICE: return "GEMM_ERR_UNSUPPORTED_DEVICE";
+    case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA";
+    case GEMM_ERR_DEVICE_TIMEOUT: return "GEMM_ERR_DEVICE_TIMEOUT";
+    }
+    return "GEMM_ERR_UNKNOWN";
+}
+
+int32_t gemm_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,56 @@
+// gemm_internal.h -- what the host planner (gemm_api.cu) and the kernel
+// translation unit (gemm_kernels.cu) share.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace tsm {
+
+constexpr int kTileM = 128;  // rows of C per tile = TMEM lanes of one accumulator
+constexpr int kTileK = 64;   // K depth of one k-block: one 128-byte swizzle row of f16
+constexpr int kThreads = 192;  // warp 0 TMA producer, warp 1 MMA issuer, warps 2..5 epilogue
+
+// Bits of the device status word: which role's bounded wait ran out.
+constexpr uint32_t kStatusProducer = 1u;
+constexpr uint32_t kStatusMma = 2u;
+constexpr uint32_t kStatusEpilogue = 4u;
+constexpr uint32_t kStatusDrain = 8u;
+
+// Everything the persistent kernel needs besides its three tensor maps.
+struct KernelParams {
+    int32_t M, N, K;
+    int32_t tiles_m, tiles_n;
+    int32_t k_blocks;     // ceil(K / kTileK)
+    int32_t split_k;      // K ranges per tile (1 = the output map is C itself)
+    int32_t batch;
+    int32_t group_m;      // raster: tiles of M walked together
+    int32_t inject_stall; // test hook: the epilogue waits on a barrier nothing signals
+    int64_t num_units;    // batch * split_k * tiles_m * tiles_n
+    uint64_t timeout_ns;  // limit of every device-side wait
+    uint32_t *status;     // device status word (OR of kStatus* bits)
+};
+
+// Shared-memory budget of one CTA for a tile width (host and device agree).
+struct SmemBudget {
+    int stages;
+    int stage_bytes;
+    int smem_bytes;
+    int tmem_cols;
+};
+SmemBudget smem_budget(int tile_n);
+
+// Kernel-side entry points (defined in gemm_kernels.cu).
+cudaError_t set_kernel_attributes(int tile_n);
+cudaError_t launch_tcgen05_gemm(int tile_n, const CUtensorMap &map_a, const CUtensorMap &map_b,
+                                const CUtensorMap &map_out, const KernelParams &p, int grid,
+                                cudaStream_t stream);
+cudaError_t launch_splitk_reduce(const float *W, float *C, int32_t M, int32_t N, int32_t S,
+                                 int32_t batch, int64_t ldw, int64_t ldc, int64_t strideC,
+                                 int grid, cudaStream_t stream);
+cudaError_t launch_zero_fill(float *C, int32_t M, int32_t N, int32_t batch, int64_t ldc,
+                             int64_t strideC, int grid, cudaStream_t stream);
+cudaError_t device_status_word(uint32_t **ptr);
+
+}  // namespace tsm

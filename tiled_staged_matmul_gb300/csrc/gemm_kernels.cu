@@ -1,0 +1,530 @@
+// gemm_kernels.cu -- the sm_103a kernels of the K-tiled, operand-staged GEMM.
+//
+// The method ("The PTSS Cliff: A Kernel That Won't Build", sections "The
+// Idea: Stage in SLM, Tile K" and "The Pass, Step by Step"): instead of
+// holding whole operand tiles in registers, stage them in fast on-chip memory
+// and walk K in fixed-size chunks, carrying the accumulator across chunks.
+// On GB300 that becomes:
+//
+//   * staging: a ring of STAGES shared-memory slots, each holding one
+//     128 x 64 A tile and one 64 x BN B tile, filled by TMA from tensor maps
+//     whose extent masks out-of-range elements to zero ("Intel XPU Backend
+//     for Triton", section "Use Tensor Descriptors to load tl.dot arguments
+//     and save results");
+//   * the K_TILE loop: one 64-deep k-block per slot, four 128 x BN x 16
+//     tcgen05 MMAs per k-block, all accumulating into one f32 tile held in
+//     tensor memory (TMEM) -- the carried accumulator of the pages' loop;
+//   * mbarriers hand each slot from the TMA producer to the MMA issuer
+//     (full) and back (empty); two TMEM accumulators let the epilogue drain
+//     one tile while the next one accumulates;
+//   * the epilogue reads TMEM into registers, writes a swizzled 32 x 32 f32
+//     box to shared memory and stores it with TMA, clipped at M and N
+//     (the pages' descriptor store, same section);
+//   * split-K: a tile's K range may be cut into S contiguous pieces whose
+//     f32 partials go to a workspace; a second kernel sums them in ascending
+//     split order, so the result never depends on which CTA finished first
+//     ("A Dumb Triton Runtime Error", sections "What I ran" and "The Takeaway
+//     and the Final Fix": inter-CTA atomics need a zeroed output and change
+//     the rounding with the order).
+//
+// Every mbarrier wait is bounded in time.  A wait that runs out records a
+// bit in the device status word and the CTA winds down: it waits (bounded)
+// for its own TMA loads, MMAs and stores still in flight, frees its TMEM and
+// returns.  Nothing traps.
+#include "gemm_internal.h"
+#include "ptx.cuh"
+
+namespace tsm {
+
+__device__ uint32_t g_status_word;
+
+// ------------------------------------------------------------- tile config
+
+template <int BN>
+struct TileCfg {
+    static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
+    static constexpr int BM = kTileM;
+    static constexpr int BK = kTileK;
+    static constexpr int A_BYTES = BM * BK * 2;            // 16 KiB
+    static constexpr int B_BOX_BYTES = 64 * BK * 2;        // one 64-column box: 8 KiB
+    static constexpr int B_BOXES = BN / 64;
+    static constexpr int B_BYTES = B_BOXES * B_BOX_BYTES;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int EPI_WARPS = 4;
+    static constexpr int EPI_BUF_BYTES = 32 * 32 * 4;      // one 32 x 32 f32 box
+    static constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BUF_BYTES;
+    static constexpr int CTRL_BYTES = 1024;
+    static constexpr int ALIGN_SLACK = 1024;
+    static constexpr int SMEM_LIMIT = 232448;              // 227 KiB opt-in per block
+    static constexpr int STAGES_FIT =
+        (SMEM_LIMIT - ALIGN_SLACK - EPI_BYTES - CTRL_BYTES) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+    static_assert(STAGES >= 2, "the ring needs at least two stages");
+    static constexpr int SMEM_BYTES = ALIGN_SLACK + STAGES * STAGE_BYTES + EPI_BYTES + CTRL_BYTES;
+    // Two accumulators of BN f32 columns each (a power of two >= 32).
+    static constexpr uint32_t TMEM_COLS = 2 * BN;
+    static_assert(SMEM_BYTES > SMEM_LIMIT / 2, "one CTA per SM keeps TMEM allocation uncontended");
+};
+
+// Instruction descriptor of tcgen05.mma.kind::f16: D f32 (bits 4-5 = 1),
+// A and B f16 (bits 7-9, 10-12 = 0), A K-major (bit 15 = 0), B MN-major
+// (bit 16 = 1: B is row-major K x N, so N is contiguous), N >> 3 in bits
+// 17-22, M >> 4 in bits 24-28.
+template <int BN>
+__device__ __forceinline__ constexpr uint32_t mma_idesc()
+{
+    return (1u << 4) | (1u << 16) | (uint32_t(BN >> 3) << 17) | (uint32_t(kTileM >> 4) << 24);
+}
+
+// Shared-memory matrix descriptor fields common to both operands: 128-byte
+// swizzle (bits 61-63 = 2), descriptor version 1 (bits 46-48), 8-row groups
+// 1024 bytes apart (stride byte offset, bits 32-45, in 16-byte units).
+__device__ __forceinline__ uint64_t desc_common()
+{
+    return (uint64_t(1024 >> 4) << 32) | (uint64_t(1) << 46) | (uint64_t(2) << 61);
+}
+
+// A: K-major, one 128-byte row per M row.  The K=16 slice of an MMA lies
+// inside one swizzle row, so the leading byte offset is unused (set to 1).
+__device__ __forceinline__ uint64_t desc_a(uint32_t saddr)
+{
+    return desc_common() | (uint64_t(1) << 16) | uint64_t((saddr & 0x3FFFFu) >> 4);
+}
+
+// B: MN-major, each 64-column box is K rows of 128 bytes; boxes (64-column
+// atoms along N) are B_BOX_BYTES apart (leading byte offset).
+template <int BN>
+__device__ __forceinline__ uint64_t desc_b(uint32_t saddr)
+{
+    return desc_common() | (uint64_t(TileCfg<BN>::B_BOX_BYTES >> 4) << 16) |
+           uint64_t((saddr & 0x3FFFFu) >> 4);
+}
+
+// ------------------------------------------------------------- helpers
+
+struct Unit {
+    int32_t m0, n0;    // first row / column of the tile
+    int32_t z_in;      // batch index of A and B
+    int32_t z_out;     // third coordinate of the output map
+    int32_t kb0, kb1;  // k-block range [kb0, kb1)
+};
+
+// Work unit -> tile.  Units are ordered (batch, split) outermost, then the
+// tiles of one matrix in a grouped raster: group_m rows of tiles are walked
+// column by column, so CTAs running at the same time share A and B panels
+// in L2 ("Intel XPU Backend for Triton", section "Use Proper Type
+// Annotations": GROUP_SIZE_M in the GEMM signature).
+__device__ __forceinline__ Unit decode_unit(int64_t u, const KernelParams &p, int bn)
+{
+    const int64_t tiles = int64_t(p.tiles_m) * p.tiles_n;
+    const int64_t z = u / tiles;
+    const int64_t t = u - z * tiles;
+    const int32_t b = int32_t(z / p.split_k);
+    const int32_t s = int32_t(z - int64_t(b) * p.split_k);
+    const int64_t group = int64_t(p.group_m) * p.tiles_n;
+    const int64_t g = t / group;
+    const int32_t first_m = int32_t(g * p.group_m);
+    const int32_t rows_in_group = min(p.tiles_m - first_m, p.group_m);
+    const int64_t r = t - g * group;
+    Unit w;
+    w.m0 = (first_m + int32_t(r % rows_in_group)) * kTileM;
+    w.n0 = int32_t(r / rows_in_group) * bn;
+    w.z_in = b;
+    w.z_out = int32_t(z);  // == b when split_k == 1
+    w.kb0 = int32_t(int64_t(s) * p.k_blocks / p.split_k);
+    w.kb1 = int32_t(int64_t(s + 1) * p.k_blocks / p.split_k);
+    return w;
+}
+
+// Bounded mbarrier wait.  Returns false if the CTA's abort flag is raised
+// (when `honor_abort`) or if `timeout_ns` passes; a timeout raises the flag
+// and ORs `who` into the device status word.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
+                                             volatile uint32_t *abort_flag, uint64_t timeout_ns,
+                                             uint32_t *status, uint32_t who, bool honor_abort)
+{
+    if (ptx::mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (ptx::mbar_try_wait(bar, parity))
+            return true;
+        if ((it & 31u) == 0) {
+            if (honor_abort && *abort_flag)
+                return false;
+            if (ptx::globaltimer_ns() - t0 > timeout_ns) {
+                *abort_flag = 1u;
+                atomicOr(status, who);
+                return false;
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------- the GEMM
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    tsm_gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a,
+                            const __grid_constant__ CUtensorMap map_b,
+                            const __grid_constant__ CUtensorMap map_out, const KernelParams p)
+{
+    using Cfg = TileCfg<BN>;
+    constexpr int S = Cfg::STAGES;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;  // the 128-byte swizzle repeats every 1024 B
+    uint8_t *const base_ptr = smem_raw + (base - raw);
+    const uint32_t epi0 = base + S * Cfg::STAGE_BYTES;
+    const uint32_t ctrl = epi0 + Cfg::EPI_BYTES;
+    uint8_t *const ctrl_ptr = base_ptr + (ctrl - base);
+
+    // Control block: barriers (8 bytes each), then the TMEM address and the
+    // CTA's abort flag.
+    const uint32_t full0 = ctrl;                     // [S]  TMA bytes landed in slot s
+    const uint32_t empty0 = ctrl + 8u * S;           // [S]  MMAs reading slot s are done
+    const uint32_t tfull0 = ctrl + 16u * S;          // [2]  accumulator b is complete
+    const uint32_t tempty0 = ctrl + 16u * S + 16u;   // [2]  epilogue has read accumulator b
+    const uint32_t done_bar = ctrl + 16u * S + 32u;  // all MMAs of this CTA completed
+    const uint32_t stall_bar = ctrl + 16u * S + 40u; // never signalled (test hook)
+    uint32_t *const tmem_slot = reinterpret_cast<uint32_t *>(ctrl_ptr + 16 * S + 48);
+    volatile uint32_t *const abort_flag = tmem_slot + 1;
+
+    const int warp = int(threadIdx.x >> 5);
+    const int lane = int(threadIdx.x & 31);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            ptx::mbar_init(full0 + 8u * s, 1);
+            ptx::mbar_init(empty0 + 8u * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(tfull0 + 8u * b, 1);
+            ptx::mbar_init(tempty0 + 8u * b, Cfg::EPI_WARPS);
+        }
+        ptx::mbar_init(done_bar, 1);
+        ptx::mbar_init(stall_bar, 1);
+        *abort_flag = 0u;
+        ptx::fence_mbar_init();
+        ptx::prefetch_tensormap(&map_a);
+        ptx::prefetch_tensormap(&map_b);
+        ptx::prefetch_tensormap(&map_out);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_addr(tmem_slot), Cfg::TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    ptx::tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer
+            uint32_t stage = 0, phase = 0;
+            uint64_t issued = 0;
+            bool ok = true;
+            for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+                const Unit w = decode_unit(u, p, BN);
+                for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
+                    if (!wait_bounded(empty0 + 8u * stage, phase ^ 1u, abort_flag, p.timeout_ns,
+                                      p.status, kStatusProducer, true)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = full0 + 8u * stage;
+                    const uint32_t sa = base + stage * Cfg::STAGE_BYTES;
+                    ptx::mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES);
+                    ptx::tma_load_3d(sa, &map_a, fb, kb * kTileK, w.m0, w.z_in);
+#pragma unroll
+                    for (int j = 0; j < Cfg::B_BOXES; ++j)
+                        ptx::tma_load_3d(sa + Cfg::A_BYTES + j * Cfg::B_BOX_BYTES, &map_b, fb,
+                                         w.n0 + 64 * j, kb * kTileK, w.z_in);
+                    ++issued;
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // Wait (bounded) for this thread's last loads to land, so that no
+            // TMA write into shared memory outlives the CTA.
+            const uint64_t last = issued < uint64_t(S) ? issued : uint64_t(S);
+            for (uint64_t i = 0; i < last; ++i) {
+                const uint64_t t = issued - 1 - i;
+                wait_bounded(full0 + 8u * uint32_t(t % S), uint32_t((t / S) & 1u), abort_flag,
+                             p.timeout_ns, p.status, kStatusDrain, false);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer (one thread)
+            constexpr uint32_t idesc = mma_idesc<BN>();
+            uint32_t stage = 0, phase = 0, abuf = 0, aphase = 0;
+            bool ok = true;
+            for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+                const Unit w = decode_unit(u, p, BN);
+                if (!wait_bounded(tempty0 + 8u * abuf, aphase ^ 1u, abort_flag, p.timeout_ns,
+                                  p.status, kStatusMma, true)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after_sync();
+                const uint32_t d = tmem_base + abuf * uint32_t(BN);
+                for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
+                    if (!wait_bounded(full0 + 8u * stage, phase, abort_flag, p.timeout_ns,
+                                      p.status, kStatusMma, true)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after_sync();
+                    const uint32_t sa = base + stage * Cfg::STAGE_BYTES;
+                    const uint32_t sb = sa + Cfg::A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < kTileK / 16; ++kk) {
+                        // A: advance 16 f16 = 32 bytes along the swizzled row.
+                        // B: advance 16 K rows = 2048 bytes.
+                        ptx::mma_f16_ss(d, desc_a(sa + 32u * kk), desc_b<BN>(sb + 2048u * kk),
+                                        idesc, (kb > w.kb0 || kk > 0) ? 1u : 0u);
+                    }
+                    ptx::mma_commit(empty0 + 8u * stage);  // slot free once these MMAs finish
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok)
+                    break;
+                ptx::mma_commit(tfull0 + 8u * abuf);  // accumulator ready for the epilogue
+                if (++abuf == 2) {
+                    abuf = 0;
+                    aphase ^= 1u;
+                }
+            }
+            // Every MMA this thread issued must finish before TMEM is freed.
+            ptx::mma_commit(done_bar);
+            wait_bounded(done_bar, 0, abort_flag, p.timeout_ns, p.status, kStatusDrain, false);
+        }
+    } else {
+        // ---------------- epilogue: warps 2..5, TMEM lane quarter = warp % 4
+        const int e = warp - 2;
+        const int q = warp & 3;
+        const uint32_t bufs = epi0 + uint32_t(e) * 2u * Cfg::EPI_BUF_BYTES;
+        uint32_t abuf = 0, aphase = 0, sbuf = 0;
+        for (int64_t u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+            const Unit w = decode_unit(u, p, BN);
+            bool got = wait_bounded(tfull0 + 8u * abuf, aphase, abort_flag, p.timeout_ns, p.status,
+                                    kStatusEpilogue, true);
+            if (p.inject_stall && got)
+                got = wait_bounded(stall_bar, 0, abort_flag, p.timeout_ns, p.status,
+                                   kStatusEpilogue, true);
+            if (!__all_sync(0xffffffffu, got))
+                break;
+            ptx::tc_fence_after_sync();
+            const int32_t row0 = w.m0 + 32 * q;
+            int nch = 0;
+            if (row0 < p.M) {
+                const int live = (p.N - w.n0 + 31) / 32;
+                nch = live < BN / 32 ? live : BN / 32;
+            }
+            const uint32_t tm_row = tmem_base + (uint32_t(32 * q) << 16) + abuf * uint32_t(BN);
+            for (int c = 0; c < nch; ++c) {
+                uint32_t r[32];
+                ptx::tmem_ld_32x32b_x32(tm_row + 32u * c, r);
+                ptx::tmem_wait_ld();
+                if (c == nch - 1) {
+                    // Last read of this accumulator: hand it back to the MMA issuer.
+                    ptx::tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0)
+                        ptx::mbar_arrive(tempty0 + 8u * abuf);
+                }
+                if (lane == 0)
+                    ptx::bulk_wait_group_read<1>();  // the store that used this buffer has read it
+                __syncwarp();
+                // Row `lane` of the 32 x 32 box, 16-byte chunk j at (j ^ row % 8):
+                // the layout the tensor map's 128-byte swizzle expects.
+                const uint32_t buf = bufs + sbuf * Cfg::EPI_BUF_BYTES;
+                const uint32_t row_addr = buf + uint32_t(lane) * 128u;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    ptx::st_shared_v4(row_addr + (uint32_t(j ^ (lane & 7)) << 4), r[4 * j],
+                                      r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    ptx::tma_store_3d(&map_out, buf, w.n0 + 32 * c, row0, w.z_out);
+                    ptx::bulk_commit_group();
+                }
+                sbuf ^= 1u;
+            }
+            if (nch == 0) {
+                ptx::tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0)
+                    ptx::mbar_arrive(tempty0 + 8u * abuf);
+            }
+            if (++abuf == 2) {
+                abuf = 0;
+                aphase ^= 1u;
+            }
+        }
+        if (lane == 0)
+            ptx::bulk_wait_group_all();  // stores complete before the CTA exits
+        __syncwarp();
+    }
+
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        ptx::tc_fence_after_sync();
+        ptx::tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------- split-K reduce
+
+// C[b][i][j] = sum over s = 0, 1, ..., S-1 (in that order) of
+// W[b*S + s][i][j].  Four adjacent columns per thread; W's rows are ldw
+// floats (ldw a multiple of 4), so the loads are aligned float4s.
+__global__ void __launch_bounds__(256)
+    tsm_splitk_reduce_kernel(const float *__restrict__ W, float *__restrict__ C, int32_t M,
+                             int32_t N, int32_t S, int32_t batch, int64_t ldw, int64_t ldc,
+                             int64_t strideC)
+{
+    const int64_t n4 = (N + 3) / 4;
+    const int64_t per_mat = int64_t(M) * n4;
+    const int64_t total = per_mat * batch;
+    const int64_t wmat = int64_t(M) * ldw;
+    for (int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+         idx += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t b = idx / per_mat;
+        const int64_t r = idx - b * per_mat;
+        const int64_t i = r / n4;
+        const int32_t j = int32_t(r - i * n4) * 4;
+        const float *w = W + b * S * wmat + i * ldw + j;
+        float4 acc = __ldg(reinterpret_cast<const float4 *>(w));
+#pragma unroll 8
+        for (int32_t s = 1; s < S; ++s) {
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(w + int64_t(s) * wmat));
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        float *c = C + b * strideC + i * ldc + j;
+        if (j + 3 < N) {
+            *reinterpret_cast<float4 *>(c) = acc;
+        } else {
+            c[0] = acc.x;
+            if (j + 1 < N)
+                c[1] = acc.y;
+            if (j + 2 < N)
+                c[2] = acc.z;
+        }
+    }
+}
+
+// K == 0: every cell is the empty sum.
+__global__ void __launch_bounds__(256)
+    tsm_zero_fill_kernel(float *__restrict__ C, int32_t M, int32_t N, int32_t batch, int64_t ldc,
+                         int64_t strideC)
+{
+    const int64_t per_mat = int64_t(M) * N;
+    const int64_t total = per_mat * batch;
+    for (int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+         idx += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t b = idx / per_mat;
+        const int64_t r = idx - b * per_mat;
+        const int64_t i = r / N;
+        const int64_t j = r - i * N;
+        C[b * strideC + i * ldc + j] = 0.0f;
+    }
+}
+
+// ------------------------------------------------------------- host side
+
+template <int BN>
+static SmemBudget budget_of()
+{
+    using Cfg = TileCfg<BN>;
+    return SmemBudget{Cfg::STAGES, Cfg::STAGE_BYTES, Cfg::SMEM_BYTES, int(Cfg::TMEM_COLS)};
+}
+
+SmemBudget smem_budget(int tile_n)
+{
+    switch (tile_n) {
+    case 64: return budget_of<64>();
+    case 128: return budget_of<128>();
+    default: return budget_of<256>();
+    }
+}
+
+template <int BN>
+static cudaError_t set_attr()
+{
+    return cudaFuncSetAttribute(tsm_gemm_tcgen05_kernel<BN>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                TileCfg<BN>::SMEM_BYTES);
+}
+
+cudaError_t set_kernel_attributes(int tile_n)
+{
+    switch (tile_n) {
+    case 64: return set_attr<64>();
+    case 128: return set_attr<128>();
+    case 256: return set_attr<256>();
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int BN>
+static cudaError_t launch_bn(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o,
+                             const KernelParams &p, int grid, cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(grid), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = TileCfg<BN>::SMEM_BYTES;
+    cfg.stream = stream;
+    cfg.attrs = nullptr;
+    cfg.numAttrs = 0;
+    return cudaLaunchKernelEx(&cfg, tsm_gemm_tcgen05_kernel<BN>, a, b, o, p);
+}
+
+cudaError_t launch_tcgen05_gemm(int tile_n, const CUtensorMap &map_a, const CUtensorMap &map_b,
+                                const CUtensorMap &map_out, const KernelParams &p, int grid,
+                                cudaStream_t stream)
+{
+    switch (tile_n) {
+    case 64: return launch_bn<64>(map_a, map_b, map_out, p, grid, stream);
+    case 128: return launch_bn<128>(map_a, map_b, map_out, p, grid, stream);
+    case 256: return launch_bn<256>(map_a, map_b, map_out, p, grid, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_splitk_reduce(const float *W, float *C, int32_t M, int32_t N, int32_t S,
+                                 int32_t batch, int64_t ldw, int64_t ldc, int64_t strideC,
+                                 int grid, cudaStream_t stream)
+{
+    tsm_splitk_reduce_kernel<<<grid, 256, 0, stream>>>(W, C, M, N, S, batch, ldw, ldc, strideC);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_zero_fill(float *C, int32_t M, int32_t N, int32_t batch, int64_t ldc,
+                             int64_t strideC, int grid, cudaStream_t stream)
+{
+    tsm_zero_fill_kernel<<<grid, 256, 0, stream>>>(C, M, N, batch, ldc, strideC);
+    return cudaGetLastError();
+}
+
+cudaError_t device_status_word(uint32_t **ptr)
+{
+    return cudaGetSymbolAddress(reinterpret_cast<void **>(ptr), g_status_word);
+}
+
+}  // namespace tsm
