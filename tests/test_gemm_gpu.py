@@ -247,10 +247,17 @@ def test_non_default_stream(b):
 
 
 def test_torch_convenience_wrapper(b):
-    A, B = synthetic.operands(190, 210, 330, "int4", seed=10)
-    out = b.gemm(A.cuda(), B.cuda())
+    A, B = synthetic.operands(190, 210, 336, "int4", seed=10)
+    dA = A.cuda()
+    dB = torch.zeros((336, 216), dtype=torch.float16, device="cuda")[:, :210]
+    dB.copy_(B)
+    out = b.gemm(dA, dB)  # N = 210: out gets a padded pitch, returned as a view
     torch.cuda.synchronize()
+    assert out.shape == (190, 210) and out.stride(0) % 4 == 0
     check_exact(out.cpu().numpy(), ref_of(A, B))
+    with pytest.raises(ValueError):
+        b.gemm(torch.zeros((8, 30), dtype=torch.float16, device="cuda"),
+               torch.zeros((30, 8), dtype=torch.float16, device="cuda"))
 
 
 # ---------------------------------------------------------------- device-side argument checks
@@ -264,10 +271,17 @@ def test_host_pointer_rejected(b):
 
 
 def test_allocation_too_small_rejected(b):
-    dA = torch.zeros((64 * 64,), dtype=torch.float16, device="cuda")
-    dB = torch.zeros((64 * 64,), dtype=torch.float16, device="cuda")
-    dC = torch.zeros((64 * 64,), dtype=torch.float32, device="cuda")
-    # claims 1 << 30 rows of A: far beyond the allocation
-    st = b.gemm_f16_f32acc(dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), 64, 64, 1 << 28, 1 << 28,
-                           64, 64, 0)
-    assert st == b.GEMM_ERR_INVALID_VALUE
+    """C claims rows past the end of its allocation: rejected before launch.
+    A, B and C share one fresh 64 MiB allocation (A and B at its start), so
+    the claimed span of C overlaps neither operand and the allocation-range
+    check is what fires."""
+    torch.cuda.empty_cache()
+    buf = torch.empty(64 << 20, dtype=torch.uint8, device="cuda")
+    base = buf.data_ptr()
+    A, B = base, base + (1 << 20)
+    C = base + (64 << 20) - 64 * 64 * 4  # exactly 64 x 64 f32 fit before the end
+    assert b.gemm_f16_f32acc(A, B, C, 64, 64, 64, 64, 64, 64, 0) == b.GEMM_OK
+    assert b.gemm_get_device_status(0) == b.GEMM_OK
+    st = b.gemm_f16_f32acc(A, B, C, 128, 64, 64, 64, 64, 64, 0)  # 128 rows do not
+    assert st == b.GEMM_ERR_INVALID_VALUE, b.gemm_status_string(st)
+    del buf

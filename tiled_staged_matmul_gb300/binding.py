@@ -166,16 +166,22 @@ def gemm(A, B, out=None, *, split_k=0, tile_n=0, timeout_ms=0, inject_stall=0, s
     if batched and B.shape[0] != batch:
         raise ValueError("batch sizes differ")
     if out is None:
-        shape = (batch, M, N) if batched else (M, N)
-        out = torch.empty(shape, dtype=torch.float32, device=A.device)
+        # rows padded to a 16-byte pitch (the TMA's rule); the view hides it
+        ldc_alloc = max(4, -(-N // 4) * 4)
+        shape = (batch, M, ldc_alloc) if batched else (M, ldc_alloc)
+        out = torch.empty(shape, dtype=torch.float32, device=A.device)[..., :N]
     if out.dtype != torch.float32:
         raise TypeError("out must be torch.float32")
     for t, name in ((A, "A"), (B, "B"), (out, "out")):
         if t.numel() and t.stride(-1) != 1:
             raise ValueError(f"{name} must have a unit last stride")
-    lda = A.stride(-2) if M > 1 else max(K, 1)
-    ldb = B.stride(-2) if K > 1 else max(N, 1)
-    ldc = out.stride(-2) if M > 1 else max(N, 1)
+    for t, name, mult in ((A, "A", 8), (B, "B", 8), (out, "out", 4)):
+        if t.numel() and (t.data_ptr() % 16 or (t.dim() and t.shape[-2] > 1 and t.stride(-2) % mult)):
+            raise ValueError(f"{name} needs a 16-byte aligned base and a row stride that is a "
+                             f"multiple of {mult} elements (pad its rows)")
+    lda = A.stride(-2) if M > 1 else -(-max(K, 1) // 8) * 8
+    ldb = B.stride(-2) if K > 1 else -(-max(N, 1) // 8) * 8
+    ldc = out.stride(-2) if M > 1 else -(-max(N, 1) // 4) * 4
     sA = A.stride(0) if batched else 0
     sB = B.stride(0) if batched else 0
     sC = out.stride(0) if batched else 0

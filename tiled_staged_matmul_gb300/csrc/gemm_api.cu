@@ -416,8 +416,21 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
     kp.timeout_ns = uint64_t(timeout_ns_for(o, pl));
     kp.status = ds->status;
 
+    kp.n_tma = N;
+    kp.tail = 0;
+    kp.c_direct = pr.C;
+    kp.ldc = pr.ldc;
+    kp.stride_c = sC;
     if (pl.split_k == 1) {
-        if ((st = encode_3d(&map_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pr.C, pr.N, pr.M, pr.batch,
+        // TMA stores write whole 16-byte granules: let the map end at the last
+        // multiple of 4 columns and write the rest with plain stores, so that
+        // C's row padding past N stays untouched.
+        if (N % 4) {
+            kp.n_tma = N & ~3;
+            kp.tail = 1;
+        }
+        const int64_t map_cols = kp.n_tma > 0 ? kp.n_tma : pr.N;  // an unused map still needs extent
+        if ((st = encode_3d(&map_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pr.C, map_cols, pr.M, pr.batch,
                             pr.ldc, sC, 32, 32, CU_TENSOR_MAP_L2_PROMOTION_NONE, "C")) != GEMM_OK)
             return st;
         if ((e = launch_tcgen05_gemm(pl.tile_n, map_a, map_b, map_out, kp, pl.grid, stream)) != cudaSuccess)

@@ -30,6 +30,14 @@ struct KernelParams {
     int64_t num_units;    // batch * split_k * tiles_m * tiles_n
     uint64_t timeout_ns;  // limit of every device-side wait
     uint32_t *status;     // device status word (OR of kStatus* bits)
+    // A TMA store writes whole 16-byte granules of a row, so it covers only
+    // the columns below n_tma (a multiple of 4); when `tail` is set the
+    // epilogue writes columns [n_tma, N) of C with plain stores.
+    int32_t n_tma;
+    int32_t tail;
+    float *c_direct;      // C itself (tail stores)
+    int64_t ldc;
+    int64_t stride_c;
 };
 
 // Shared-memory budget of one CTA for a tile width (host and device agree).

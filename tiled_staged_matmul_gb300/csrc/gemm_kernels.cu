@@ -341,24 +341,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0)
                         ptx::mbar_arrive(tempty0 + 8u * abuf);
                 }
-                if (lane == 0)
-                    ptx::bulk_wait_group_read<1>();  // the store that used this buffer has read it
-                __syncwarp();
-                // Row `lane` of the 32 x 32 box, 16-byte chunk j at (j ^ row % 8):
-                // the layout the tensor map's 128-byte swizzle expects.
-                const uint32_t buf = bufs + sbuf * Cfg::EPI_BUF_BYTES;
-                const uint32_t row_addr = buf + uint32_t(lane) * 128u;
+                const int32_t col0 = w.n0 + 32 * c;
+                if (col0 < p.n_tma) {
+                    if (lane == 0)
+                        ptx::bulk_wait_group_read<1>();  // the store that used this buffer has read it
+                    __syncwarp();
+                    // Row `lane` of the 32 x 32 box, 16-byte chunk j at (j ^ row % 8):
+                    // the layout the tensor map's 128-byte swizzle expects.
+                    const uint32_t buf = bufs + sbuf * Cfg::EPI_BUF_BYTES;
+                    const uint32_t row_addr = buf + uint32_t(lane) * 128u;
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    ptx::st_shared_v4(row_addr + (uint32_t(j ^ (lane & 7)) << 4), r[4 * j],
-                                      r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    ptx::tma_store_3d(&map_out, buf, w.n0 + 32 * c, row0, w.z_out);
-                    ptx::bulk_commit_group();
+                    for (int j = 0; j < 8; ++j)
+                        ptx::st_shared_v4(row_addr + (uint32_t(j ^ (lane & 7)) << 4), r[4 * j],
+                                          r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::tma_store_3d(&map_out, buf, col0, row0, w.z_out);
+                        ptx::bulk_commit_group();
+                    }
+                    sbuf ^= 1u;
                 }
-                sbuf ^= 1u;
+                if (p.tail && col0 + 32 > p.n_tma) {
+                    // Columns [n_tma, N): fewer than four, written one by one.
+                    const int32_t row = row0 + lane;
+                    if (row < p.M) {
+                        float *dst = p.c_direct + int64_t(w.z_out) * p.stride_c + int64_t(row) * p.ldc;
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) {
+                            const int32_t col = col0 + t;
+                            if (col >= p.n_tma && col < p.N)
+                                dst[col] = __uint_as_float(r[t]);
+                        }
+                    }
+                }
             }
             if (nch == 0) {
                 ptx::tc_fence_before_sync();
