@@ -157,6 +157,35 @@ gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int64_t batch,
                         const gemm_options_t *opts, int32_t num_sms,
                         gemm_plan_info_t *plan);
 
+/* C = A . B like gemm_f16_f32acc, for callers that cannot allocate device
+ * memory while they run: code being captured into a CUDA graph that must not
+ * gain allocation nodes, allocators or memory managers that call into this
+ * library and may not re-enter themselves, and hosts that reserved all of
+ * the GPU's memory in advance.  The paper has no counterpart to this entry
+ * point; it exists for those callers only.
+ *
+ * It allocates nothing.  When the plan splits K (split_k: 0 = the planner's
+ * choice, S >= 1 = S ranges), the f32 partial sums go to one fixed 16 MiB
+ * array compiled into the library (a file-scope __device__ array, so every
+ * GPU that loads the library holds those 16 MiB until the process exits),
+ * instead of the stream-ordered pool.  A plan whose partials need more than
+ * 16 MiB (S x M x round_up(N, 4) x 4 bytes) is rejected with
+ * GEMM_ERR_INVALID_VALUE and a message naming the size.  K == 0 is rejected
+ * too; use gemm_f16_f32acc for it.
+ *
+ * The first call on a device resolves the array's device address and
+ * queries the device (no allocation); make that first call before any
+ * stream capture begins.  Every call on a device shares the one array and
+ * it keeps the last call's partials: calls whose work overlaps on the GPU
+ * (for example on two streams at once) race on it and must be ordered by the
+ * caller.  Nothing in it needs to start at zero -- every partial the reduce
+ * reads is written earlier in the same call.  Arguments, layout, ownership
+ * and errors are otherwise those of gemm_f16_f32acc (single matrix). */
+gemm_status_t gemm_f16_f32acc_splitk_noalloc(const uint16_t *A, const uint16_t *B, float *C,
+                                             int64_t M, int64_t N, int64_t K,
+                                             int64_t lda, int64_t ldb, int64_t ldc,
+                                             int32_t split_k, gemm_stream_t stream);
+
 /* Waits for `stream`, then reports and clears the current device's status
  * word: GEMM_OK, or GEMM_ERR_DEVICE_TIMEOUT if a bounded wait of an earlier
  * call ran out (that call's output is then incomplete), or GEMM_ERR_CUDA if

@@ -76,6 +76,9 @@ def _load() -> ctypes.CDLL:
     lib.gemm_status_string.argtypes = [ctypes.c_int]
     lib.gemm_version.restype = ctypes.c_int32
     lib.gemm_version.argtypes = []
+    lib.gemm_f16_f32acc_splitk_noalloc.restype = ctypes.c_int
+    lib.gemm_f16_f32acc_splitk_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64,
+                                                   i32, vp]
     return lib
 
 
@@ -103,6 +106,12 @@ def gemm_f16_f32acc_opts(A, B, C, M, N, K, lda, ldb, ldc, strideA, strideB, stri
     p = ctypes.byref(opts) if opts is not None else None
     return _lib.gemm_f16_f32acc_opts(A, B, C, M, N, K, lda, ldb, ldc, strideA, strideB,
                                      strideC, batch, p, stream)
+
+
+def gemm_f16_f32acc_splitk_noalloc(A, B, C, M, N, K, lda, ldb, ldc, split_k=0, stream=0) -> int:
+    """The entry point that allocates nothing (split-K partials in a fixed
+    16 MiB device array inside the library); see include/tsm_gemm.h."""
+    return _lib.gemm_f16_f32acc_splitk_noalloc(A, B, C, M, N, K, lda, ldb, ldc, split_k, stream)
 
 
 def gemm_plan(M, N, K, batch=1, opts: GemmOptions | None = None, num_sms=0) -> dict:

@@ -562,3 +562,181 @@ const char *gemm_status_string(gemm_status_t s)
 int32_t gemm_version(void) { return 100; }
 
 }  // extern "C"
+
+// ------------------------------------------------------------- no-allocation entry point
+//
+// Some callers cannot allocate device memory at call time: code running
+// inside a CUDA stream capture that must not add allocation nodes, an
+// allocator or memory-accounting layer that may not re-enter itself, or an
+// embedded host that reserved every byte of the GPU up front.  For them the
+// split-K path can take its partial sums from a fixed array that lives in
+// this file instead of the stream-ordered pool.  The array is a file-scope
+// __device__ object: every GPU that loads the library holds it until the
+// process exits.
+
+namespace tsm {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB of f32 partials
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+struct NoAllocDevice {
+    bool ready = false;
+    void *scratch = nullptr;  // device address of g_noalloc_scratch on this device
+    int sms = 0;
+    int smem_optin = 0;
+    uint32_t *status = nullptr;
+    bool attrs_set[3] = {false, false, false};
+};
+
+NoAllocDevice g_noalloc_devices[kMaxDevices];
+std::mutex g_noalloc_mutex;
+
+// Once per device, with that device current: resolve the array's device
+// address (the host-side name is only a stand-in), the SM count and the
+// status word.  None of this allocates.
+gemm_status_t noalloc_setup(int dev, NoAllocDevice **out)
+{
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(GEMM_ERR_INVALID_VALUE, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    NoAllocDevice &d = g_noalloc_devices[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0;
+        cudaError_t e;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+            return fail_cuda(e, "cudaDeviceGetAttribute(compute capability)");
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (major != 10 || minor != 3)
+            return fail(GEMM_ERR_UNSUPPORTED_DEVICE,
+                        "device %d has compute capability %d.%d; this library is built for 10.3 only",
+                        dev, major, minor);
+        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if ((e = cudaGetSymbolAddress(&d.scratch, g_noalloc_scratch)) != cudaSuccess)
+            return fail_cuda(e, "cudaGetSymbolAddress(static split-K scratch)");
+        if ((e = device_status_word(&d.status)) != cudaSuccess)
+            return fail_cuda(e, "cudaGetSymbolAddress(status word)");
+        d.ready = true;
+    }
+    *out = &d;
+    return GEMM_OK;
+}
+
+}  // namespace
+}  // namespace tsm
+
+extern "C" gemm_status_t gemm_f16_f32acc_splitk_noalloc(const uint16_t *A, const uint16_t *B,
+                                                        float *C, int64_t M, int64_t N, int64_t K,
+                                                        int64_t lda, int64_t ldb, int64_t ldc,
+                                                        int32_t split_k, gemm_stream_t stream_)
+{
+    using namespace tsm;
+    g_last_error.clear();
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    Problem pr{A, B, C, M, N, K, lda, ldb, ldc, 0, 0, 0, 1};
+    bool trivial = false;
+    gemm_status_t st = check_host(pr, &trivial);
+    if (st != GEMM_OK || trivial)
+        return st;
+    if (split_k < 0)
+        return fail(GEMM_ERR_INVALID_VALUE, "split_k must be >= 0");
+    if (K == 0)
+        return fail(GEMM_ERR_INVALID_VALUE, "K == 0 is not served by the no-allocation entry point");
+
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return fail_cuda(e, "cudaGetDevice");
+    NoAllocDevice *nd = nullptr;
+    if ((st = noalloc_setup(dev, &nd)) != GEMM_OK)
+        return st;
+    if ((st = check_device_pointer(C, span_bytes(1, 0, M, ldc, N, 4), dev, "C")) != GEMM_OK)
+        return st;
+    if ((st = check_device_pointer(A, span_bytes(1, 0, M, lda, K, 2), dev, "A")) != GEMM_OK)
+        return st;
+    if ((st = check_device_pointer(B, span_bytes(1, 0, K, ldb, N, 2), dev, "B")) != GEMM_OK)
+        return st;
+
+    gemm_options_t o = {};
+    o.split_k = split_k;
+    gemm_plan_info_t pl;
+    if ((st = make_plan(M, N, K, 1, &o, nd->sms, &pl)) != GEMM_OK)
+        return st;
+    if (uint64_t(pl.workspace_bytes) > kNoAllocScratchBytes)
+        return fail(GEMM_ERR_INVALID_VALUE,
+                    "split-K partials need %lld bytes (S=%d x %lld x %lld f32); the static scratch "
+                    "holds %zu bytes -- use a smaller split_k or gemm_f16_f32acc",
+                    (long long)pl.workspace_bytes, pl.split_k, (long long)M, (long long)((N + 3) / 4 * 4),
+                    kNoAllocScratchBytes);
+    if (nd->smem_optin < pl.smem_bytes)
+        return fail(GEMM_ERR_UNSUPPORTED_DEVICE, "device allows %d bytes of shared memory per block, the kernel needs %lld",
+                    nd->smem_optin, (long long)pl.smem_bytes);
+    const int ti = tile_index(pl.tile_n);
+    if (!nd->attrs_set[ti]) {
+        if ((e = set_kernel_attributes(pl.tile_n)) != cudaSuccess)
+            return fail_cuda(e, "cudaFuncSetAttribute(max dynamic shared memory)");
+        nd->attrs_set[ti] = true;
+    }
+
+    alignas(64) CUtensorMap map_a, map_b, map_out;
+    if ((st = encode_3d(&map_a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, A, K, M, 1, lda, M * lda, kTileK,
+                        kTileM, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "A")) != GEMM_OK)
+        return st;
+    if ((st = encode_3d(&map_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, B, N, K, 1, ldb, K * ldb, 64,
+                        kTileK, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "B")) != GEMM_OK)
+        return st;
+
+    KernelParams kp = {};
+    kp.M = int32_t(M);
+    kp.N = int32_t(N);
+    kp.K = int32_t(K);
+    kp.tiles_m = pl.tiles_m;
+    kp.tiles_n = pl.tiles_n;
+    kp.k_blocks = pl.k_blocks;
+    kp.split_k = pl.split_k;
+    kp.batch = 1;
+    kp.group_m = pl.group_m;
+    kp.inject_stall = 0;
+    kp.num_units = pl.units;
+    kp.timeout_ns = uint64_t(timeout_ns_for(nullptr, pl));
+    kp.status = nd->status;
+    kp.n_tma = int32_t(N);
+    kp.tail = 0;
+    kp.c_direct = C;
+    kp.ldc = ldc;
+    kp.stride_c = M * ldc;
+
+    if (pl.split_k == 1) {
+        // No partials to keep: the ordinary single-pass kernel, which needs no scratch.
+        if (N % 4) {
+            kp.n_tma = int32_t(N) & ~3;
+            kp.tail = 1;
+        }
+        const int64_t map_cols = kp.n_tma > 0 ? kp.n_tma : N;
+        if ((st = encode_3d(&map_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, map_cols, M, 1, ldc,
+                            M * ldc, 32, 32, CU_TENSOR_MAP_L2_PROMOTION_NONE, "C")) != GEMM_OK)
+            return st;
+        if ((e = launch_tcgen05_gemm(pl.tile_n, map_a, map_b, map_out, kp, pl.grid, stream)) != cudaSuccess)
+            return fail_cuda(e, "GEMM kernel launch");
+        return GEMM_OK;
+    }
+
+    // Every (split, row < M, column < N) partial is written before the reduce
+    // reads it, so nothing in the scratch has to start at zero.
+    const int64_t ldw = (N + 3) / 4 * 4;
+    if ((st = encode_3d(&map_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, nd->scratch, N, M, pl.split_k,
+                        ldw, M * ldw, 32, 32, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        "static split-K scratch")) != GEMM_OK)
+        return st;
+    if ((e = launch_tcgen05_gemm(pl.tile_n, map_a, map_b, map_out, kp, pl.grid, stream)) != cudaSuccess)
+        return fail_cuda(e, "GEMM kernel launch");
+    const int64_t threads = M * ((N + 3) / 4);
+    const int grid = int(std::min<int64_t>((threads + 255) / 256, int64_t(nd->sms) * 8));
+    if ((e = launch_splitk_reduce(static_cast<const float *>(nd->scratch), C, int32_t(M), int32_t(N),
+                                  pl.split_k, 1, ldw, ldc, M * ldc, grid, stream)) != cudaSuccess)
+        return fail_cuda(e, "split-K reduce launch");
+    return GEMM_OK;
+}
