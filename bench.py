@@ -44,7 +44,10 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                   help="one of the named workloads in tiled_staged_matmul_gb300.synthetic")
+    p.add_argument("--shape", default=None,
+                   help="MxNxK: an ad-hoc shape with N(0, 1/sqrt(K)) operands instead of --workload")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=10)
@@ -181,7 +184,7 @@ def run_ours(args, rank, local_rank, world):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    w = synthetic.WORKLOADS[args.workload]
+    w = pick_workload(args)
     A_h, B_h = synthetic.workload_operands(w)
     A = A_h.to(dev)
     B = B_h.to(dev)
@@ -243,7 +246,7 @@ def run_ours(args, rank, local_rank, world):
     else:
         roofline = {"bound": "hbm", "achieved": round(gbs_launch, 1), "peak": peaks["hbm_gbs"],
                     "unit": "GB/s", "frac": round(gbs_launch / peaks["hbm_gbs"], 4)}
-    roofline["traffic"] = recorded_traffic(args.workload)
+    roofline["traffic"] = recorded_traffic(w.name)
     roofline["peak_source"] = (f"{peaks['source']} (MEASURED_PEAKS.json bf16 burst; f16 dense "
                                "rate taken equal to bf16, the nominal ratio)"
                                if roofline["bound"] == "tensor" else
@@ -282,6 +285,15 @@ def run_ours(args, rank, local_rank, world):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, A_h, B_h, target_s=15.0)
     return result
+
+
+def pick_workload(args):
+    from tiled_staged_matmul_gb300 import synthetic
+    if args.shape:
+        M, N, K = (int(x) for x in args.shape.lower().split("x"))
+        return synthetic.Workload(f"gemm_{M}x{N}x{K}_normal_invsqrtk", M, N, K,
+                                  "normal_invsqrtk", 2000)
+    return synthetic.WORKLOADS[args.workload]
 
 
 def run_e2e(args, w, A_h, B_h, dev, world):
@@ -349,7 +361,7 @@ def run_reference(args, rank, world):
     import oracle
     from tiled_staged_matmul_gb300 import synthetic
 
-    w = synthetic.WORKLOADS[args.workload]
+    w = pick_workload(args)
     A_h, B_h = synthetic.workload_operands(w)
     rows = max(1, min(w.M, int(4e9 // (2 * w.N * w.K)) or 1))
     for i in range(max(args.warmup, 0)):
