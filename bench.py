@@ -71,6 +71,14 @@ def max_over_ranks(x: float, world: int, device=None) -> float:
     return float(t.item())
 
 
+def replica_throughput(flops_per_rank: float, ms_local: float, world: int, device=None):
+    """Whole-job throughput of `world` independent replicas: every rank did
+    `flops_per_rank`; the slowest rank's time per step decides.  Returns
+    (TFLOP/s over all ranks, the max ms per step)."""
+    ms = max_over_ranks(ms_local, world, device)
+    return world * flops_per_rank / (ms * 1e-3) / 1e12, ms
+
+
 def barrier(world: int) -> None:
     if world > 1:
         import torch.distributed as dist
@@ -231,8 +239,7 @@ def run_ours(args, rank, local_rank, world):
 
     per_step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms_local = sum(per_step_ms) / len(per_step_ms)
-    ms = max_over_ranks(ms_local, world, dev)
-    value = world * w.flops / (ms * 1e-3) / 1e12
+    value, ms = replica_throughput(w.flops, ms_local, world, dev)
 
     peaks = measured_peaks()
     tflops_launch = w.flops / (ms_local * 1e-3) / 1e12
