@@ -95,11 +95,14 @@ typedef struct gemm_options {
     int32_t inject_stall; /* test hook, 0 in normal use; 1 makes the epilogue wait on a
                              barrier that nothing signals, so that its bounded wait runs
                              out and the call reports GEMM_ERR_DEVICE_TIMEOUT */
+    int32_t tile_m;     /* 0: planner's choice; 128: one CTA per tile; 256: a CTA pair per
+                           tile (a 2-CTA cluster issuing tcgen05 cta_group::2 MMAs; needs
+                           tile_n 128 or 256) */
 } gemm_options_t;
 
 /* What the planner chose for a problem (see gemm_plan). */
 typedef struct gemm_plan_info {
-    int32_t tile_m;       /* rows of C per tile (128) */
+    int32_t tile_m;       /* rows of C per tile: 128 (one CTA) or 256 (a CTA pair) */
     int32_t tile_n;       /* columns of C per tile */
     int32_t tile_k;       /* K depth of one staged k-block (64) */
     int32_t stages;       /* k-blocks in flight in the shared-memory ring */
@@ -108,7 +111,8 @@ typedef struct gemm_plan_info {
     int32_t tiles_n;      /* ceil(N / tile_n) */
     int32_t k_blocks;     /* ceil(K / tile_k) */
     int64_t units;        /* batch * split_k * tiles_m * tiles_n work units */
-    int32_t grid;         /* persistent CTAs launched: min(units, SMs) */
+    int32_t grid;         /* persistent CTAs launched: min(units, SMs) for one CTA per
+                             tile, 2 x min(units, SMs / 2) for CTA pairs */
     int32_t group_m;      /* tiles of M walked together in the raster order */
     int64_t stage_bytes;  /* shared memory of one k-block: A tile + B tile */
     int64_t smem_bytes;   /* dynamic shared memory of one CTA */
@@ -165,7 +169,8 @@ gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int64_t batch,
  * point; it exists for those callers only.
  *
  * It allocates nothing.  When the plan splits K (split_k: 0 = the planner's
- * choice, S >= 1 = S ranges), the f32 partial sums go to one fixed 16 MiB
+ * choice, lowered if needed until the partials fit; S >= 1 = exactly S
+ * ranges, clamped to the k-blocks), the f32 partial sums go to one fixed 16 MiB
  * array compiled into the library (a file-scope __device__ array, so every
  * GPU that loads the library holds those 16 MiB until the process exits),
  * instead of the stream-ordered pool.  A plan whose partials need more than

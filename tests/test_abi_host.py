@@ -107,16 +107,19 @@ def test_stage_footprint_matches_the_pages_arithmetic(b):
     assert g["K"] * g["N"] * e == g["b_tile_bytes"]
     assert g["a_tile_bytes"] + g["b_tile_bytes"] == g["total_bytes"]
     assert (g["total_bytes"] <= g["budget_bytes"]) == g["fits"]
-    p = b.gemm_plan(8192, 8192, 8192, 1, b._opts(tile_n=256), SMS)
+    p = b.gemm_plan(8192, 8192, 8192, 1, b._opts(tile_n=256, tile_m=128), SMS)
     assert p["tile_m"] * p["tile_k"] * e == g["a_tile_bytes"]
     assert p["tile_k"] * p["tile_n"] * e == g["b_tile_bytes"]
     assert p["stage_bytes"] == g["total_bytes"]
 
 
-@pytest.mark.parametrize("tile_n", [64, 128, 256])
-def test_ring_fills_the_shared_memory_budget(b, tile_n):
-    p = b.gemm_plan(4096, 4096, 4096, 1, b._opts(tile_n=tile_n), SMS)
-    assert p["stage_bytes"] == 2 * 128 * 64 + 2 * 64 * tile_n
+@pytest.mark.parametrize("tile_m,tile_n", [(128, 64), (128, 128), (128, 256), (256, 128), (256, 256)])
+def test_ring_fills_the_shared_memory_budget(b, tile_m, tile_n):
+    p = b.gemm_plan(4096, 4096, 4096, 1, b._opts(tile_n=tile_n, tile_m=tile_m), SMS)
+    assert (p["tile_m"], p["tile_n"]) == (tile_m, tile_n)
+    # per CTA: 128 rows of A, and all of the tile's B columns (one CTA) or half (a pair)
+    b_cols = tile_n if tile_m == 128 else tile_n // 2
+    assert p["stage_bytes"] == 2 * 128 * 64 + 2 * 64 * b_cols
     assert p["stages"] >= 2
     assert p["smem_bytes"] <= 232448
     # one more stage would not fit
@@ -125,17 +128,26 @@ def test_ring_fills_the_shared_memory_budget(b, tile_n):
     assert p["smem_bytes"] > 232448 // 2
 
 
+def test_pair_needs_a_wide_tile(b):
+    with pytest.raises(b.GemmError):
+        b.gemm_plan(4096, 4096, 4096, 1, b._opts(tile_n=64, tile_m=256), SMS)
+
+
 @pytest.mark.parametrize("M,N,K", [(64, 128, 128), (1000, 1000, 1000), (4096, 4096, 4096),
                                    (256, 256, 65536), (8192, 8192, 8192), (1, 1, 1),
                                    (300, 7, 100000), (1, 5000, 64)])
 def test_plan_invariants(b, M, N, K):
     p = b.gemm_plan(M, N, K, 1, None, SMS)
-    assert p["tiles_m"] == -(-M // 128)
+    assert p["tile_m"] in (128, 256)
+    assert p["tiles_m"] == -(-M // p["tile_m"])
     assert p["tiles_n"] == -(-N // p["tile_n"])
     assert p["k_blocks"] == -(-K // 64)
     assert 1 <= p["split_k"] <= p["k_blocks"]
     assert p["units"] == p["tiles_m"] * p["tiles_n"] * p["split_k"]
-    assert p["grid"] == min(p["units"], SMS)
+    if p["tile_m"] == 128:
+        assert p["grid"] == min(p["units"], SMS)
+    else:
+        assert p["grid"] == 2 * min(p["units"], SMS // 2)
     ldw = -(-N // 4) * 4
     assert p["workspace_bytes"] == (p["split_k"] * M * ldw * 4 if p["split_k"] > 1 else 0)
 
@@ -143,13 +155,13 @@ def test_plan_invariants(b, M, N, K):
 def test_long_K_small_output_splits_K(b):
     p = b.gemm_plan(256, 256, 65536, 1, None, SMS)
     assert p["split_k"] > 1
-    assert p["units"] <= SMS
+    assert p["grid"] <= SMS
     assert p["k_blocks"] // p["split_k"] >= 4
 
 
 def test_large_square_uses_wide_tiles_without_split(b):
     p = b.gemm_plan(8192, 8192, 8192, 1, None, SMS)
-    assert p["tile_n"] == 256 and p["split_k"] == 1
+    assert (p["tile_m"], p["tile_n"], p["split_k"]) == (256, 256, 1)  # CTA pairs
 
 
 def test_forced_split_is_clamped_to_k_blocks(b):

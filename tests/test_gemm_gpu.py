@@ -29,6 +29,10 @@ def b():
     return binding
 
 
+# (tile_m, tile_n): one CTA per 128-row tile, or a CTA pair per 256-row tile
+TILES = [(128, 64), (128, 128), (128, 256), (256, 128), (256, 256)]
+
+
 def ref_of(A, B):
     M, K = A.shape
     N = B.shape[1]
@@ -92,9 +96,26 @@ def test_long_K_integer_bit_exact_for_every_split(b):
     w = integer_twin(WORKLOADS["gemm_256x256x65536_uniform"])
     A, B = synthetic.workload_operands(w)
     ref = ref_of(A, B)
-    for s in (1, 2, 3, 7, 64, 0):
-        C, _ = run_gemm(b, A, B, split_k=s)
-        check_exact(C.numpy(), ref)
+    for tile_m, tile_n in ((128, 128), (256, 256)):
+        for s in (1, 2, 3, 7, 64, 0):
+            C, _ = run_gemm(b, A, B, split_k=s, tile_m=tile_m, tile_n=tile_n)
+            check_exact(C.numpy(), ref)
+
+
+@pytest.mark.parametrize("tile_m,tile_n", TILES)
+def test_every_tile_shape_on_random_inputs(b, tile_m, tile_n):
+    A, B = synthetic.operands(700, 900, 1500, "normal", seed=tile_m + tile_n)
+    C, dC = run_gemm(b, A, B, tile_m=tile_m, tile_n=tile_n)
+    check_tolerance(C.numpy(), ref_of(A, B), 1500)
+    assert dC.outside_untouched()
+
+
+def test_pair_tiles_with_many_units_per_cluster(b):
+    # 2048 x 2048 on 256 x 128 pair tiles: 128 units over at most 76 clusters,
+    # so clusters walk several tiles and both TMEM accumulators take turns.
+    A, B = synthetic.operands(2048, 2048, 512, "int4", seed=17)
+    C, _ = run_gemm(b, A, B, tile_m=256, tile_n=128)
+    check_exact(C.numpy(), ref_of(A, B))
 
 
 def _sampled_cells(w, C, A, B, n=4096, seed=0):
@@ -136,10 +157,10 @@ RAGGED = [(1, 1, 1), (1, 8, 1), (7, 9, 63), (129, 257, 65), (130, 250, 1000),
 
 
 @pytest.mark.parametrize("M,N,K", RAGGED)
-@pytest.mark.parametrize("tile_n", [64, 128, 256])
-def test_ragged_integer_bit_exact(b, M, N, K, tile_n):
+@pytest.mark.parametrize("tile_m,tile_n", TILES)
+def test_ragged_integer_bit_exact(b, M, N, K, tile_m, tile_n):
     A, B = synthetic.operands(M, N, K, "int4", seed=M * 7 + N * 13 + K)
-    C, dC = run_gemm(b, A, B, tile_n=tile_n)
+    C, dC = run_gemm(b, A, B, tile_n=tile_n, tile_m=tile_m)
     check_exact(C.numpy(), ref_of(A, B))
     assert dC.outside_untouched()
 
@@ -223,10 +244,11 @@ def test_batched(b):
         assert dC.outside_untouched()
 
 
-def test_batched_random_with_split(b):
+@pytest.mark.parametrize("tile_m", [128, 256])
+def test_batched_random_with_split(b, tile_m):
     M, N, K, batch = 256, 192, 8192, 2
     A, B = synthetic.operands(M, N, K, "uniform", seed=12, batch=batch)
-    C, _ = run_gemm(b, A, B, batch=batch, split_k=5)
+    C, _ = run_gemm(b, A, B, batch=batch, split_k=5, tile_m=tile_m, tile_n=128)
     for i in range(batch):
         check_tolerance(C[i].numpy(), ref_of(A[i], B[i]), K)
 

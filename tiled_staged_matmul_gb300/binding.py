@@ -28,7 +28,8 @@ GEMM_ERR_DEVICE_TIMEOUT = 6
 
 class GemmOptions(ctypes.Structure):
     _fields_ = [("split_k", ctypes.c_int32), ("tile_n", ctypes.c_int32),
-                ("timeout_ms", ctypes.c_int32), ("inject_stall", ctypes.c_int32)]
+                ("timeout_ms", ctypes.c_int32), ("inject_stall", ctypes.c_int32),
+                ("tile_m", ctypes.c_int32)]
 
 
 class GemmPlanInfo(ctypes.Structure):
@@ -85,8 +86,8 @@ def _load() -> ctypes.CDLL:
 _lib = _load()
 
 
-def _opts(split_k=0, tile_n=0, timeout_ms=0, inject_stall=0):
-    return GemmOptions(int(split_k), int(tile_n), int(timeout_ms), int(inject_stall))
+def _opts(split_k=0, tile_n=0, timeout_ms=0, inject_stall=0, tile_m=0):
+    return GemmOptions(int(split_k), int(tile_n), int(timeout_ms), int(inject_stall), int(tile_m))
 
 
 # ------------------------------------------------------------------ raw C names
@@ -155,7 +156,8 @@ def _stream_handle(stream):
     return stream.cuda_stream
 
 
-def gemm(A, B, out=None, *, split_k=0, tile_n=0, timeout_ms=0, inject_stall=0, stream=None):
+def gemm(A, B, out=None, *, split_k=0, tile_n=0, tile_m=0, timeout_ms=0, inject_stall=0,
+         stream=None):
     """``out = A @ B`` for f16 CUDA tensors A (M x K) and B (K x N), f32 out.
 
     3-D tensors (batch x M x K, batch x K x N) run as one batched call.  Rows
@@ -194,7 +196,7 @@ def gemm(A, B, out=None, *, split_k=0, tile_n=0, timeout_ms=0, inject_stall=0, s
     sA = A.stride(0) if batched else 0
     sB = B.stride(0) if batched else 0
     sC = out.stride(0) if batched else 0
-    opts = _opts(split_k, tile_n, timeout_ms, inject_stall)
+    opts = _opts(split_k, tile_n, timeout_ms, inject_stall, tile_m)
     st = gemm_f16_f32acc_opts(A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K, lda, ldb,
                               ldc, sA, sB, sC, batch, opts, _stream_handle(stream))
     check(st)

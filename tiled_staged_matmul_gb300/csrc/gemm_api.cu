@@ -87,7 +87,7 @@ struct DeviceState {
     int sms = 0;
     int cc_major = 0, cc_minor = 0;
     int smem_optin = 0;
-    bool attrs_set[3] = {false, false, false};  // tile_n 64, 128, 256
+    bool attrs_set[5] = {false, false, false, false, false};  // see config_index
     cudaMemPool_t pool = nullptr;
     uint32_t *status = nullptr;
 };
@@ -129,7 +129,13 @@ gemm_status_t device_state(int dev, DeviceState **out)
     return GEMM_OK;
 }
 
-int tile_index(int tile_n) { return tile_n == 64 ? 0 : tile_n == 128 ? 1 : 2; }
+// One slot per kernel instantiation: single-CTA tile_n 64 / 128 / 256, CTA-pair 128 / 256.
+int config_index(int tile_m, int tile_n)
+{
+    if (tile_m == 2 * kTileM)
+        return tile_n == 128 ? 3 : 4;
+    return tile_n == 64 ? 0 : tile_n == 128 ? 1 : 2;
+}
 
 // ------------------------------------------------------------- argument checks
 
@@ -243,6 +249,16 @@ gemm_status_t check_device_pointer(const void *p, int64_t bytes, int dev, const 
 
 int ceil_div(int64_t a, int64_t b) { return int((a + b - 1) / b); }
 
+// Candidate tile shapes with a relative per-SM efficiency (measured on
+// GB300: the 1-CTA 128 x 256 tile keeps the tensor pipe about 72 % busy,
+// bounded by shared-memory bandwidth; a CTA pair halves each SM's B traffic).
+struct TileChoice {
+    int tile_m, tile_n;
+    double eff;
+};
+constexpr TileChoice kChoices[] = {
+    {256, 256, 1.00}, {256, 128, 0.85}, {128, 256, 0.80}, {128, 128, 0.72}, {128, 64, 0.55}};
+
 gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const gemm_options_t *o,
                         int sms, gemm_plan_info_t *pl)
 {
@@ -250,65 +266,85 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const ge
         return fail(GEMM_ERR_INVALID_VALUE, "SM count must be positive");
     memset(pl, 0, sizeof *pl);
     const int req_n = o ? o->tile_n : 0;
+    const int req_m = o ? o->tile_m : 0;
     if (req_n != 0 && req_n != 64 && req_n != 128 && req_n != 256)
         return fail(GEMM_ERR_INVALID_VALUE, "tile_n must be 0, 64, 128 or 256 (got %d)", req_n);
+    if (req_m != 0 && req_m != 128 && req_m != 256)
+        return fail(GEMM_ERR_INVALID_VALUE, "tile_m must be 0, 128 or 256 (got %d)", req_m);
+    if (req_m == 256 && req_n == 64)
+        return fail(GEMM_ERR_INVALID_VALUE, "tile_m 256 (a CTA pair) needs tile_n 128 or 256");
+    if (req_m == 256 && sms < 2)
+        return fail(GEMM_ERR_INVALID_VALUE, "a CTA pair needs at least two SMs");
     const int req_s = o ? o->split_k : 0;
     if (req_s < 0)
         return fail(GEMM_ERR_INVALID_VALUE, "split_k must be >= 0");
-    const int tiles_m = ceil_div(std::max<int64_t>(M, 1), kTileM);
     const int k_blocks = ceil_div(std::max<int64_t>(K, 1), kTileK);
-    auto tiles_of = [&](int bn) { return int64_t(tiles_m) * ceil_div(std::max<int64_t>(N, 1), bn) * batch; };
-
-    int bn = req_n;
-    int split = 1;
-    if (bn == 0) {
-        // Long K on a small output: too few tiles to fill the SMs, so the K
-        // range is split (the pages' "long K" case; see the split rule below).
-        const bool long_k = tiles_of(256) * 2 <= sms && k_blocks >= 16;
+    const int64_t Mx = std::max<int64_t>(M, 1), Nx = std::max<int64_t>(N, 1);
+    const int64_t ldw = (N + 3) / 4 * 4;
+    auto tiles_of = [&](int tm, int tn) { return int64_t(ceil_div(Mx, tm)) * ceil_div(Nx, tn) * batch; };
+    auto slots_of = [&](int tm) { return int64_t(tm == 2 * kTileM ? sms / 2 : sms); };
+    auto allowed = [&](const TileChoice &c) {
+        return (req_m == 0 || req_m == c.tile_m) && (req_n == 0 || req_n == c.tile_n) &&
+               (c.tile_m == kTileM || sms >= 2);
+    };
+    // K ranges that put about one unit on every slot, at least 4 k-blocks each.
+    auto split_for = [&](int tm, int tn) -> int {
+        if (req_s > 0)
+            return std::min(req_s, k_blocks);
+        const int64_t tiles = tiles_of(tm, tn);
+        if (K == 0 || tiles >= slots_of(tm))
+            return 1;
+        return int(std::max<int64_t>(1, std::min<int64_t>(slots_of(tm) / tiles, k_blocks / 4)));
+    };
+    // Long K on a small output: the split-K regime.  Pick the tile that moves
+    // the fewest bytes from L2 into shared memory, partials included.
+    const bool long_k = req_s == 0 && K > 0 && k_blocks >= 16 &&
+                        tiles_of(2 * kTileM, 256) * 2 <= slots_of(2 * kTileM);
+    const TileChoice *best = nullptr;
+    double best_cost = 0;
+    for (const TileChoice &c : kChoices) {
+        if (!allowed(c))
+            continue;
+        const int64_t tiles = tiles_of(c.tile_m, c.tile_n);
+        double cost;
         if (long_k) {
-            bn = 128;
+            const int sk = split_for(c.tile_m, c.tile_n);
+            const double stage = 2.0 * c.tile_m * kTileK + 2.0 * kTileK * c.tile_n;
+            cost = double(tiles) * sk * ceil_div(k_blocks, sk) * stage +
+                   (sk > 1 ? 2.0 * sk * double(M) * ldw * 4 * batch : 0.0);
         } else {
-            // Fewest waves of persistent CTAs, weighted by the relative cost of
-            // a narrow tile (more shared-memory traffic per flop).
-            double best = 0;
-            for (int cand : {256, 128, 64}) {
-                const double w = double((tiles_of(cand) + sms - 1) / sms) * cand *
-                                 (cand == 256 ? 1.0 : cand == 128 ? 1.1 : 1.3);
-                if (bn == 0 || w < best) {
-                    best = w;
-                    bn = cand;
-                }
-            }
+            // Fewest waves of persistent CTAs, weighted by the per-SM efficiency
+            // of the tile (a wave does tile_n columns of 128 rows on every SM).
+            const int64_t waves = (tiles + slots_of(c.tile_m) - 1) / slots_of(c.tile_m);
+            cost = double(waves) * c.tile_n / c.eff;
+        }
+        if (!best || cost < best_cost) {
+            best = &c;
+            best_cost = cost;
         }
     }
-    const int64_t tiles = tiles_of(bn);
-    if (req_s > 0) {
-        split = std::min(req_s, k_blocks);
-    } else if (K > 0 && tiles < sms) {
-        // Enough K ranges to put one unit on every SM, at least 4 k-blocks each.
-        const int64_t by_sms = sms / tiles;
-        const int64_t by_depth = k_blocks / 4;
-        split = int(std::max<int64_t>(1, std::min(by_sms, by_depth)));
-    }
-    if (K == 0)
-        split = 1;
-    const SmemBudget sb = smem_budget(bn);
-    pl->tile_m = kTileM;
+    if (!best)
+        return fail(GEMM_ERR_INVALID_VALUE, "no tile shape matches tile_m=%d tile_n=%d", req_m, req_n);
+    const int tm = best->tile_m, bn = best->tile_n;
+    const int split = K == 0 ? 1 : split_for(tm, bn);
+    const int64_t tiles = tiles_of(tm, bn);
+    const SmemBudget sb = smem_budget(tm, bn);
+    pl->tile_m = tm;
     pl->tile_n = bn;
     pl->tile_k = kTileK;
     pl->stages = sb.stages;
     pl->split_k = split;
-    pl->tiles_m = tiles_m;
-    pl->tiles_n = ceil_div(std::max<int64_t>(N, 1), bn);
+    pl->tiles_m = ceil_div(Mx, tm);
+    pl->tiles_n = ceil_div(Nx, bn);
     pl->k_blocks = k_blocks;
     pl->units = tiles * split;
     if (pl->units > kInt32Max)
         return fail(GEMM_ERR_INVALID_VALUE, "problem has too many tiles");
-    pl->grid = int(std::min<int64_t>(pl->units, sms));
-    pl->group_m = std::min(tiles_m, 8);
+    const int64_t ctas_per_unit = tm == 2 * kTileM ? 2 : 1;
+    pl->grid = int(std::min<int64_t>(pl->units, slots_of(tm)) * ctas_per_unit);
+    pl->group_m = std::min(pl->tiles_m, 8);
     pl->stage_bytes = sb.stage_bytes;
     pl->smem_bytes = sb.smem_bytes;
-    const int64_t ldw = (N + 3) / 4 * 4;
     pl->workspace_bytes = split > 1 ? batch * int64_t(split) * M * ldw * 4 : 0;
     return GEMM_OK;
 }
@@ -384,9 +420,9 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
     if (ds->smem_optin < pl.smem_bytes)
         return fail(GEMM_ERR_UNSUPPORTED_DEVICE, "device allows %d bytes of shared memory per block, the kernel needs %lld",
                     ds->smem_optin, (long long)pl.smem_bytes);
-    const int ti = tile_index(pl.tile_n);
+    const int ti = config_index(pl.tile_m, pl.tile_n);
     if (!ds->attrs_set[ti]) {
-        if ((e = set_kernel_attributes(pl.tile_n)) != cudaSuccess)
+        if ((e = set_kernel_attributes(pl.tile_m, pl.tile_n)) != cudaSuccess)
             return fail_cuda(e, "cudaFuncSetAttribute(max dynamic shared memory)");
         ds->attrs_set[ti] = true;
     }
@@ -433,7 +469,7 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
         if ((st = encode_3d(&map_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pr.C, map_cols, pr.M, pr.batch,
                             pr.ldc, sC, 32, 32, CU_TENSOR_MAP_L2_PROMOTION_NONE, "C")) != GEMM_OK)
             return st;
-        if ((e = launch_tcgen05_gemm(pl.tile_n, map_a, map_b, map_out, kp, pl.grid, stream)) != cudaSuccess)
+        if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, map_a, map_b, map_out, kp, pl.grid, stream)) != cudaSuccess)
             return fail_cuda(e, "GEMM kernel launch");
         return GEMM_OK;
     }
@@ -447,7 +483,7 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
                    pr.batch * pl.split_k, ldw, int64_t(pr.M) * ldw, 32, 32,
                    CU_TENSOR_MAP_L2_PROMOTION_NONE, "split-K workspace");
     if (st == GEMM_OK) {
-        if ((e = launch_tcgen05_gemm(pl.tile_n, map_a, map_b, map_out, kp, pl.grid, stream)) != cudaSuccess)
+        if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, map_a, map_b, map_out, kp, pl.grid, stream)) != cudaSuccess)
             st = fail_cuda(e, "GEMM kernel launch");
     }
     if (st == GEMM_OK) {
@@ -588,7 +624,7 @@ struct NoAllocDevice {
     int sms = 0;
     int smem_optin = 0;
     uint32_t *status = nullptr;
-    bool attrs_set[3] = {false, false, false};
+    bool attrs_set[5] = {false, false, false, false, false};
 };
 
 NoAllocDevice g_noalloc_devices[kMaxDevices];
@@ -665,6 +701,13 @@ extern "C" gemm_status_t gemm_f16_f32acc_splitk_noalloc(const uint16_t *A, const
     gemm_plan_info_t pl;
     if ((st = make_plan(M, N, K, 1, &o, nd->sms, &pl)) != GEMM_OK)
         return st;
+    if (split_k == 0 && uint64_t(pl.workspace_bytes) > kNoAllocScratchBytes) {
+        // The planner's split does not fit: take the largest split that does.
+        const int64_t per_split = M * ((N + 3) / 4 * 4) * 4;
+        o.split_k = int32_t(std::max<int64_t>(1, int64_t(kNoAllocScratchBytes) / per_split));
+        if ((st = make_plan(M, N, K, 1, &o, nd->sms, &pl)) != GEMM_OK)
+            return st;
+    }
     if (uint64_t(pl.workspace_bytes) > kNoAllocScratchBytes)
         return fail(GEMM_ERR_INVALID_VALUE,
                     "split-K partials need %lld bytes (S=%d x %lld x %lld f32); the static scratch "
@@ -674,9 +717,9 @@ extern "C" gemm_status_t gemm_f16_f32acc_splitk_noalloc(const uint16_t *A, const
     if (nd->smem_optin < pl.smem_bytes)
         return fail(GEMM_ERR_UNSUPPORTED_DEVICE, "device allows %d bytes of shared memory per block, the kernel needs %lld",
                     nd->smem_optin, (long long)pl.smem_bytes);
-    const int ti = tile_index(pl.tile_n);
+    const int ti = config_index(pl.tile_m, pl.tile_n);
     if (!nd->attrs_set[ti]) {
-        if ((e = set_kernel_attributes(pl.tile_n)) != cudaSuccess)
+        if ((e = set_kernel_attributes(pl.tile_m, pl.tile_n)) != cudaSuccess)
             return fail_cuda(e, "cudaFuncSetAttribute(max dynamic shared memory)");
         nd->attrs_set[ti] = true;
     }
@@ -719,7 +762,7 @@ extern "C" gemm_status_t gemm_f16_f32acc_splitk_noalloc(const uint16_t *A, const
         if ((st = encode_3d(&map_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, map_cols, M, 1, ldc,
                             M * ldc, 32, 32, CU_TENSOR_MAP_L2_PROMOTION_NONE, "C")) != GEMM_OK)
             return st;
-        if ((e = launch_tcgen05_gemm(pl.tile_n, map_a, map_b, map_out, kp, pl.grid, stream)) != cudaSuccess)
+        if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, map_a, map_b, map_out, kp, pl.grid, stream)) != cudaSuccess)
             return fail_cuda(e, "GEMM kernel launch");
         return GEMM_OK;
     }
@@ -731,7 +774,7 @@ extern "C" gemm_status_t gemm_f16_f32acc_splitk_noalloc(const uint16_t *A, const
                         ldw, M * ldw, 32, 32, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                         "static split-K scratch")) != GEMM_OK)
         return st;
-    if ((e = launch_tcgen05_gemm(pl.tile_n, map_a, map_b, map_out, kp, pl.grid, stream)) != cudaSuccess)
+    if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, map_a, map_b, map_out, kp, pl.grid, stream)) != cudaSuccess)
         return fail_cuda(e, "GEMM kernel launch");
     const int64_t threads = M * ((N + 3) / 4);
     const int grid = int(std::min<int64_t>((threads + 255) / 256, int64_t(nd->sms) * 8));

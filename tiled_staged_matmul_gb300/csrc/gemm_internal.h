@@ -47,11 +47,11 @@ struct SmemBudget {
     int smem_bytes;
     int tmem_cols;
 };
-SmemBudget smem_budget(int tile_n);
+SmemBudget smem_budget(int tile_m, int tile_n);
 
 // Kernel-side entry points (defined in gemm_kernels.cu).
-cudaError_t set_kernel_attributes(int tile_n);
-cudaError_t launch_tcgen05_gemm(int tile_n, const CUtensorMap &map_a, const CUtensorMap &map_b,
+cudaError_t set_kernel_attributes(int tile_m, int tile_n);
+cudaError_t launch_tcgen05_gemm(int tile_m, int tile_n, const CUtensorMap &map_a, const CUtensorMap &map_b,
                                 const CUtensorMap &map_out, const KernelParams &p, int grid,
                                 cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const float *W, float *C, int32_t M, int32_t N, int32_t S,

@@ -40,16 +40,23 @@ __device__ uint32_t g_status_word;
 
 // ------------------------------------------------------------- tile config
 
-template <int BN>
+// BN: columns of C per tile.  PAIR: the tile is computed by a CTA pair (a
+// 2-CTA cluster) with tcgen05 cta_group::2 -- 256 rows per tile, each CTA
+// staging its own 128 rows of A and its own BN/2 columns of B, and holding
+// its 128 rows of the accumulator.  Without PAIR one CTA does a 128-row tile.
+template <int BN, bool PAIR>
 struct TileCfg {
     static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
-    static constexpr int BM = kTileM;
+    static_assert(!PAIR || BN >= 128, "a CTA pair needs at least 64 B columns per CTA");
+    static constexpr int ROWS = kTileM;                    // rows of A / C per CTA
+    static constexpr int TILE_M = PAIR ? 2 * kTileM : kTileM;
     static constexpr int BK = kTileK;
-    static constexpr int A_BYTES = BM * BK * 2;            // 16 KiB
+    static constexpr int B_COLS = PAIR ? BN / 2 : BN;      // B columns staged by one CTA
+    static constexpr int A_BYTES = ROWS * BK * 2;          // 16 KiB
     static constexpr int B_BOX_BYTES = 64 * BK * 2;        // one 64-column box: 8 KiB
-    static constexpr int B_BOXES = BN / 64;
+    static constexpr int B_BOXES = B_COLS / 64;
     static constexpr int B_BYTES = B_BOXES * B_BOX_BYTES;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // per CTA
     static constexpr int EPI_WARPS = 4;
     static constexpr int EPI_BUF_BYTES = 32 * 32 * 4;      // one 32 x 32 f32 box
     static constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BUF_BYTES;
@@ -61,19 +68,21 @@ struct TileCfg {
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
     static_assert(STAGES >= 2, "the ring needs at least two stages");
     static constexpr int SMEM_BYTES = ALIGN_SLACK + STAGES * STAGE_BYTES + EPI_BYTES + CTRL_BYTES;
-    // Two accumulators of BN f32 columns each (a power of two >= 32).
+    // Two accumulators of BN f32 columns each per CTA (a power of two >= 32).
     static constexpr uint32_t TMEM_COLS = 2 * BN;
+    static constexpr uint32_t TEMPTY_ARRIVALS = PAIR ? 2 * EPI_WARPS : EPI_WARPS;
     static_assert(SMEM_BYTES > SMEM_LIMIT / 2, "one CTA per SM keeps TMEM allocation uncontended");
 };
 
 // Instruction descriptor of tcgen05.mma.kind::f16: D f32 (bits 4-5 = 1),
 // A and B f16 (bits 7-9, 10-12 = 0), A K-major (bit 15 = 0), B MN-major
 // (bit 16 = 1: B is row-major K x N, so N is contiguous), N >> 3 in bits
-// 17-22, M >> 4 in bits 24-28.
-template <int BN>
+// 17-22, M >> 4 in bits 24-28 (M = 256 for a CTA pair).
+template <int BN, bool PAIR>
 __device__ __forceinline__ constexpr uint32_t mma_idesc()
 {
-    return (1u << 4) | (1u << 16) | (uint32_t(BN >> 3) << 17) | (uint32_t(kTileM >> 4) << 24);
+    return (1u << 4) | (1u << 16) | (uint32_t(BN >> 3) << 17) |
+           (uint32_t(TileCfg<BN, PAIR>::TILE_M >> 4) << 24);
 }
 
 // Shared-memory matrix descriptor fields common to both operands: 128-byte
@@ -92,11 +101,10 @@ __device__ __forceinline__ uint64_t desc_a(uint32_t saddr)
 }
 
 // B: MN-major, each 64-column box is K rows of 128 bytes; boxes (64-column
-// atoms along N) are B_BOX_BYTES apart (leading byte offset).
-template <int BN>
+// atoms along N) are 8 KiB apart (leading byte offset).
 __device__ __forceinline__ uint64_t desc_b(uint32_t saddr)
 {
-    return desc_common() | (uint64_t(TileCfg<BN>::B_BOX_BYTES >> 4) << 16) |
+    return desc_common() | (uint64_t((64 * kTileK * 2) >> 4) << 16) |
            uint64_t((saddr & 0x3FFFFu) >> 4);
 }
 
@@ -114,7 +122,7 @@ struct Unit {
 // column by column, so CTAs running at the same time share A and B panels
 // in L2 ("Intel XPU Backend for Triton", section "Use Proper Type
 // Annotations": GROUP_SIZE_M in the GEMM signature).
-__device__ __forceinline__ Unit decode_unit(int64_t u, const KernelParams &p, int bn)
+__device__ __forceinline__ Unit decode_unit(int64_t u, const KernelParams &p, int tile_m, int bn)
 {
     const int64_t tiles = int64_t(p.tiles_m) * p.tiles_n;
     const int64_t z = u / tiles;
@@ -127,7 +135,7 @@ __device__ __forceinline__ Unit decode_unit(int64_t u, const KernelParams &p, in
     const int32_t rows_in_group = min(p.tiles_m - first_m, p.group_m);
     const int64_t r = t - g * group;
     Unit w;
-    w.m0 = (first_m + int32_t(r % rows_in_group)) * kTileM;
+    w.m0 = (first_m + int32_t(r % rows_in_group)) * tile_m;
     w.n0 = int32_t(r / rows_in_group) * bn;
     w.z_in = b;
     w.z_out = int32_t(z);  // == b when split_k == 1
@@ -136,12 +144,20 @@ __device__ __forceinline__ Unit decode_unit(int64_t u, const KernelParams &p, in
     return w;
 }
 
+// Where a CTA records that it gives up: its own abort flag and, in a CTA
+// pair, the peer's (a shared::cluster address), so that both wind down.
+struct AbortFlags {
+    volatile uint32_t *local;
+    uint32_t peer;       // shared::cluster address of the peer's flag (0: none)
+    uint64_t timeout_ns;
+    uint32_t *status;
+};
+
 // Bounded mbarrier wait.  Returns false if the CTA's abort flag is raised
-// (when `honor_abort`) or if `timeout_ns` passes; a timeout raises the flag
+// (when `honor_abort`) or if `timeout_ns` passes; a timeout raises the flags
 // and ORs `who` into the device status word.
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
-                                             volatile uint32_t *abort_flag, uint64_t timeout_ns,
-                                             uint32_t *status, uint32_t who, bool honor_abort)
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const AbortFlags &af,
+                                             uint32_t who, bool honor_abort)
 {
     if (ptx::mbar_try_wait(bar, parity))
         return true;
@@ -150,11 +166,13 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
         if (ptx::mbar_try_wait(bar, parity))
             return true;
         if ((it & 31u) == 0) {
-            if (honor_abort && *abort_flag)
+            if (honor_abort && *af.local)
                 return false;
-            if (ptx::globaltimer_ns() - t0 > timeout_ns) {
-                *abort_flag = 1u;
-                atomicOr(status, who);
+            if (ptx::globaltimer_ns() - t0 > af.timeout_ns) {
+                *af.local = 1u;
+                if (af.peer)
+                    ptx::st_cluster_u32(af.peer, 1u);
+                atomicOr(af.status, who);
                 return false;
             }
         }
@@ -163,13 +181,13 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
 
 // ------------------------------------------------------------- the GEMM
 
-template <int BN>
+template <int BN, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     tsm_gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a,
                             const __grid_constant__ CUtensorMap map_b,
                             const __grid_constant__ CUtensorMap map_out, const KernelParams p)
 {
-    using Cfg = TileCfg<BN>;
+    using Cfg = TileCfg<BN, PAIR>;
     constexpr int S = Cfg::STAGES;
 
     extern __shared__ uint8_t smem_raw[];
@@ -181,18 +199,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *const ctrl_ptr = base_ptr + (ctrl - base);
 
     // Control block: barriers (8 bytes each), then the TMEM address and the
-    // CTA's abort flag.
+    // CTA's abort flag.  In a CTA pair `full` and `tempty` are used in the
+    // leader only; `empty` and `tfull` in both (the leader's MMA commits
+    // arrive on both CTAs' copies).
     const uint32_t full0 = ctrl;                     // [S]  TMA bytes landed in slot s
     const uint32_t empty0 = ctrl + 8u * S;           // [S]  MMAs reading slot s are done
     const uint32_t tfull0 = ctrl + 16u * S;          // [2]  accumulator b is complete
     const uint32_t tempty0 = ctrl + 16u * S + 16u;   // [2]  epilogue has read accumulator b
-    const uint32_t done_bar = ctrl + 16u * S + 32u;  // all MMAs of this CTA completed
+    const uint32_t done_bar = ctrl + 16u * S + 32u;  // all MMAs of this CTA (pair) completed
     const uint32_t stall_bar = ctrl + 16u * S + 40u; // never signalled (test hook)
     uint32_t *const tmem_slot = reinterpret_cast<uint32_t *>(ctrl_ptr + 16 * S + 48);
     volatile uint32_t *const abort_flag = tmem_slot + 1;
 
     const int warp = int(threadIdx.x >> 5);
     const int lane = int(threadIdx.x & 31);
+    const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;  // 0: the pair's MMA issuer
+    const bool leader = rank == 0;
+    const int64_t cluster = PAIR ? (blockIdx.x >> 1) : blockIdx.x;
+    const int64_t nclusters = PAIR ? (gridDim.x >> 1) : gridDim.x;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -201,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(tfull0 + 8u * b, 1);
-            ptx::mbar_init(tempty0 + 8u * b, Cfg::EPI_WARPS);
+            ptx::mbar_init(tempty0 + 8u * b, Cfg::TEMPTY_ARRIVALS);
         }
         ptx::mbar_init(done_bar, 1);
         ptx::mbar_init(stall_bar, 1);
@@ -211,37 +235,62 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tensormap(&map_b);
         ptx::prefetch_tensormap(&map_out);
     }
+    if constexpr (PAIR)
+        ptx::cluster_sync();  // the peer's barriers exist before anything signals them
     if (warp == 1) {
-        ptx::tmem_alloc(ptx::smem_addr(tmem_slot), Cfg::TMEM_COLS);
-        ptx::tmem_relinquish();
+        ptx::tmem_alloc<PAIR>(ptx::smem_addr(tmem_slot), Cfg::TMEM_COLS);
+        ptx::tmem_relinquish<PAIR>();
     }
     ptx::tc_fence_before_sync();
     __syncthreads();
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
+    AbortFlags af;
+    af.local = abort_flag;
+    af.peer = PAIR ? ptx::mapa_shared(ptx::smem_addr(const_cast<uint32_t *>(abort_flag)), rank ^ 1u)
+                   : 0u;
+    af.timeout_ns = p.timeout_ns;
+    af.status = p.status;
+    // The leader's `full` and `tempty` barriers as shared::cluster addresses.
+    const uint32_t full_lead0 = PAIR ? ptx::mapa_shared(full0, 0) : full0;
+    const uint32_t tempty_lead0 = PAIR ? ptx::mapa_shared(tempty0, 0) : tempty0;
+    const int32_t row_off = PAIR ? int32_t(rank) * kTileM : 0;       // this CTA's rows
+    const int32_t col_off = PAIR ? int32_t(rank) * Cfg::B_COLS : 0;  // this CTA's B columns
+
     if (warp == 0) {
         if (lane == 0) {
-            // ---------------- TMA producer
+            // ---------------- TMA producer (each CTA fills its own ring)
             uint32_t stage = 0, phase = 0;
             uint64_t issued = 0;
             bool ok = true;
-            for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-                const Unit w = decode_unit(u, p, BN);
+            for (int64_t u = cluster; ok && u < p.num_units; u += nclusters) {
+                const Unit w = decode_unit(u, p, Cfg::TILE_M, BN);
                 for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!wait_bounded(empty0 + 8u * stage, phase ^ 1u, abort_flag, p.timeout_ns,
-                                      p.status, kStatusProducer, true)) {
+                    if (!wait_bounded(empty0 + 8u * stage, phase ^ 1u, af, kStatusProducer, true)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t fb = full0 + 8u * stage;
                     const uint32_t sa = base + stage * Cfg::STAGE_BYTES;
-                    ptx::mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES);
-                    ptx::tma_load_3d(sa, &map_a, fb, kb * kTileK, w.m0, w.z_in);
+                    if constexpr (PAIR) {
+                        // Both CTAs' bytes are counted on the leader's barrier.
+                        const uint32_t fb = full_lead0 + 8u * stage;
+                        if (leader)
+                            ptx::mbar_arrive_expect_tx(full0 + 8u * stage, 2 * Cfg::STAGE_BYTES);
+                        ptx::tma_load_3d_pair(sa, &map_a, fb, kb * kTileK, w.m0 + row_off, w.z_in);
 #pragma unroll
-                    for (int j = 0; j < Cfg::B_BOXES; ++j)
-                        ptx::tma_load_3d(sa + Cfg::A_BYTES + j * Cfg::B_BOX_BYTES, &map_b, fb,
-                                         w.n0 + 64 * j, kb * kTileK, w.z_in);
+                        for (int j = 0; j < Cfg::B_BOXES; ++j)
+                            ptx::tma_load_3d_pair(sa + Cfg::A_BYTES + j * Cfg::B_BOX_BYTES, &map_b,
+                                                  fb, w.n0 + col_off + 64 * j, kb * kTileK, w.z_in);
+                    } else {
+                        const uint32_t fb = full0 + 8u * stage;
+                        ptx::mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES);
+                        ptx::tma_load_3d(sa, &map_a, fb, kb * kTileK, w.m0, w.z_in);
+#pragma unroll
+                        for (int j = 0; j < Cfg::B_BOXES; ++j)
+                            ptx::tma_load_3d(sa + Cfg::A_BYTES + j * Cfg::B_BOX_BYTES, &map_b, fb,
+                                             w.n0 + 64 * j, kb * kTileK, w.z_in);
+                    }
                     ++issued;
                     if (++stage == S) {
                         stage = 0;
@@ -249,33 +298,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            // Wait (bounded) for this thread's last loads to land, so that no
-            // TMA write into shared memory outlives the CTA.
-            const uint64_t last = issued < uint64_t(S) ? issued : uint64_t(S);
-            for (uint64_t i = 0; i < last; ++i) {
-                const uint64_t t = issued - 1 - i;
-                wait_bounded(full0 + 8u * uint32_t(t % S), uint32_t((t / S) & 1u), abort_flag,
-                             p.timeout_ns, p.status, kStatusDrain, false);
+            if (leader) {
+                // Wait (bounded) for the last loads to land, so that no TMA
+                // write into shared memory outlives the CTA.  In a pair the
+                // leader's barrier also counts the peer's bytes.
+                const uint64_t last = issued < uint64_t(S) ? issued : uint64_t(S);
+                for (uint64_t i = 0; i < last; ++i) {
+                    const uint64_t t = issued - 1 - i;
+                    wait_bounded(full0 + 8u * uint32_t(t % S), uint32_t((t / S) & 1u), af,
+                                 kStatusDrain, false);
+                }
+            } else if (*abort_flag) {
+                // The peer has no barrier of its own for its loads: after an
+                // abort give them a fixed grace period to land.
+                const uint64_t t0 = ptx::globaltimer_ns();
+                while (ptx::globaltimer_ns() - t0 < 200000ull) {
+                }
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ---------------- MMA issuer (one thread)
-            constexpr uint32_t idesc = mma_idesc<BN>();
+        if (lane == 0 && leader) {
+            // ---------------- MMA issuer (one thread; the leader of a pair)
+            constexpr uint32_t idesc = mma_idesc<BN, PAIR>();
+            constexpr uint16_t both = PAIR ? 3 : 1;
             uint32_t stage = 0, phase = 0, abuf = 0, aphase = 0;
             bool ok = true;
-            for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-                const Unit w = decode_unit(u, p, BN);
-                if (!wait_bounded(tempty0 + 8u * abuf, aphase ^ 1u, abort_flag, p.timeout_ns,
-                                  p.status, kStatusMma, true)) {
+            for (int64_t u = cluster; ok && u < p.num_units; u += nclusters) {
+                const Unit w = decode_unit(u, p, Cfg::TILE_M, BN);
+                if (!wait_bounded(tempty0 + 8u * abuf, aphase ^ 1u, af, kStatusMma, true)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after_sync();
                 const uint32_t d = tmem_base + abuf * uint32_t(BN);
                 for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!wait_bounded(full0 + 8u * stage, phase, abort_flag, p.timeout_ns,
-                                      p.status, kStatusMma, true)) {
+                    if (!wait_bounded(full0 + 8u * stage, phase, af, kStatusMma, true)) {
                         ok = false;
                         break;
                     }
@@ -286,10 +343,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int kk = 0; kk < kTileK / 16; ++kk) {
                         // A: advance 16 f16 = 32 bytes along the swizzled row.
                         // B: advance 16 K rows = 2048 bytes.
-                        ptx::mma_f16_ss(d, desc_a(sa + 32u * kk), desc_b<BN>(sb + 2048u * kk),
-                                        idesc, (kb > w.kb0 || kk > 0) ? 1u : 0u);
+                        ptx::mma_f16_ss<PAIR>(d, desc_a(sa + 32u * kk), desc_b(sb + 2048u * kk),
+                                              idesc, (kb > w.kb0 || kk > 0) ? 1u : 0u);
                     }
-                    ptx::mma_commit(empty0 + 8u * stage);  // slot free once these MMAs finish
+                    ptx::mma_commit<PAIR>(empty0 + 8u * stage, both);  // slot free in both CTAs
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
@@ -297,15 +354,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!ok)
                     break;
-                ptx::mma_commit(tfull0 + 8u * abuf);  // accumulator ready for the epilogue
+                ptx::mma_commit<PAIR>(tfull0 + 8u * abuf, both);  // accumulator ready
                 if (++abuf == 2) {
                     abuf = 0;
                     aphase ^= 1u;
                 }
             }
             // Every MMA this thread issued must finish before TMEM is freed.
-            ptx::mma_commit(done_bar);
-            wait_bounded(done_bar, 0, abort_flag, p.timeout_ns, p.status, kStatusDrain, false);
+            ptx::mma_commit<PAIR>(done_bar, 1);
+            wait_bounded(done_bar, 0, af, kStatusDrain, false);
         }
     } else {
         // ---------------- epilogue: warps 2..5, TMEM lane quarter = warp % 4
@@ -313,17 +370,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;
         const uint32_t bufs = epi0 + uint32_t(e) * 2u * Cfg::EPI_BUF_BYTES;
         uint32_t abuf = 0, aphase = 0, sbuf = 0;
-        for (int64_t u = blockIdx.x; u < p.num_units; u += gridDim.x) {
-            const Unit w = decode_unit(u, p, BN);
-            bool got = wait_bounded(tfull0 + 8u * abuf, aphase, abort_flag, p.timeout_ns, p.status,
-                                    kStatusEpilogue, true);
+        for (int64_t u = cluster; u < p.num_units; u += nclusters) {
+            const Unit w = decode_unit(u, p, Cfg::TILE_M, BN);
+            bool got = wait_bounded(tfull0 + 8u * abuf, aphase, af, kStatusEpilogue, true);
             if (p.inject_stall && got)
-                got = wait_bounded(stall_bar, 0, abort_flag, p.timeout_ns, p.status,
-                                   kStatusEpilogue, true);
+                got = wait_bounded(stall_bar, 0, af, kStatusEpilogue, true);
             if (!__all_sync(0xffffffffu, got))
                 break;
             ptx::tc_fence_after_sync();
-            const int32_t row0 = w.m0 + 32 * q;
+            const int32_t row0 = w.m0 + row_off + 32 * q;
             int nch = 0;
             if (row0 < p.M) {
                 const int live = (p.N - w.n0 + 31) / 32;
@@ -338,8 +393,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // Last read of this accumulator: hand it back to the MMA issuer.
                     ptx::tc_fence_before_sync();
                     __syncwarp();
-                    if (lane == 0)
-                        ptx::mbar_arrive(tempty0 + 8u * abuf);
+                    if (lane == 0) {
+                        if constexpr (PAIR)
+                            ptx::mbar_arrive_cluster(tempty_lead0 + 8u * abuf);
+                        else
+                            ptx::mbar_arrive(tempty0 + 8u * abuf);
+                    }
                 }
                 const int32_t col0 = w.n0 + 32 * c;
                 if (col0 < p.n_tma) {
@@ -379,8 +438,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (nch == 0) {
                 ptx::tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0)
-                    ptx::mbar_arrive(tempty0 + 8u * abuf);
+                if (lane == 0) {
+                    if constexpr (PAIR)
+                        ptx::mbar_arrive_cluster(tempty_lead0 + 8u * abuf);
+                    else
+                        ptx::mbar_arrive(tempty0 + 8u * abuf);
+                }
             }
             if (++abuf == 2) {
                 abuf = 0;
@@ -394,10 +457,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     ptx::tc_fence_before_sync();
     __syncthreads();
+    if constexpr (PAIR)
+        ptx::cluster_sync();  // neither CTA leaves while the other may still signal it
     if (warp == 1) {
         __syncwarp();
         ptx::tc_fence_after_sync();
-        ptx::tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+        ptx::tmem_dealloc<PAIR>(tmem_base, Cfg::TMEM_COLS);
     }
 }
 
@@ -463,62 +528,90 @@ __global__ void __launch_bounds__(256)
 
 // ------------------------------------------------------------- host side
 
-template <int BN>
+template <int BN, bool PAIR>
 static SmemBudget budget_of()
 {
-    using Cfg = TileCfg<BN>;
+    using Cfg = TileCfg<BN, PAIR>;
     return SmemBudget{Cfg::STAGES, Cfg::STAGE_BYTES, Cfg::SMEM_BYTES, int(Cfg::TMEM_COLS)};
 }
 
-SmemBudget smem_budget(int tile_n)
+SmemBudget smem_budget(int tile_m, int tile_n)
 {
+    if (tile_m == 2 * kTileM)
+        return tile_n == 128 ? budget_of<128, true>() : budget_of<256, true>();
     switch (tile_n) {
-    case 64: return budget_of<64>();
-    case 128: return budget_of<128>();
-    default: return budget_of<256>();
+    case 64: return budget_of<64, false>();
+    case 128: return budget_of<128, false>();
+    default: return budget_of<256, false>();
     }
 }
 
-template <int BN>
+template <int BN, bool PAIR>
 static cudaError_t set_attr()
 {
-    return cudaFuncSetAttribute(tsm_gemm_tcgen05_kernel<BN>,
+    return cudaFuncSetAttribute(tsm_gemm_tcgen05_kernel<BN, PAIR>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                TileCfg<BN>::SMEM_BYTES);
+                                TileCfg<BN, PAIR>::SMEM_BYTES);
 }
 
-cudaError_t set_kernel_attributes(int tile_n)
+cudaError_t set_kernel_attributes(int tile_m, int tile_n)
 {
+    if (tile_m == 2 * kTileM) {
+        switch (tile_n) {
+        case 128: return set_attr<128, true>();
+        case 256: return set_attr<256, true>();
+        default: return cudaErrorInvalidValue;
+        }
+    }
     switch (tile_n) {
-    case 64: return set_attr<64>();
-    case 128: return set_attr<128>();
-    case 256: return set_attr<256>();
+    case 64: return set_attr<64, false>();
+    case 128: return set_attr<128, false>();
+    case 256: return set_attr<256, false>();
     default: return cudaErrorInvalidValue;
     }
 }
 
-template <int BN>
+template <int BN, bool PAIR>
 static cudaError_t launch_bn(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o,
                              const KernelParams &p, int grid, cudaStream_t stream)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(grid), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = TileCfg<BN>::SMEM_BYTES;
+    cfg.dynamicSmemBytes = TileCfg<BN, PAIR>::SMEM_BYTES;
     cfg.stream = stream;
-    cfg.attrs = nullptr;
-    cfg.numAttrs = 0;
-    return cudaLaunchKernelEx(&cfg, tsm_gemm_tcgen05_kernel<BN>, a, b, o, p);
+    cudaLaunchAttribute attr[1];
+    if (PAIR) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    } else {
+        cfg.attrs = nullptr;
+        cfg.numAttrs = 0;
+    }
+    return cudaLaunchKernelEx(&cfg, tsm_gemm_tcgen05_kernel<BN, PAIR>, a, b, o, p);
 }
 
-cudaError_t launch_tcgen05_gemm(int tile_n, const CUtensorMap &map_a, const CUtensorMap &map_b,
-                                const CUtensorMap &map_out, const KernelParams &p, int grid,
-                                cudaStream_t stream)
+cudaError_t launch_tcgen05_gemm(int tile_m, int tile_n, const CUtensorMap &map_a,
+                                const CUtensorMap &map_b, const CUtensorMap &map_out,
+                                const KernelParams &p, int grid, cudaStream_t stream)
 {
+    if (tile_m == 2 * kTileM) {
+        if (grid % 2)
+            return cudaErrorInvalidValue;
+        switch (tile_n) {
+        case 128: return launch_bn<128, true>(map_a, map_b, map_out, p, grid, stream);
+        case 256: return launch_bn<256, true>(map_a, map_b, map_out, p, grid, stream);
+        default: return cudaErrorInvalidValue;
+        }
+    }
     switch (tile_n) {
-    case 64: return launch_bn<64>(map_a, map_b, map_out, p, grid, stream);
-    case 128: return launch_bn<128>(map_a, map_b, map_out, p, grid, stream);
-    case 256: return launch_bn<256>(map_a, map_b, map_out, p, grid, stream);
+    case 64: return launch_bn<64, false>(map_a, map_b, map_out, p, grid, stream);
+    case 128: return launch_bn<128, false>(map_a, map_b, map_out, p, grid, stream);
+    case 256: return launch_bn<256, false>(map_a, map_b, map_out, p, grid, stream);
     default: return cudaErrorInvalidValue;
     }
 }
