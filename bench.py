@@ -204,6 +204,15 @@ def run_ours(args, rank, local_rank, world):
     working_set = 2 * w.M * w.K + 2 * w.K * w.N + 4 * w.M * w.N
     flush = working_set < 2 * L2_BYTES
     scrub = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    sweep = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    sink = torch.empty(1, dtype=torch.float32, device=dev) if flush else None
+
+    def flush_l2():
+        # Write a buffer twice the L2, then read another one: the inputs are
+        # evicted and the L2 is left holding clean lines, so the timed GEMM
+        # does not pay for writing back the scrub's dirty lines.
+        scrub.zero_()
+        torch.sum(sweep, dim=0, keepdim=True, out=sink)
 
     def call():
         binding.check(binding.gemm_f16_f32acc(A.data_ptr(), B.data_ptr(), C.data_ptr(),
@@ -211,7 +220,7 @@ def run_ours(args, rank, local_rank, world):
 
     for _ in range(max(args.warmup, 3)):
         if flush:
-            scrub.zero_()
+            flush_l2()
         call()
     binding.check(binding.gemm_get_device_status(stream.cuda_stream))
     torch.cuda.synchronize()
@@ -226,7 +235,7 @@ def run_ours(args, rank, local_rank, world):
     t0 = time.time()
     for i in range(args.steps):
         if flush:
-            scrub.zero_()
+            flush_l2()
         starts[i].record(stream)
         call()
         ends[i].record(stream)
@@ -278,7 +287,7 @@ def run_ours(args, rank, local_rank, world):
                    "dist": w.dist, "seed": w.seed, "accumulate": "f32",
                    "tile_n": plan["tile_n"], "split_k": plan["split_k"],
                    "stages": plan["stages"], "grid": plan["grid"],
-                   "l2": "flushed before every step" if flush else
+                   "l2": "flushed before every step (write 2xL2, then read 2xL2)" if flush else
                          f"inputs+output {working_set / 2**20:.0f} MiB > L2, no flush",
                    "parallelism": f"replicas x{world}"},
         "gpu_launches": args.steps * launches_per_call,

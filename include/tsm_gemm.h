@@ -98,6 +98,20 @@ typedef struct gemm_options {
     int32_t tile_m;     /* 0: planner's choice; 128: one CTA per tile; 256: a CTA pair per
                            tile (a 2-CTA cluster issuing tcgen05 cta_group::2 MMAs; needs
                            tile_n 128 or 256) */
+    int32_t splitk_reduce; /* 0 or 2: sum split-K partials inside the GEMM kernel when the
+                              plan allows it (every cluster owns one unit), else in a second
+                              kernel; 1: always the second kernel.  Both sum the splits in
+                              ascending order, so the results are bitwise the same. */
+    int32_t l2_prefetch; /* 0 or 1: off; 2: on -- each unit first asks L2 for its whole K
+                            range of A and B (measured slower on GB300, kept for study) */
+    int32_t reserved;   /* 0 */
+    uint64_t *trace;    /* NULL, or a device buffer of grid x 8 uint64 (grid from gemm_plan):
+                           per CTA, %globaltimer stamps (ns) of kernel entry, setup done,
+                           first k-block landed, last MMA issued, last accumulator ready,
+                           output written, in-kernel split-K sum written, exit (0 where a
+                           stage does not apply to the CTA's role).  For profiling only:
+                           the timer ticks in steps of about a quarter microsecond and
+                           stamps of different warps are not ordered within a step. */
 } gemm_options_t;
 
 /* What the planner chose for a problem (see gemm_plan). */
@@ -117,6 +131,7 @@ typedef struct gemm_plan_info {
     int64_t stage_bytes;  /* shared memory of one k-block: A tile + B tile */
     int64_t smem_bytes;   /* dynamic shared memory of one CTA */
     int64_t workspace_bytes; /* split-K partials (0 when split_k == 1) */
+    int32_t fused_reduce; /* 1: the partials are summed inside the GEMM kernel */
 } gemm_plan_info_t;
 
 /* C = A . B for one matrix.

@@ -149,7 +149,17 @@ def test_plan_invariants(b, M, N, K):
     else:
         assert p["grid"] == 2 * min(p["units"], SMS // 2)
     ldw = -(-N // 4) * 4
-    assert p["workspace_bytes"] == (p["split_k"] * M * ldw * 4 if p["split_k"] > 1 else 0)
+    if p["split_k"] == 1:
+        assert p["workspace_bytes"] == 0 and not p["fused_reduce"]
+    elif p["fused_reduce"]:
+        # the separate reduction's partials plus one arrival counter per tile;
+        # every cluster owns exactly one unit
+        tiles = p["tiles_m"] * p["tiles_n"]
+        counters = -(-(tiles * 4) // 16) * 16
+        assert p["workspace_bytes"] == p["split_k"] * M * ldw * 4 + counters
+        assert p["units"] * (2 if p["tile_m"] == 256 else 1) == p["grid"]
+    else:
+        assert p["workspace_bytes"] == p["split_k"] * M * ldw * 4
 
 
 def test_long_K_small_output_splits_K(b):
@@ -172,3 +182,18 @@ def test_forced_split_is_clamped_to_k_blocks(b):
 def test_bad_options_rejected(b):
     with pytest.raises(b.GemmError):
         b.gemm_plan(128, 128, 128, 1, b._opts(tile_n=96), SMS)
+
+
+def test_separate_reduce_can_be_forced(b):
+    p = b.gemm_plan(256, 256, 65536, 1, b._opts(splitk_reduce=1), SMS)
+    assert p["split_k"] > 1 and not p["fused_reduce"]
+    assert p["workspace_bytes"] == p["split_k"] * 256 * 256 * 4
+    with pytest.raises(b.GemmError):
+        b.gemm_plan(256, 256, 65536, 1, b._opts(splitk_reduce=3), SMS)
+
+
+def test_more_units_than_clusters_never_fuses(b):
+    # 64 splits of four 128 x 128 tiles = 256 units > 152 CTAs: a CTA would
+    # wait on a split that only it can compute later, so the sum is a second kernel.
+    p = b.gemm_plan(256, 256, 65536, 1, b._opts(split_k=64, tile_m=128, tile_n=128), SMS)
+    assert p["units"] > SMS and not p["fused_reduce"]

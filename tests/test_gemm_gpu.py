@@ -102,6 +102,32 @@ def test_long_K_integer_bit_exact_for_every_split(b):
             check_exact(C.numpy(), ref)
 
 
+@pytest.mark.parametrize("M,N,K,tile_m,tile_n,split_k", [
+    (256, 256, 65536, 256, 256, 0), (256, 256, 65536, 128, 128, 38), (300, 250, 20000, 256, 128, 0),
+    (130, 70, 9000, 128, 64, 11), (1000, 1000, 1000, 256, 128, 2)])
+def test_in_kernel_and_separate_reduce_agree_bitwise(b, M, N, K, tile_m, tile_n, split_k):
+    """Both reductions sum the splits in ascending order, so they agree bit for bit."""
+    plan = b.gemm_plan(M, N, K, 1, b.GemmOptions(split_k, tile_n, 0, 0, tile_m, 0))
+    assert plan["split_k"] > 1 and plan["fused_reduce"]
+    A, B = synthetic.operands(M, N, K, "uniform", seed=M + K)
+    C_in, dC = run_gemm(b, A, B, split_k=split_k, tile_m=tile_m, tile_n=tile_n, splitk_reduce=2)
+    C_sep, _ = run_gemm(b, A, B, split_k=split_k, tile_m=tile_m, tile_n=tile_n, splitk_reduce=1)
+    assert torch.equal(C_in, C_sep)
+    assert dC.outside_untouched()
+    check_tolerance(C_in.numpy(), ref_of(A, B), K)
+
+
+def test_in_kernel_reduce_batched(b):
+    M, N, K, batch = 200, 136, 12000, 3
+    A, B = synthetic.operands(M, N, K, "int4", seed=23, batch=batch)
+    plan = b.gemm_plan(M, N, K, batch)
+    assert plan["split_k"] > 1 and plan["fused_reduce"]
+    C, dC = run_gemm(b, A, B, batch=batch, sA=M * K + 64, sB=K * 136 + 64, sC=M * 136 + 20)
+    for i in range(batch):
+        check_exact(C[i].numpy(), ref_of(A[i], B[i]))
+    assert dC.outside_untouched()
+
+
 @pytest.mark.parametrize("tile_m,tile_n", TILES)
 def test_every_tile_shape_on_random_inputs(b, tile_m, tile_n):
     A, B = synthetic.operands(700, 900, 1500, "normal", seed=tile_m + tile_n)

@@ -29,7 +29,9 @@ GEMM_ERR_DEVICE_TIMEOUT = 6
 class GemmOptions(ctypes.Structure):
     _fields_ = [("split_k", ctypes.c_int32), ("tile_n", ctypes.c_int32),
                 ("timeout_ms", ctypes.c_int32), ("inject_stall", ctypes.c_int32),
-                ("tile_m", ctypes.c_int32)]
+                ("tile_m", ctypes.c_int32), ("splitk_reduce", ctypes.c_int32),
+                ("l2_prefetch", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("trace", ctypes.c_void_p)]
 
 
 class GemmPlanInfo(ctypes.Structure):
@@ -39,7 +41,8 @@ class GemmPlanInfo(ctypes.Structure):
                 ("tiles_n", ctypes.c_int32), ("k_blocks", ctypes.c_int32),
                 ("units", ctypes.c_int64), ("grid", ctypes.c_int32),
                 ("group_m", ctypes.c_int32), ("stage_bytes", ctypes.c_int64),
-                ("smem_bytes", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64)]
+                ("smem_bytes", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
+                ("fused_reduce", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -86,8 +89,9 @@ def _load() -> ctypes.CDLL:
 _lib = _load()
 
 
-def _opts(split_k=0, tile_n=0, timeout_ms=0, inject_stall=0, tile_m=0):
-    return GemmOptions(int(split_k), int(tile_n), int(timeout_ms), int(inject_stall), int(tile_m))
+def _opts(split_k=0, tile_n=0, timeout_ms=0, inject_stall=0, tile_m=0, splitk_reduce=0):
+    return GemmOptions(int(split_k), int(tile_n), int(timeout_ms), int(inject_stall), int(tile_m),
+                       int(splitk_reduce))
 
 
 # ------------------------------------------------------------------ raw C names

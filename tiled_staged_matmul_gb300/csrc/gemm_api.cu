@@ -278,6 +278,8 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const ge
     const int req_s = o ? o->split_k : 0;
     if (req_s < 0)
         return fail(GEMM_ERR_INVALID_VALUE, "split_k must be >= 0");
+    if (o && (o->splitk_reduce < 0 || o->splitk_reduce > 2))
+        return fail(GEMM_ERR_INVALID_VALUE, "splitk_reduce must be 0, 1 or 2");
     const int k_blocks = ceil_div(std::max<int64_t>(K, 1), kTileK);
     const int64_t Mx = std::max<int64_t>(M, 1), Nx = std::max<int64_t>(N, 1);
     const int64_t ldw = (N + 3) / 4 * 4;
@@ -310,8 +312,10 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const ge
         if (long_k) {
             const int sk = split_for(c.tile_m, c.tile_n);
             const double stage = 2.0 * c.tile_m * kTileK + 2.0 * kTileK * c.tile_n;
+            // Partial sums cost about four times their bytes (written, waited
+            // for, read back and summed), measured on the 256 x 256 x 65536 case.
             cost = double(tiles) * sk * ceil_div(k_blocks, sk) * stage +
-                   (sk > 1 ? 2.0 * sk * double(M) * ldw * 4 * batch : 0.0);
+                   (sk > 1 ? 4.0 * 2.0 * sk * double(M) * ldw * 4 * batch : 0.0);
         } else {
             // Fewest waves of persistent CTAs, weighted by the per-SM efficiency
             // of the tile (a wave does tile_n columns of 128 rows on every SM).
@@ -345,7 +349,20 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const ge
     pl->group_m = std::min(pl->tiles_m, 8);
     pl->stage_bytes = sb.stage_bytes;
     pl->smem_bytes = sb.smem_bytes;
-    pl->workspace_bytes = split > 1 ? batch * int64_t(split) * M * ldw * 4 : 0;
+    // Split-K partials are summed inside the GEMM kernel when every cluster
+    // owns exactly one unit (so all splits of a tile run at once) and one
+    // reducer's rows of every split fit the idle shared-memory ring (and a
+    // TMA box: at most 256 splits).
+    const int64_t reducers = int64_t(split) * ctas_per_unit;
+    const int64_t rows_per = (tm + reducers - 1) / reducers;
+    const int req_r = o ? o->splitk_reduce : 0;
+    pl->fused_reduce = split > 1 && req_r != 1 && split <= 256 && pl->units <= slots_of(tm) &&
+                       rows_per * bn * 4 * split <= int64_t(sb.stages) * sb.stage_bytes;
+    if (split == 1)
+        pl->workspace_bytes = 0;
+    else  // [batch * split][M][ldw] f32, and for the in-kernel sum a counter per tile
+        pl->workspace_bytes = batch * int64_t(split) * M * ldw * 4 +
+                              (pl->fused_reduce ? (tiles * 4 + 15) / 16 * 16 : 0);
     return GEMM_OK;
 }
 
@@ -354,17 +371,18 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const ge
 gemm_status_t encode_3d(CUtensorMap *map, CUtensorMapDataType dt, int elem, const void *base,
                         int64_t cols, int64_t rows, int64_t mats, int64_t ld, int64_t stride,
                         uint32_t box_cols, uint32_t box_rows, CUtensorMapL2promotion promo,
-                        const char *name)
+                        const char *name, uint32_t box_mats = 1,
+                        CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B)
 {
     Driver &d = driver();
     if (!d.loaded)
         return fail(GEMM_ERR_CUDA, "%s", d.error.c_str());
     const cuuint64_t dims[3] = {cuuint64_t(cols), cuuint64_t(rows), cuuint64_t(mats)};
     const cuuint64_t strides[2] = {cuuint64_t(ld) * elem, cuuint64_t(stride) * elem};
-    const cuuint32_t box[3] = {box_cols, box_rows, 1};
+    const cuuint32_t box[3] = {box_cols, box_rows, box_mats};
     const cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = d.encode_tiled(map, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
-                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, promo,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, promo,
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(GEMM_ERR_INVALID_VALUE, "tensor map for %s rejected (CUresult %d)", name, int(r));
@@ -451,6 +469,7 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
     kp.num_units = pl.units;
     kp.timeout_ns = uint64_t(timeout_ns_for(o, pl));
     kp.status = ds->status;
+    kp.trace = o ? reinterpret_cast<unsigned long long *>(o->trace) : nullptr;
 
     kp.n_tma = N;
     kp.tail = 0;
@@ -469,9 +488,48 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
         if ((st = encode_3d(&map_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pr.C, map_cols, pr.M, pr.batch,
                             pr.ldc, sC, 32, 32, CU_TENSOR_MAP_L2_PROMOTION_NONE, "C")) != GEMM_OK)
             return st;
-        if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, map_a, map_b, map_out, kp, pl.grid, stream)) != cudaSuccess)
+        if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, map_a, map_b, map_out, map_out, kp, pl.grid, stream)) != cudaSuccess)
             return fail_cuda(e, "GEMM kernel launch");
         return GEMM_OK;
+    }
+
+    // Asking L2 for a unit's whole K range up front measured slower than the
+    // ring's own loads (the burst delays the first k-block), so it is opt-in.
+    kp.prefetch_l2 = (o && o->l2_prefetch == 2) ? 1 : 0;
+
+    if (pl.fused_reduce) {
+        // Split-K summed inside the GEMM kernel: one launch.  Partials go to
+        // W[b*S + s] (M x ldw f32) through the output map, as for the separate
+        // reduction; the reduce map reads rows_per rows of all S splits of a tile.
+        const int64_t ldw = (pr.N + 3) / 4 * 4;
+        const int64_t partial_bytes = pr.batch * int64_t(pl.split_k) * pr.M * ldw * 4;
+        const int64_t tiles = int64_t(pl.tiles_m) * pl.tiles_n * pr.batch;
+        void *ws = nullptr;
+        if ((e = cudaMallocFromPoolAsync(&ws, size_t(pl.workspace_bytes), ds->pool, stream)) != cudaSuccess)
+            return fail_cuda(e, "split-K workspace allocation");
+        const int64_t cpu = pl.tile_m == 2 * kTileM ? 2 : 1;
+        kp.fused = 1;
+        kp.reducers = int32_t(pl.split_k * cpu);
+        kp.rows_per = int32_t((pl.tile_m + kp.reducers - 1) / kp.reducers);
+        kp.counters = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + partial_bytes);
+        alignas(64) CUtensorMap map_red;
+        st = encode_3d(&map_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ws, pr.N, pr.M,
+                       pr.batch * pl.split_k, ldw, int64_t(pr.M) * ldw, 32, 32,
+                       CU_TENSOR_MAP_L2_PROMOTION_NONE, "split-K workspace");
+        if (st == GEMM_OK)
+            st = encode_3d(&map_red, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ws, pr.N, pr.M,
+                           pr.batch * pl.split_k, ldw, int64_t(pr.M) * ldw, uint32_t(pl.tile_n),
+                           uint32_t(kp.rows_per), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           "split-K workspace (reduce)", uint32_t(pl.split_k),
+                           CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (st == GEMM_OK && (e = cudaMemsetAsync(kp.counters, 0, size_t(tiles) * 4, stream)) != cudaSuccess)
+            st = fail_cuda(e, "zeroing the split-K arrival counters");
+        if (st == GEMM_OK &&
+            (e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, map_a, map_b, map_out, map_red, kp, pl.grid,
+                                     stream)) != cudaSuccess)
+            st = fail_cuda(e, "GEMM kernel launch");
+        cudaFreeAsync(ws, stream);
+        return st;
     }
 
     // Split-K: partials W[b*S + s] (M x ldw f32 each), then the fixed-order sum.
@@ -483,7 +541,7 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
                    pr.batch * pl.split_k, ldw, int64_t(pr.M) * ldw, 32, 32,
                    CU_TENSOR_MAP_L2_PROMOTION_NONE, "split-K workspace");
     if (st == GEMM_OK) {
-        if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, map_a, map_b, map_out, kp, pl.grid, stream)) != cudaSuccess)
+        if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, map_a, map_b, map_out, map_out, kp, pl.grid, stream)) != cudaSuccess)
             st = fail_cuda(e, "GEMM kernel launch");
     }
     if (st == GEMM_OK) {
@@ -574,9 +632,10 @@ gemm_status_t gemm_get_device_status(gemm_stream_t stream)
     const uint32_t zero = 0;
     cudaMemcpy(ds->status, &zero, sizeof zero, cudaMemcpyHostToDevice);
     return fail(GEMM_ERR_DEVICE_TIMEOUT,
-                "a bounded device-side wait ran out (roles: %s%s%s%s); the output of that call is incomplete",
+                "a bounded device-side wait ran out (roles: %s%s%s%s%s); the output of that call is incomplete",
                 (word & kStatusProducer) ? "producer " : "", (word & kStatusMma) ? "mma " : "",
-                (word & kStatusEpilogue) ? "epilogue " : "", (word & kStatusDrain) ? "drain" : "");
+                (word & kStatusEpilogue) ? "epilogue " : "", (word & kStatusDrain) ? "drain " : "",
+                (word & kStatusReduce) ? "split-K-reduce" : "");
 }
 
 const char *gemm_last_error_string(void) { return g_last_error.c_str(); }
@@ -698,6 +757,7 @@ extern "C" gemm_status_t gemm_f16_f32acc_splitk_noalloc(const uint16_t *A, const
 
     gemm_options_t o = {};
     o.split_k = split_k;
+    o.splitk_reduce = 1;  // partials in the scratch, summed by the separate reduce kernel
     gemm_plan_info_t pl;
     if ((st = make_plan(M, N, K, 1, &o, nd->sms, &pl)) != GEMM_OK)
         return st;
@@ -762,7 +822,7 @@ extern "C" gemm_status_t gemm_f16_f32acc_splitk_noalloc(const uint16_t *A, const
         if ((st = encode_3d(&map_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, map_cols, M, 1, ldc,
                             M * ldc, 32, 32, CU_TENSOR_MAP_L2_PROMOTION_NONE, "C")) != GEMM_OK)
             return st;
-        if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, map_a, map_b, map_out, kp, pl.grid, stream)) != cudaSuccess)
+        if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, map_a, map_b, map_out, map_out, kp, pl.grid, stream)) != cudaSuccess)
             return fail_cuda(e, "GEMM kernel launch");
         return GEMM_OK;
     }
@@ -774,7 +834,7 @@ extern "C" gemm_status_t gemm_f16_f32acc_splitk_noalloc(const uint16_t *A, const
                         ldw, M * ldw, 32, 32, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                         "static split-K scratch")) != GEMM_OK)
         return st;
-    if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, map_a, map_b, map_out, kp, pl.grid, stream)) != cudaSuccess)
+    if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, map_a, map_b, map_out, map_out, kp, pl.grid, stream)) != cudaSuccess)
         return fail_cuda(e, "GEMM kernel launch");
     const int64_t threads = M * ((N + 3) / 4);
     const int grid = int(std::min<int64_t>((threads + 255) / 256, int64_t(nd->sms) * 8));

@@ -17,6 +17,7 @@ constexpr uint32_t kStatusProducer = 1u;
 constexpr uint32_t kStatusMma = 2u;
 constexpr uint32_t kStatusEpilogue = 4u;
 constexpr uint32_t kStatusDrain = 8u;
+constexpr uint32_t kStatusReduce = 16u;
 
 // Everything the persistent kernel needs besides its three tensor maps.
 struct KernelParams {
@@ -35,9 +36,36 @@ struct KernelParams {
     // epilogue writes columns [n_tma, N) of C with plain stores.
     int32_t n_tma;
     int32_t tail;
-    float *c_direct;      // C itself (tail stores)
+    float *c_direct;      // C itself (tail stores, in-kernel split-K sums)
     int64_t ldc;
     int64_t stride_c;
+    // In-kernel split-K reduction (each cluster owns exactly one unit): the
+    // partials are TMA-stored like those of the separate reduction
+    // ([batch * split][M][ldw] f32, through the output map); the
+    // split_k x (CTAs per unit) reducers of a tile each own rows_per rows of
+    // it, fetch those rows of every split with one TMA load (the reduce map)
+    // and sum them in ascending split order.  counters holds one arrival
+    // count per tile, zeroed before the launch.
+    int32_t fused;
+    int32_t reducers;
+    int32_t rows_per;
+    int32_t prefetch_l2;  // 1: the producer first asks L2 for its unit's whole K range
+    uint32_t *counters;
+    // Optional per-CTA timeline (kTraceSlots globaltimer stamps per CTA), or null.
+    unsigned long long *trace;
+};
+
+// Trace slots (ns, %globaltimer), one row of kTraceSlots per CTA.
+constexpr int kTraceSlots = 8;
+enum TraceSlot {
+    kTraceEntry = 0,       // kernel entry
+    kTraceSetup = 1,       // barriers, TMEM and tensor maps ready
+    kTraceFirstData = 2,   // MMA issuer: first k-block landed in shared memory
+    kTraceLastMma = 3,     // MMA issuer: last MMA issued
+    kTraceAccReady = 4,    // epilogue: last accumulator ready
+    kTraceStored = 5,      // epilogue: output (or partial) written
+    kTraceReduced = 6,     // epilogue: in-kernel split-K sum written
+    kTraceExit = 7         // before TMEM is freed
 };
 
 // Shared-memory budget of one CTA for a tile width (host and device agree).
@@ -52,8 +80,8 @@ SmemBudget smem_budget(int tile_m, int tile_n);
 // Kernel-side entry points (defined in gemm_kernels.cu).
 cudaError_t set_kernel_attributes(int tile_m, int tile_n);
 cudaError_t launch_tcgen05_gemm(int tile_m, int tile_n, const CUtensorMap &map_a, const CUtensorMap &map_b,
-                                const CUtensorMap &map_out, const KernelParams &p, int grid,
-                                cudaStream_t stream);
+                                const CUtensorMap &map_out, const CUtensorMap &map_red,
+                                const KernelParams &p, int grid, cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const float *W, float *C, int32_t M, int32_t N, int32_t S,
                                  int32_t batch, int64_t ldw, int64_t ldc, int64_t strideC,
                                  int grid, cudaStream_t stream);

@@ -179,13 +179,20 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
     }
 }
 
+__device__ __forceinline__ void trace_stamp(const KernelParams &p, int slot)
+{
+    if (p.trace)
+        p.trace[int64_t(blockIdx.x) * kTraceSlots + slot] = ptx::globaltimer_ns();
+}
+
 // ------------------------------------------------------------- the GEMM
 
 template <int BN, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     tsm_gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a,
                             const __grid_constant__ CUtensorMap map_b,
-                            const __grid_constant__ CUtensorMap map_out, const KernelParams p)
+                            const __grid_constant__ CUtensorMap map_out,
+                            const __grid_constant__ CUtensorMap map_red, const KernelParams p)
 {
     using Cfg = TileCfg<BN, PAIR>;
     constexpr int S = Cfg::STAGES;
@@ -210,6 +217,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t stall_bar = ctrl + 16u * S + 40u; // never signalled (test hook)
     uint32_t *const tmem_slot = reinterpret_cast<uint32_t *>(ctrl_ptr + 16 * S + 48);
     volatile uint32_t *const abort_flag = tmem_slot + 1;
+    volatile uint32_t *const red_ok = tmem_slot + 2;  // in-kernel split-K: go / no-go
+    const uint32_t red_bar = ctrl + 16u * S + 64u;    // in-kernel split-K: partial chunks landed
 
     const int warp = int(threadIdx.x >> 5);
     const int lane = int(threadIdx.x & 31);
@@ -219,6 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t nclusters = PAIR ? (gridDim.x >> 1) : gridDim.x;
 
     if (threadIdx.x == 0) {
+        trace_stamp(p, kTraceEntry);
         for (int s = 0; s < S; ++s) {
             ptx::mbar_init(full0 + 8u * s, 1);
             ptx::mbar_init(empty0 + 8u * s, 1);
@@ -229,12 +239,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::mbar_init(done_bar, 1);
         ptx::mbar_init(stall_bar, 1);
+        ptx::mbar_init(red_bar, 1);
         *abort_flag = 0u;
         ptx::fence_mbar_init();
         ptx::prefetch_tensormap(&map_a);
         ptx::prefetch_tensormap(&map_b);
         ptx::prefetch_tensormap(&map_out);
+        if (p.fused)
+            ptx::prefetch_tensormap(&map_red);
     }
+    __syncwarp();
     if constexpr (PAIR)
         ptx::cluster_sync();  // the peer's barriers exist before anything signals them
     if (warp == 1) {
@@ -242,9 +256,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_relinquish<PAIR>();
     }
     ptx::tc_fence_before_sync();
-    __syncthreads();
+    ptx::cta_sync();
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    if (threadIdx.x == 0)
+        trace_stamp(p, kTraceSetup);
 
     AbortFlags af;
     af.local = abort_flag;
@@ -266,6 +282,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int64_t u = cluster; ok && u < p.num_units; u += nclusters) {
                 const Unit w = decode_unit(u, p, Cfg::TILE_M, BN);
+                if (p.prefetch_l2) {
+                    // The unit's whole K range of A and B at once: DRAM sees the
+                    // requests together (better page locality than the ring's
+                    // few k-blocks in flight); the ring's loads then hit L2.
+                    for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
+                        ptx::tma_prefetch_l2_3d(&map_a, kb * kTileK, w.m0 + row_off, w.z_in);
+#pragma unroll
+                        for (int j = 0; j < Cfg::B_BOXES; ++j)
+                            ptx::tma_prefetch_l2_3d(&map_b, w.n0 + col_off + 64 * j, kb * kTileK, w.z_in);
+                    }
+                }
                 for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!wait_bounded(empty0 + 8u * stage, phase ^ 1u, af, kStatusProducer, true)) {
                         ok = false;
@@ -316,6 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+        __syncwarp();  // lanes 1..31 wait for lane 0 before the CTA barrier
     } else if (warp == 1) {
         if (lane == 0 && leader) {
             // ---------------- MMA issuer (one thread; the leader of a pair)
@@ -337,6 +365,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     ptx::tc_fence_after_sync();
+                    if (u == cluster && kb == w.kb0)
+                        trace_stamp(p, kTraceFirstData);
                     const uint32_t sa = base + stage * Cfg::STAGE_BYTES;
                     const uint32_t sb = sa + Cfg::A_BYTES;
 #pragma unroll
@@ -360,10 +390,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     aphase ^= 1u;
                 }
             }
+            trace_stamp(p, kTraceLastMma);
             // Every MMA this thread issued must finish before TMEM is freed.
             ptx::mma_commit<PAIR>(done_bar, 1);
             wait_bounded(done_bar, 0, af, kStatusDrain, false);
         }
+        __syncwarp();  // lanes 1..31 wait for lane 0 before the CTA barrier
     } else {
         // ---------------- epilogue: warps 2..5, TMEM lane quarter = warp % 4
         const int e = warp - 2;
@@ -378,6 +410,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!__all_sync(0xffffffffu, got))
                 break;
             ptx::tc_fence_after_sync();
+            if (warp == 2 && lane == 0)
+                trace_stamp(p, kTraceAccReady);
             const int32_t row0 = w.m0 + row_off + 32 * q;
             int nch = 0;
             if (row0 < p.M) {
@@ -453,12 +487,121 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0)
             ptx::bulk_wait_group_all();  // stores complete before the CTA exits
         __syncwarp();
+        if (warp == 2 && lane == 0)
+            trace_stamp(p, kTraceStored);
+
+        if (p.fused) {
+            // ---------------- in-kernel split-K sum
+            // Every cluster owns one unit.  Each CTA's partial is in the
+            // workspace (its TMA stores completed above); the CTA arrives on
+            // its tile's counter, waits (bounded) until all reducers =
+            // split_k x CTAs-per-unit have arrived, fetches rows_per rows of
+            // every split of the tile with one TMA load into the idle ring, sums
+            // them in ascending split order (the order of the separate reduce
+            // kernel, so the sums are bitwise the same) and writes C.  All four
+            // epilogue warps pass the three named barriers on every path.
+            const int et = int(threadIdx.x) - 64;  // 0..127
+            if (lane == 0) {
+                ptx::fence_proxy_async_global();  // this warp's TMA stores, before the release
+                __threadfence();
+            }
+            ptx::named_bar_sync(1, 128);
+            const Unit w = decode_unit(cluster, p, Cfg::TILE_M, BN);
+            const int64_t tiles = int64_t(p.tiles_m) * p.tiles_n;
+            const int64_t z = cluster / tiles;
+            const int64_t t = cluster - z * tiles;
+            const int64_t bz = z / p.split_k;
+            const int32_t sp = int32_t(z - bz * p.split_k);
+            const int32_t ri = sp * (PAIR ? 2 : 1) + int32_t(rank);
+            const int32_t r0 = ri * p.rows_per;               // first tile row this CTA sums
+            const bool active = r0 < Cfg::TILE_M && w.m0 + r0 < p.M;
+            const uint32_t box_bytes = uint32_t(p.rows_per) * BN * 4u * uint32_t(p.split_k);
+            if (et == 0) {
+                uint32_t okv = 0;
+                if (!*abort_flag) {
+                    uint32_t *count = p.counters + (bz * tiles + t);
+                    __threadfence();
+                    atomicAdd(count, 1u);  // arrive
+                    const uint32_t target = uint32_t(p.reducers);
+                    okv = 1;
+                    if (ptx::ld_acquire_gpu_u32(count) != target) {
+                        const uint64_t t0 = ptx::globaltimer_ns();
+                        for (uint32_t it = 1;; ++it) {
+                            __nanosleep(64);  // every waiter polls the same word: back off
+                            if (ptx::ld_acquire_gpu_u32(count) == target)
+                                break;
+                            if ((it & 7u) == 0) {
+                                if (*abort_flag) {
+                                    okv = 0;
+                                    break;
+                                }
+                                if (ptx::globaltimer_ns() - t0 > p.timeout_ns) {
+                                    *abort_flag = 1u;
+                                    if (af.peer)
+                                        ptx::st_cluster_u32(af.peer, 1u);
+                                    atomicOr(p.status, kStatusReduce);
+                                    okv = 0;
+                                    break;
+                                }
+                            }
+                        }
+                    }
+                    if (okv && active) {
+                        __threadfence();
+                        ptx::fence_proxy_async_global();
+                        ptx::mbar_arrive_expect_tx(red_bar, box_bytes);
+                        // box {BN columns, rows_per rows, split_k splits}
+                        ptx::tma_load_3d(base, &map_red, red_bar, w.n0, w.m0 + r0,
+                                         int32_t(bz * p.split_k));
+                    }
+                }
+                *red_ok = okv;
+            }
+            ptx::named_bar_sync(1, 128);
+            if (*red_ok && active) {
+                // The load is in flight and finishes on its own: wait it out.
+                if (wait_bounded(red_bar, 0, af, kStatusReduce, false)) {
+                    const float4 *stg = reinterpret_cast<const float4 *>(base_ptr);
+                    const int32_t per_split = p.rows_per * (BN / 4);  // float4s of one split
+                    for (int32_t f = et; f < per_split; f += 128) {
+                        float4 acc = stg[f];
+                        for (int32_t s2 = 1; s2 < p.split_k; ++s2) {
+                            const float4 v = stg[s2 * per_split + f];
+                            acc.x += v.x;
+                            acc.y += v.y;
+                            acc.z += v.z;
+                            acc.w += v.w;
+                        }
+                        const int32_t row = f / (BN / 4);
+                        const int32_t gr = w.m0 + r0 + row;
+                        const int32_t gc = w.n0 + (f - row * (BN / 4)) * 4;
+                        if (row < p.rows_per && r0 + row < Cfg::TILE_M && gr < p.M && gc < p.N) {
+                            float *dst = p.c_direct + bz * p.stride_c + int64_t(gr) * p.ldc + gc;
+                            if (gc + 3 < p.N) {
+                                *reinterpret_cast<float4 *>(dst) = acc;
+                            } else {
+                                dst[0] = acc.x;
+                                if (gc + 1 < p.N)
+                                    dst[1] = acc.y;
+                                if (gc + 2 < p.N)
+                                    dst[2] = acc.z;
+                            }
+                        }
+                    }
+                }
+            }
+            ptx::named_bar_sync(1, 128);
+            if (et == 0)
+                trace_stamp(p, kTraceReduced);
+        }
     }
 
     ptx::tc_fence_before_sync();
-    __syncthreads();
+    ptx::cta_sync();
     if constexpr (PAIR)
         ptx::cluster_sync();  // neither CTA leaves while the other may still signal it
+    if (threadIdx.x == 0)
+        trace_stamp(p, kTraceExit);
     if (warp == 1) {
         __syncwarp();
         ptx::tc_fence_after_sync();
@@ -573,7 +716,8 @@ cudaError_t set_kernel_attributes(int tile_m, int tile_n)
 
 template <int BN, bool PAIR>
 static cudaError_t launch_bn(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o,
-                             const KernelParams &p, int grid, cudaStream_t stream)
+                             const CUtensorMap &r, const KernelParams &p, int grid,
+                             cudaStream_t stream)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(grid), 1, 1);
@@ -592,26 +736,27 @@ static cudaError_t launch_bn(const CUtensorMap &a, const CUtensorMap &b, const C
         cfg.attrs = nullptr;
         cfg.numAttrs = 0;
     }
-    return cudaLaunchKernelEx(&cfg, tsm_gemm_tcgen05_kernel<BN, PAIR>, a, b, o, p);
+    return cudaLaunchKernelEx(&cfg, tsm_gemm_tcgen05_kernel<BN, PAIR>, a, b, o, r, p);
 }
 
 cudaError_t launch_tcgen05_gemm(int tile_m, int tile_n, const CUtensorMap &map_a,
                                 const CUtensorMap &map_b, const CUtensorMap &map_out,
-                                const KernelParams &p, int grid, cudaStream_t stream)
+                                const CUtensorMap &map_red, const KernelParams &p, int grid,
+                                cudaStream_t stream)
 {
     if (tile_m == 2 * kTileM) {
         if (grid % 2)
             return cudaErrorInvalidValue;
         switch (tile_n) {
-        case 128: return launch_bn<128, true>(map_a, map_b, map_out, p, grid, stream);
-        case 256: return launch_bn<256, true>(map_a, map_b, map_out, p, grid, stream);
+        case 128: return launch_bn<128, true>(map_a, map_b, map_out, map_red, p, grid, stream);
+        case 256: return launch_bn<256, true>(map_a, map_b, map_out, map_red, p, grid, stream);
         default: return cudaErrorInvalidValue;
         }
     }
     switch (tile_n) {
-    case 64: return launch_bn<64, false>(map_a, map_b, map_out, p, grid, stream);
-    case 128: return launch_bn<128, false>(map_a, map_b, map_out, p, grid, stream);
-    case 256: return launch_bn<256, false>(map_a, map_b, map_out, p, grid, stream);
+    case 64: return launch_bn<64, false>(map_a, map_b, map_out, map_red, p, grid, stream);
+    case 128: return launch_bn<128, false>(map_a, map_b, map_out, map_red, p, grid, stream);
+    case 256: return launch_bn<256, false>(map_a, map_b, map_out, map_red, p, grid, stream);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -91,6 +91,15 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void *map, 
         : "memory");
 }
 
+// Hint: fetch a tiled 3-D box into L2 (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const void *map, int32_t c0, int32_t c1, int32_t c2)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
 // Tiled 3-D store shared -> global; parts of the box outside the tensor are
 // not written.
 __device__ __forceinline__ void tma_store_3d(const void *map, uint32_t src, int32_t c0,
@@ -142,6 +151,54 @@ __device__ __forceinline__ uint64_t policy_evict_first()
     return p;
 }
 
+// Plain (untiled) bulk copy global -> this CTA's shared memory, counted in
+// bytes on `bar`.  Addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// Orders this thread's earlier generic-proxy accesses to global memory with
+// its later async-proxy ones (a bulk copy that reads what was just acquired).
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// ----------------------------------------------------------------- global memory
+
+__device__ __forceinline__ uint64_t ld_acquire_gpu(const unsigned long long *p)
+{
+    uint64_t v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu_u32(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Named barrier `id` over `count` threads (a multiple of 32) of this CTA.
+// The non-aligned form: defined even when the lanes of a warp reach it at
+// different times, which the role code (one lane per role) can cause.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count)
+{
+    asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// All threads of the CTA, non-aligned (see named_bar_sync).
+__device__ __forceinline__ void cta_sync()
+{
+    asm volatile("barrier.sync 0;" ::: "memory");
+}
+
 // ----------------------------------------------------------------- clusters
 
 __device__ __forceinline__ uint32_t cluster_ctarank()
@@ -153,10 +210,11 @@ __device__ __forceinline__ uint32_t cluster_ctarank()
 
 // All threads of every CTA in the cluster; release/acquire orders the
 // shared-memory writes before it with the reads after it, cluster-wide.
+// Non-aligned, like cta_sync.
 __device__ __forceinline__ void cluster_sync()
 {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.arrive.release;\n\t"
+                 "barrier.cluster.wait.acquire;" ::: "memory");
 }
 
 // The shared::cluster address of the same shared-memory location in CTA `rank`.
