@@ -48,6 +48,13 @@ def parse_args(argv=None):
                    help="one of the named workloads in tiled_staged_matmul_gb300.synthetic")
     p.add_argument("--shape", default=None,
                    help="MxNxK: an ad-hoc shape with N(0, 1/sqrt(K)) operands instead of --workload")
+    p.add_argument("--tile-m", type=int, default=0, help="128 or 256 (CTA pair); 0: planner")
+    p.add_argument("--tile-n", type=int, default=0, help="64, 128 or 256; 0: planner")
+    p.add_argument("--split-k", type=int, default=0, help="K ranges; 0: planner")
+    p.add_argument("--splitk-reduce", type=int, default=0,
+                   help="0/2: in-kernel split-K sum when possible, 1: separate reduce kernel")
+    p.add_argument("--trace", action="store_true",
+                   help="add a per-CTA phase timeline (one extra traced step) to the JSON line")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=10)
@@ -198,8 +205,9 @@ def run_ours(args, rank, local_rank, world):
     B = B_h.to(dev)
     C = torch.empty((w.M, w.N), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
-    plan = binding.gemm_plan(w.M, w.N, w.K)
-    launches_per_call = 2 if plan["split_k"] > 1 else 1
+    opts = binding.GemmOptions(args.split_k, args.tile_n, 0, 0, args.tile_m, args.splitk_reduce)
+    plan = binding.gemm_plan(w.M, w.N, w.K, 1, opts)
+    launches_per_call = 2 if plan["split_k"] > 1 and not plan["fused_reduce"] else 1
 
     working_set = 2 * w.M * w.K + 2 * w.K * w.N + 4 * w.M * w.N
     flush = working_set < 2 * L2_BYTES
@@ -214,9 +222,10 @@ def run_ours(args, rank, local_rank, world):
         scrub.zero_()
         torch.sum(sweep, dim=0, keepdim=True, out=sink)
 
-    def call():
-        binding.check(binding.gemm_f16_f32acc(A.data_ptr(), B.data_ptr(), C.data_ptr(),
-                                              w.M, w.N, w.K, w.K, w.N, w.N, stream.cuda_stream))
+    def call(o=opts):
+        binding.check(binding.gemm_f16_f32acc_opts(A.data_ptr(), B.data_ptr(), C.data_ptr(),
+                                                   w.M, w.N, w.K, w.K, w.N, w.N, 0, 0, 0, 1,
+                                                   o, stream.cuda_stream))
 
     for _ in range(max(args.warmup, 3)):
         if flush:
@@ -285,7 +294,9 @@ def run_ours(args, rank, local_rank, world):
         "data": "synthetic",
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
                    "dist": w.dist, "seed": w.seed, "accumulate": "f32",
-                   "tile_n": plan["tile_n"], "split_k": plan["split_k"],
+                   "tile_m": plan["tile_m"], "tile_n": plan["tile_n"], "split_k": plan["split_k"],
+                   "splitk_sum": ("in-kernel" if plan["fused_reduce"] else "separate kernel")
+                   if plan["split_k"] > 1 else "none",
                    "stages": plan["stages"], "grid": plan["grid"],
                    "l2": "flushed before every step (write 2xL2, then read 2xL2)" if flush else
                          f"inputs+output {working_set / 2**20:.0f} MiB > L2, no flush",
@@ -295,12 +306,42 @@ def run_ours(args, rank, local_rank, world):
     }
     clocks = sampler.summary(t0, t1)
     result["clocks"] = {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")}
+    if args.trace:
+        result["trace"] = traced_step(args, binding, call, plan, flush_l2 if flush else None, dev)
 
     if not args.no_e2e:
         result["e2e"] = run_e2e(args, w, A_h, B_h, dev, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, A_h, B_h, target_s=15.0)
     return result
+
+
+TRACE_PHASES = ("entry", "setup", "first_data", "last_mma", "acc_ready", "stored", "reduced",
+                "exit")
+
+
+def traced_step(args, binding, call, plan, flush, dev):
+    """One more step with the kernel's per-CTA trace on: for every phase, the
+    min / median / max over CTAs of its time after the first CTA started
+    (us; the timer ticks in steps of about 0.25 us)."""
+    import torch
+    tr = torch.zeros((plan["grid"], 8), dtype=torch.int64, device=dev)
+    o = binding.GemmOptions(args.split_k, args.tile_n, 0, 0, args.tile_m, args.splitk_reduce,
+                            0, 0, tr.data_ptr())
+    if flush:
+        flush()
+    call(o)
+    torch.cuda.synchronize()
+    t = tr.cpu().double()
+    t0 = t[:, 0][t[:, 0] > 0].min()
+    out = {}
+    for i, name in enumerate(TRACE_PHASES):
+        col = t[:, i][t[:, i] > 0]
+        if col.numel():
+            rel = ((col - t0) / 1000.0).sort().values
+            out[name] = [round(float(rel[0]), 2), round(float(rel[rel.numel() // 2]), 2),
+                         round(float(rel[-1]), 2)]
+    return {"unit": "us after the first CTA entered, [min, median, max] over CTAs", **out}
 
 
 def pick_workload(args):

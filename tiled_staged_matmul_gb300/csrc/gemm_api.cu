@@ -307,6 +307,11 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const ge
     for (const TileChoice &c : kChoices) {
         if (!allowed(c))
             continue;
+        // Long K: one CTA per tile measured faster than CTA pairs (the first
+        // k-block lands sooner and each reducer sums fewer rows), e.g. 26.9 us
+        // against 29.2 us on 256 x 256 x 65536.
+        if (long_k && req_m == 0 && c.tile_m != kTileM)
+            continue;
         const int64_t tiles = tiles_of(c.tile_m, c.tile_n);
         double cost;
         if (long_k) {
