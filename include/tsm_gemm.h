@@ -100,11 +100,16 @@ typedef struct gemm_options {
                            tile_n 128 or 256) */
     int32_t splitk_reduce; /* 0 or 2: sum split-K partials inside the GEMM kernel when the
                               plan allows it (every cluster owns one unit), else in a second
-                              kernel; 1: always the second kernel.  Both sum the splits in
-                              ascending order, so the results are bitwise the same. */
+                              kernel; 1: always the second kernel, and no split tail.  Both
+                              sum the splits in ascending order, so the results of one split
+                              count are bitwise the same. */
     int32_t l2_prefetch; /* 0 or 1: off; 2: on -- each unit first asks L2 for its whole K
                             range of A and B (measured slower on GB300, kept for study) */
-    int32_t reserved;   /* 0 */
+    int32_t split_tail; /* 0: off; 1: when there are more tiles than slots and the last wave is
+                           at most half full, split each of its tiles into K ranges summed in
+                           the kernel so that wave keeps every slot busy.  Measured on GB300 at
+                           4096^3 and 8192^3: no gain (only two-way splits fit, and storing and
+                           summing the partials costs about as much as half a tile saves). */
     uint64_t *trace;    /* NULL, or a device buffer of grid x 8 uint64 (grid from gemm_plan):
                            per CTA, %globaltimer stamps (ns) of kernel entry, setup done,
                            first k-block landed, last MMA issued, last accumulator ready,
@@ -131,7 +136,10 @@ typedef struct gemm_plan_info {
     int64_t stage_bytes;  /* shared memory of one k-block: A tile + B tile */
     int64_t smem_bytes;   /* dynamic shared memory of one CTA */
     int64_t workspace_bytes; /* split-K partials (0 when split_k == 1) */
-    int32_t fused_reduce; /* 1: the partials are summed inside the GEMM kernel */
+    int32_t fused_reduce; /* 1: split partials are summed inside the GEMM kernel */
+    int32_t tail_tiles;   /* with gemm_options_t.split_tail: the tiles of the partial last wave,
+                             each split into tail_split K ranges summed in the kernel; 0: none */
+    int32_t tail_split;
 } gemm_plan_info_t;
 
 /* C = A . B for one matrix.

@@ -135,7 +135,8 @@ def test_pair_needs_a_wide_tile(b):
 
 @pytest.mark.parametrize("M,N,K", [(64, 128, 128), (1000, 1000, 1000), (4096, 4096, 4096),
                                    (256, 256, 65536), (8192, 8192, 8192), (1, 1, 1),
-                                   (300, 7, 100000), (1, 5000, 64)])
+                                   (300, 7, 100000), (1, 5000, 64), (2304, 2304, 1024),
+                                   (6144, 6144, 6144), (4096, 4096, 512)])
 def test_plan_invariants(b, M, N, K):
     p = b.gemm_plan(M, N, K, 1, None, SMS)
     assert p["tile_m"] in (128, 256)
@@ -143,20 +144,32 @@ def test_plan_invariants(b, M, N, K):
     assert p["tiles_n"] == -(-N // p["tile_n"])
     assert p["k_blocks"] == -(-K // 64)
     assert 1 <= p["split_k"] <= p["k_blocks"]
-    assert p["units"] == p["tiles_m"] * p["tiles_n"] * p["split_k"]
+    tiles = p["tiles_m"] * p["tiles_n"]
+    if p["tail_split"]:
+        # split tail: whole tiles for the full waves, the rest split tail_split ways
+        slots = SMS // (2 if p["tile_m"] == 256 else 1)
+        assert p["split_k"] == 1 and p["fused_reduce"]
+        assert p["tail_tiles"] == tiles % slots and p["tail_split"] >= 2
+        assert p["units"] == tiles - p["tail_tiles"] + p["tail_tiles"] * p["tail_split"]
+        assert p["tail_tiles"] * p["tail_split"] <= slots
+    else:
+        assert p["units"] == tiles * p["split_k"]
     if p["tile_m"] == 128:
         assert p["grid"] == min(p["units"], SMS)
     else:
         assert p["grid"] == 2 * min(p["units"], SMS // 2)
     ldw = -(-N // 4) * 4
-    if p["split_k"] == 1:
+    tile_bytes = p["tile_m"] * p["tile_n"] * 4
+    if p["tail_split"]:
+        counters = -(-(p["tail_tiles"] * 4) // 16) * 16
+        assert p["workspace_bytes"] == p["tail_tiles"] * p["tail_split"] * tile_bytes + counters
+    elif p["split_k"] == 1:
         assert p["workspace_bytes"] == 0 and not p["fused_reduce"]
     elif p["fused_reduce"]:
-        # the separate reduction's partials plus one arrival counter per tile;
+        # one compact partial tile per split unit, one arrival counter per tile;
         # every cluster owns exactly one unit
-        tiles = p["tiles_m"] * p["tiles_n"]
         counters = -(-(tiles * 4) // 16) * 16
-        assert p["workspace_bytes"] == p["split_k"] * M * ldw * 4 + counters
+        assert p["workspace_bytes"] == tiles * p["split_k"] * tile_bytes + counters
         assert p["units"] * (2 if p["tile_m"] == 256 else 1) == p["grid"]
     else:
         assert p["workspace_bytes"] == p["split_k"] * M * ldw * 4
@@ -197,3 +210,20 @@ def test_more_units_than_clusters_never_fuses(b):
     # wait on a split that only it can compute later, so the sum is a second kernel.
     p = b.gemm_plan(256, 256, 65536, 1, b._opts(split_k=64, tile_m=128, tile_n=128), SMS)
     assert p["units"] > SMS and not p["fused_reduce"]
+
+
+def test_split_tail_for_partial_last_waves(b):
+    on = b.GemmOptions(0, 0, 0, 0, 0, 0, 0, 1)
+    # off unless asked for
+    assert b.gemm_plan(8192, 8192, 8192, 1, None, SMS)["tail_split"] == 0
+    # 1024 pair tiles on 76 clusters: 13 full waves, 36 tiles left, split 2 ways
+    p = b.gemm_plan(8192, 8192, 8192, 1, on, SMS)
+    assert (p["tail_tiles"], p["tail_split"]) == (36, 2)
+    assert p["units"] == 1024 - 36 + 72 and p["fused_reduce"]
+    # a last wave more than half full keeps whole tiles
+    p = b.gemm_plan(6144, 6144, 6144, 1, on, SMS)
+    assert p["tail_split"] == 0 and not p["fused_reduce"]
+    # never with the separate-reduce option, nor for batches
+    off = b.GemmOptions(0, 0, 0, 0, 0, 1, 0, 1)
+    assert b.gemm_plan(8192, 8192, 8192, 1, off, SMS)["tail_split"] == 0
+    assert b.gemm_plan(4096, 4096, 4096, 2, on, SMS)["tail_split"] == 0

@@ -117,6 +117,24 @@ def test_in_kernel_and_separate_reduce_agree_bitwise(b, M, N, K, tile_m, tile_n,
     check_tolerance(C_in.numpy(), ref_of(A, B), K)
 
 
+@pytest.mark.parametrize("M,N,K", [(2304, 2304, 1024), (4096, 4096, 512), (2200, 2270, 832)])
+def test_split_tail(b, M, N, K):
+    """Plans whose partial last wave is split across all slots: exact on
+    integers, and the same within tolerance as whole tiles on random inputs."""
+    plan = b.gemm_plan(M, N, K, 1, b.GemmOptions(0, 0, 0, 0, 0, 0, 0, 1))
+    assert plan["tail_split"] >= 2, plan
+    A, B = synthetic.operands(M, N, K, "int4", seed=M + N)
+    C, dC = run_gemm(b, A, B, split_tail=1)
+    check_exact(C.numpy(), ref_of(A, B))
+    assert dC.outside_untouched()
+    A, B = synthetic.operands(M, N, K, "normal", seed=M + N + 1)
+    C_tail, _ = run_gemm(b, A, B, split_tail=1)
+    C_whole, _ = run_gemm(b, A, B)
+    check_tolerance(C_tail.numpy(), ref_of(A, B), K)
+    diff = np.abs(C_tail.numpy().astype(np.float64) - C_whole.numpy())
+    assert diff.max() <= 1e-3 * math.sqrt(K)
+
+
 def test_in_kernel_reduce_batched(b):
     M, N, K, batch = 200, 136, 12000, 3
     A, B = synthetic.operands(M, N, K, "int4", seed=23, batch=batch)
@@ -306,6 +324,20 @@ def test_torch_convenience_wrapper(b):
     with pytest.raises(ValueError):
         b.gemm(torch.zeros((8, 30), dtype=torch.float16, device="cuda"),
                torch.zeros((30, 8), dtype=torch.float16, device="cuda"))
+
+
+def test_host_pipeline_results(b):
+    """Host-resident problems through the double-buffered pipeline: every
+    result matches its own inputs, also once buffer sets are reused."""
+    M, N, K = 300, 264, 520
+    pipe = b.HostPipeline(M, N, K, depth=2)
+    problems = [synthetic.operands(M, N, K, "int4", seed=400 + i) for i in range(5)]
+    outs = [torch.empty((M, N), dtype=torch.float32).pin_memory() for _ in problems]
+    for (A, B), C in zip(problems, outs):
+        pipe.submit(A.pin_memory(), B.pin_memory(), C)
+    pipe.synchronize()
+    for (A, B), C in zip(problems, outs):
+        check_exact(C.numpy(), ref_of(A, B))
 
 
 # ---------------------------------------------------------------- device-side argument checks

@@ -25,8 +25,15 @@ def b():
     return binding
 
 
-@pytest.mark.parametrize("M,N,K,split_k", [(512, 512, 1024, 1), (256, 256, 8192, 4)])
-def test_stalled_wait_times_out_and_the_next_call_is_exact(b, M, N, K, split_k):
+@pytest.mark.parametrize("M,N,K,split_k,tile_m,tile_n", [
+    (512, 512, 1024, 1, 0, 0),        # one CTA per tile
+    (256, 256, 8192, 4, 0, 0),        # split K, one CTA per tile
+    (512, 512, 1024, 1, 256, 256),    # CTA pairs
+    (256, 256, 8192, 4, 256, 256),    # CTA pairs, split-K summed in the kernel
+    (256, 256, 8192, 8, 128, 128),    # one CTA per tile, split-K summed in the kernel
+    (2304, 2304, 1024, 0, 256, 256),  # CTA pairs with a split tail (opt-in)
+])
+def test_stalled_wait_times_out_and_the_next_call_is_exact(b, M, N, K, split_k, tile_m, tile_n):
     A, B = synthetic.operands(M, N, K, "int4", seed=31)
     dA, dB = A.cuda(), B.cuda()
     dC = torch.empty((M, N), dtype=torch.float32, device="cuda")
@@ -34,7 +41,7 @@ def test_stalled_wait_times_out_and_the_next_call_is_exact(b, M, N, K, split_k):
     assert b.gemm_get_device_status(s) == b.GEMM_OK
     t0 = time.time()
     st = b.gemm_f16_f32acc_opts(dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), M, N, K, K, N, N,
-                                0, 0, 0, 1, b.GemmOptions(split_k, 0, 200, 1), s)
+                                0, 0, 0, 1, b.GemmOptions(split_k, tile_n, 200, 1, tile_m, 0, 0, 1), s)
     assert st == b.GEMM_OK  # queued; the failure shows on the device
     st = b.gemm_get_device_status(s)
     elapsed = time.time() - t0
@@ -44,7 +51,7 @@ def test_stalled_wait_times_out_and_the_next_call_is_exact(b, M, N, K, split_k):
     # the status word was cleared, and the context is healthy
     assert b.gemm_get_device_status(s) == b.GEMM_OK
     st = b.gemm_f16_f32acc_opts(dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), M, N, K, K, N, N,
-                                0, 0, 0, 1, b.GemmOptions(split_k, 0, 0, 0), s)
+                                0, 0, 0, 1, b.GemmOptions(split_k, tile_n, 0, 0, tile_m, 0, 0, 1), s)
     b.check(st)
     b.check(b.gemm_get_device_status(s))
     ref = oracle.gemm_f64(A, B, M, N, K)

@@ -30,7 +30,7 @@ class GemmOptions(ctypes.Structure):
     _fields_ = [("split_k", ctypes.c_int32), ("tile_n", ctypes.c_int32),
                 ("timeout_ms", ctypes.c_int32), ("inject_stall", ctypes.c_int32),
                 ("tile_m", ctypes.c_int32), ("splitk_reduce", ctypes.c_int32),
-                ("l2_prefetch", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("l2_prefetch", ctypes.c_int32), ("split_tail", ctypes.c_int32),
                 ("trace", ctypes.c_void_p)]
 
 
@@ -42,7 +42,8 @@ class GemmPlanInfo(ctypes.Structure):
                 ("units", ctypes.c_int64), ("grid", ctypes.c_int32),
                 ("group_m", ctypes.c_int32), ("stage_bytes", ctypes.c_int64),
                 ("smem_bytes", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
-                ("fused_reduce", ctypes.c_int32)]
+                ("fused_reduce", ctypes.c_int32), ("tail_tiles", ctypes.c_int32),
+                ("tail_split", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -220,3 +221,57 @@ def gemm_host(A_host, B_host, C_host, dA, dB, dC, stream=None):
         gemm(dA, dB, dC, stream=s)
         C_host.copy_(dC, non_blocking=True)
     return C_host
+
+
+class HostPipeline:
+    """C = A . B for a stream of host-resident problems of one shape.
+
+    Each ``submit`` copies A and B (pinned CPU f16 tensors) to the device,
+    runs the GEMM and copies C back into the given pinned CPU f32 tensor.
+    ``depth`` device buffer sets and three CUDA streams (upload, GEMM,
+    download) let the upload of one problem overlap the GEMM and the download
+    of the previous ones; events order the three stages of each problem and
+    keep a buffer set from being reused before its result has been read back.
+    Torch provides the memory, streams and copies; the GEMM is this library's.
+    Call ``synchronize`` before reading the last ``depth`` results."""
+
+    def __init__(self, M, N, K, depth=2, device=None):
+        import torch
+        self.M, self.N, self.K, self.depth = M, N, K, depth
+        dev = torch.device("cuda") if device is None else torch.device(device)
+        self.dA = [torch.empty((M, K), dtype=torch.float16, device=dev) for _ in range(depth)]
+        self.dB = [torch.empty((K, N), dtype=torch.float16, device=dev) for _ in range(depth)]
+        ldc = max(4, -(-N // 4) * 4)
+        self.dC = [torch.empty((M, ldc), dtype=torch.float32, device=dev)[:, :N]
+                   for _ in range(depth)]
+        self.s_in = torch.cuda.Stream(device=dev)
+        self.s_gemm = torch.cuda.Stream(device=dev)
+        self.s_out = torch.cuda.Stream(device=dev)
+        self.in_done = [torch.cuda.Event() for _ in range(depth)]
+        self.gemm_done = [torch.cuda.Event() for _ in range(depth)]
+        self.out_done = [torch.cuda.Event() for _ in range(depth)]
+        self.used = [False] * depth
+        self.count = 0
+
+    def submit(self, A_host, B_host, C_host):
+        import torch
+        i = self.count % self.depth
+        self.count += 1
+        if self.used[i]:
+            self.s_in.wait_event(self.out_done[i])  # buffer set i is free again
+        with torch.cuda.stream(self.s_in):
+            self.dA[i].copy_(A_host, non_blocking=True)
+            self.dB[i].copy_(B_host, non_blocking=True)
+            self.in_done[i].record(self.s_in)
+        self.s_gemm.wait_event(self.in_done[i])
+        gemm(self.dA[i], self.dB[i], self.dC[i], stream=self.s_gemm)
+        self.gemm_done[i].record(self.s_gemm)
+        self.s_out.wait_event(self.gemm_done[i])
+        with torch.cuda.stream(self.s_out):
+            C_host.copy_(self.dC[i], non_blocking=True)
+            self.out_done[i].record(self.s_out)
+        self.used[i] = True
+        return C_host
+
+    def synchronize(self):
+        self.s_out.synchronize()

@@ -285,6 +285,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const ge
     const int64_t ldw = (N + 3) / 4 * 4;
     auto tiles_of = [&](int tm, int tn) { return int64_t(ceil_div(Mx, tm)) * ceil_div(Nx, tn) * batch; };
     auto slots_of = [&](int tm) { return int64_t(tm == 2 * kTileM ? sms / 2 : sms); };
+    auto tile_elems_of = [](int tm, int tn) { return int64_t(tm) * tn; };
     auto allowed = [&](const TileChoice &c) {
         return (req_m == 0 || req_m == c.tile_m) && (req_n == 0 || req_n == c.tile_n) &&
                (c.tile_m == kTileM || sms >= 2);
@@ -297,6 +298,28 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const ge
         if (K == 0 || tiles >= slots_of(tm))
             return 1;
         return int(std::max<int64_t>(1, std::min<int64_t>(slots_of(tm) / tiles, k_blocks / 4)));
+    };
+    // Split tail (opt-in, gemm_options_t.split_tail): with more tiles than
+    // slots, the R tiles of a partial last wave are each split into
+    // tail_split K ranges (summed in the kernel), so the last wave keeps every
+    // slot busy for a fraction of a tile.  Returns that split (0: none).
+    auto tail_split_of = [&](int tm, int tn) -> int {
+        const int req_r0 = o ? o->splitk_reduce : 0;
+        if (!o || o->split_tail != 1 || req_s != 0 || req_r0 == 1 || batch != 1 || K == 0)
+            return 0;
+        const int64_t slots = slots_of(tm), tiles = tiles_of(tm, tn);
+        const int64_t rem = tiles % slots;
+        if (tiles <= slots || rem == 0)
+            return 0;
+        const int64_t st = std::min<int64_t>(slots / rem, k_blocks / 4);
+        if (st < 2)
+            return 0;
+        const int64_t reducers = st * (tm == 2 * kTileM ? 2 : 1);
+        const int64_t rows_per = (tm + reducers - 1) / reducers;
+        const SmemBudget b = smem_budget(tm, tn);
+        if (rows_per * tn * 4 * st > int64_t(b.stages) * b.stage_bytes || st > 256)
+            return 0;
+        return int(st);
     };
     // Long K on a small output: the split-K regime.  Pick the tile that moves
     // the fewest bytes from L2 into shared memory, partials included.
@@ -324,8 +347,14 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const ge
         } else {
             // Fewest waves of persistent CTAs, weighted by the per-SM efficiency
             // of the tile (a wave does tile_n columns of 128 rows on every SM).
-            const int64_t waves = (tiles + slots_of(c.tile_m) - 1) / slots_of(c.tile_m);
-            cost = double(waves) * c.tile_n / c.eff;
+            // A partial last wave split across all slots (see tail_split_of)
+            // costs a fraction of a wave plus the partial sums.
+            const int64_t slots = slots_of(c.tile_m);
+            double waves = double((tiles + slots - 1) / slots);
+            const int st = tail_split_of(c.tile_m, c.tile_n);
+            if (st >= 2)
+                waves = double(tiles / slots) + 1.0 / st + 0.1;
+            cost = waves * c.tile_n / c.eff;
         }
         if (!best || cost < best_cost) {
             best = &c;
@@ -363,11 +392,29 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const ge
     const int req_r = o ? o->splitk_reduce : 0;
     pl->fused_reduce = split > 1 && req_r != 1 && split <= 256 && pl->units <= slots_of(tm) &&
                        rows_per * bn * 4 * split <= int64_t(sb.stages) * sb.stage_bytes;
-    if (split == 1)
+    pl->tail_tiles = 0;
+    pl->tail_split = 0;
+    if (split == 1) {
+        const int st = tail_split_of(tm, bn);
+        if (st >= 2) {
+            pl->tail_tiles = int32_t(tiles % slots_of(tm));
+            pl->tail_split = st;
+            pl->units = tiles - pl->tail_tiles + int64_t(pl->tail_tiles) * st;
+            pl->grid = int(std::min<int64_t>(pl->units, slots_of(tm)) * ctas_per_unit);
+            pl->fused_reduce = 1;
+        }
+    }
+    // Split partials: in-kernel sums use a compact [split unit][tile_m][tile_n]
+    // workspace plus a counter per split tile; the reduce kernel reads
+    // [batch * split][M][ldw].
+    const int64_t split_tiles = pl->tail_split ? pl->tail_tiles : (split > 1 ? tiles : 0);
+    const int64_t split_units = pl->tail_split ? split_tiles * pl->tail_split : split_tiles * split;
+    if (split == 1 && !pl->tail_split)
         pl->workspace_bytes = 0;
-    else  // [batch * split][M][ldw] f32, and for the in-kernel sum a counter per tile
-        pl->workspace_bytes = batch * int64_t(split) * M * ldw * 4 +
-                              (pl->fused_reduce ? (tiles * 4 + 15) / 16 * 16 : 0);
+    else if (pl->fused_reduce)
+        pl->workspace_bytes = split_units * tile_elems_of(tm, bn) * 4 + (split_tiles * 4 + 15) / 16 * 16;
+    else
+        pl->workspace_bytes = batch * int64_t(split) * M * ldw * 4;
     return GEMM_OK;
 }
 
@@ -481,7 +528,10 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
     kp.c_direct = pr.C;
     kp.ldc = pr.ldc;
     kp.stride_c = sC;
-    if (pl.split_k == 1) {
+    // Asking L2 for a unit's whole K range up front measured slower than the
+    // ring's own loads (the burst delays the first k-block), so it is opt-in.
+    kp.prefetch_l2 = (o && o->l2_prefetch == 2) ? 1 : 0;
+    if (pl.split_k == 1 && !pl.fused_reduce) {
         // TMA stores write whole 16-byte granules: let the map end at the last
         // multiple of 4 columns and write the rest with plain stores, so that
         // C's row padding past N stays untouched.
@@ -493,45 +543,57 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
         if ((st = encode_3d(&map_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pr.C, map_cols, pr.M, pr.batch,
                             pr.ldc, sC, 32, 32, CU_TENSOR_MAP_L2_PROMOTION_NONE, "C")) != GEMM_OK)
             return st;
-        if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, map_a, map_b, map_out, map_out, kp, pl.grid, stream)) != cudaSuccess)
+        if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, map_a, map_b, map_out, map_out, map_out, kp, pl.grid, stream)) != cudaSuccess)
             return fail_cuda(e, "GEMM kernel launch");
         return GEMM_OK;
     }
 
-    // Asking L2 for a unit's whole K range up front measured slower than the
-    // ring's own loads (the burst delays the first k-block), so it is opt-in.
-    kp.prefetch_l2 = (o && o->l2_prefetch == 2) ? 1 : 0;
-
     if (pl.fused_reduce) {
-        // Split-K summed inside the GEMM kernel: one launch.  Partials go to
-        // W[b*S + s] (M x ldw f32) through the output map, as for the separate
-        // reduction; the reduce map reads rows_per rows of all S splits of a tile.
-        const int64_t ldw = (pr.N + 3) / 4 * 4;
-        const int64_t partial_bytes = pr.batch * int64_t(pl.split_k) * pr.M * ldw * 4;
+        // Split partials summed inside the GEMM kernel: one launch.  Split
+        // units store their partial tile to the compact workspace
+        // [split unit][tile_m][tile_n] (workspace map); each reducer fetches
+        // rows_per rows of every split of its tile (reduce map).
+        const bool tail = pl.tail_split > 0;
+        const int32_t S = tail ? pl.tail_split : pl.split_k;
         const int64_t tiles = int64_t(pl.tiles_m) * pl.tiles_n * pr.batch;
+        const int64_t split_tiles = tail ? pl.tail_tiles : tiles;
+        const int64_t split_units = split_tiles * S;
+        const int64_t tile_elems = int64_t(pl.tile_m) * pl.tile_n;
         void *ws = nullptr;
         if ((e = cudaMallocFromPoolAsync(&ws, size_t(pl.workspace_bytes), ds->pool, stream)) != cudaSuccess)
             return fail_cuda(e, "split-K workspace allocation");
         const int64_t cpu = pl.tile_m == 2 * kTileM ? 2 : 1;
         kp.fused = 1;
-        kp.reducers = int32_t(pl.split_k * cpu);
+        kp.split_k = S;
+        kp.dp_units = tail ? tiles - split_tiles : 0;
+        kp.reducers = int32_t(S * cpu);
         kp.rows_per = int32_t((pl.tile_m + kp.reducers - 1) / kp.reducers);
-        kp.counters = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + partial_bytes);
-        alignas(64) CUtensorMap map_red;
-        st = encode_3d(&map_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ws, pr.N, pr.M,
-                       pr.batch * pl.split_k, ldw, int64_t(pr.M) * ldw, 32, 32,
-                       CU_TENSOR_MAP_L2_PROMOTION_NONE, "split-K workspace");
+        kp.counters = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + split_units * tile_elems * 4);
+        kp.timeout_ns = uint64_t(timeout_ns_for(o, pl));
+        alignas(64) CUtensorMap map_ws, map_red;
+        // C itself for the whole tiles (and as a valid map to prefetch).
+        if (N % 4) {
+            kp.n_tma = N & ~3;
+            kp.tail = 1;
+        }
+        const int64_t map_cols = kp.n_tma > 0 ? kp.n_tma : pr.N;
+        st = encode_3d(&map_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pr.C, map_cols, pr.M, pr.batch,
+                       pr.ldc, sC, 32, 32, CU_TENSOR_MAP_L2_PROMOTION_NONE, "C");
         if (st == GEMM_OK)
-            st = encode_3d(&map_red, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ws, pr.N, pr.M,
-                           pr.batch * pl.split_k, ldw, int64_t(pr.M) * ldw, uint32_t(pl.tile_n),
+            st = encode_3d(&map_ws, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ws, pl.tile_n, pl.tile_m,
+                           split_units, pl.tile_n, tile_elems, 32, 32,
+                           CU_TENSOR_MAP_L2_PROMOTION_NONE, "split-K workspace");
+        if (st == GEMM_OK)
+            st = encode_3d(&map_red, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ws, pl.tile_n, pl.tile_m,
+                           split_units, pl.tile_n, tile_elems, uint32_t(pl.tile_n),
                            uint32_t(kp.rows_per), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                           "split-K workspace (reduce)", uint32_t(pl.split_k),
-                           CU_TENSOR_MAP_SWIZZLE_NONE);
-        if (st == GEMM_OK && (e = cudaMemsetAsync(kp.counters, 0, size_t(tiles) * 4, stream)) != cudaSuccess)
+                           "split-K workspace (reduce)", uint32_t(S), CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (st == GEMM_OK &&
+            (e = cudaMemsetAsync(kp.counters, 0, size_t(split_tiles) * 4, stream)) != cudaSuccess)
             st = fail_cuda(e, "zeroing the split-K arrival counters");
         if (st == GEMM_OK &&
-            (e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, map_a, map_b, map_out, map_red, kp, pl.grid,
-                                     stream)) != cudaSuccess)
+            (e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, map_a, map_b, map_out, map_ws, map_red, kp,
+                                     pl.grid, stream)) != cudaSuccess)
             st = fail_cuda(e, "GEMM kernel launch");
         cudaFreeAsync(ws, stream);
         return st;
@@ -546,7 +608,7 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
                    pr.batch * pl.split_k, ldw, int64_t(pr.M) * ldw, 32, 32,
                    CU_TENSOR_MAP_L2_PROMOTION_NONE, "split-K workspace");
     if (st == GEMM_OK) {
-        if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, map_a, map_b, map_out, map_out, kp, pl.grid, stream)) != cudaSuccess)
+        if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, map_a, map_b, map_out, map_out, map_out, kp, pl.grid, stream)) != cudaSuccess)
             st = fail_cuda(e, "GEMM kernel launch");
     }
     if (st == GEMM_OK) {
@@ -827,7 +889,7 @@ extern "C" gemm_status_t gemm_f16_f32acc_splitk_noalloc(const uint16_t *A, const
         if ((st = encode_3d(&map_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, map_cols, M, 1, ldc,
                             M * ldc, 32, 32, CU_TENSOR_MAP_L2_PROMOTION_NONE, "C")) != GEMM_OK)
             return st;
-        if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, map_a, map_b, map_out, map_out, kp, pl.grid, stream)) != cudaSuccess)
+        if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, map_a, map_b, map_out, map_out, map_out, kp, pl.grid, stream)) != cudaSuccess)
             return fail_cuda(e, "GEMM kernel launch");
         return GEMM_OK;
     }
@@ -839,7 +901,7 @@ extern "C" gemm_status_t gemm_f16_f32acc_splitk_noalloc(const uint16_t *A, const
                         ldw, M * ldw, 32, 32, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                         "static split-K scratch")) != GEMM_OK)
         return st;
-    if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, map_a, map_b, map_out, map_out, kp, pl.grid, stream)) != cudaSuccess)
+    if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, map_a, map_b, map_out, map_out, map_out, kp, pl.grid, stream)) != cudaSuccess)
         return fail_cuda(e, "GEMM kernel launch");
     const int64_t threads = M * ((N + 3) / 4);
     const int grid = int(std::min<int64_t>((threads + 255) / 256, int64_t(nd->sms) * 8));

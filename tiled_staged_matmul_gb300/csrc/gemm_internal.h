@@ -49,6 +49,12 @@ struct KernelParams {
     int32_t fused;
     int32_t reducers;
     int32_t rows_per;
+    // With `fused`, units [0, dp_units) are whole tiles written straight to C
+    // (the full waves of a "split tail" plan) and units from dp_units on are
+    // split units, tile-major: unit dp_units + j computes split j % split_k
+    // of tile dp_units + j / split_k, and its partial goes to the compact
+    // workspace [j][tile_m][tile_n] (through the workspace map).
+    int64_t dp_units;
     int32_t prefetch_l2;  // 1: the producer first asks L2 for its unit's whole K range
     uint32_t *counters;
     // Optional per-CTA timeline (kTraceSlots globaltimer stamps per CTA), or null.
@@ -80,8 +86,9 @@ SmemBudget smem_budget(int tile_m, int tile_n);
 // Kernel-side entry points (defined in gemm_kernels.cu).
 cudaError_t set_kernel_attributes(int tile_m, int tile_n);
 cudaError_t launch_tcgen05_gemm(int tile_m, int tile_n, const CUtensorMap &map_a, const CUtensorMap &map_b,
-                                const CUtensorMap &map_out, const CUtensorMap &map_red,
-                                const KernelParams &p, int grid, cudaStream_t stream);
+                                const CUtensorMap &map_out, const CUtensorMap &map_ws,
+                                const CUtensorMap &map_red, const KernelParams &p, int grid,
+                                cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const float *W, float *C, int32_t M, int32_t N, int32_t S,
                                  int32_t batch, int64_t ldw, int64_t ldc, int64_t strideC,
                                  int grid, cudaStream_t stream);

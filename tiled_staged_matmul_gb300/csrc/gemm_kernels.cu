@@ -113,30 +113,67 @@ __device__ __forceinline__ uint64_t desc_b(uint32_t saddr)
 struct Unit {
     int32_t m0, n0;    // first row / column of the tile
     int32_t z_in;      // batch index of A and B
-    int32_t z_out;     // third coordinate of the output map
+    int32_t z_out;     // third coordinate of the output (or workspace) map
     int32_t kb0, kb1;  // k-block range [kb0, kb1)
+    int32_t split;     // fused split unit: 1 (its partial goes to the workspace), else 0
+    int32_t s;         // fused split unit: its split index
+    int64_t red_tile;  // fused split unit: index of its tile among the split tiles
 };
 
-// Work unit -> tile.  Units are ordered (batch, split) outermost, then the
-// tiles of one matrix in a grouped raster: group_m rows of tiles are walked
-// column by column, so CTAs running at the same time share A and B panels
-// in L2 ("Intel XPU Backend for Triton", section "Use Proper Type
-// Annotations": GROUP_SIZE_M in the GEMM signature).
-__device__ __forceinline__ Unit decode_unit(int64_t u, const KernelParams &p, int tile_m, int bn)
+// Tile index (within one matrix) -> first row / column, in a grouped raster:
+// group_m rows of tiles are walked column by column, so CTAs running at the
+// same time share A and B panels in L2 ("Intel XPU Backend for Triton",
+// section "Use Proper Type Annotations": GROUP_SIZE_M in the GEMM signature).
+__device__ __forceinline__ void raster(int64_t t, const KernelParams &p, int tile_m, int bn,
+                                       int32_t &m0, int32_t &n0)
 {
-    const int64_t tiles = int64_t(p.tiles_m) * p.tiles_n;
-    const int64_t z = u / tiles;
-    const int64_t t = u - z * tiles;
-    const int32_t b = int32_t(z / p.split_k);
-    const int32_t s = int32_t(z - int64_t(b) * p.split_k);
     const int64_t group = int64_t(p.group_m) * p.tiles_n;
     const int64_t g = t / group;
     const int32_t first_m = int32_t(g * p.group_m);
     const int32_t rows_in_group = min(p.tiles_m - first_m, p.group_m);
     const int64_t r = t - g * group;
+    m0 = (first_m + int32_t(r % rows_in_group)) * tile_m;
+    n0 = int32_t(r / rows_in_group) * bn;
+}
+
+// Work unit -> tile and K range.
+//   fused plans: units below dp_units are whole tiles; the others are split
+//     units, tile-major (the splits of one tile sit on neighbouring clusters).
+//   otherwise: (batch, split) outermost, then the tiles of one matrix; split
+//     partials go to [batch * split_k + s][M][ldw] for the reduce kernel.
+__device__ __forceinline__ Unit decode_unit(int64_t u, const KernelParams &p, int tile_m, int bn)
+{
+    const int64_t tiles = int64_t(p.tiles_m) * p.tiles_n;
     Unit w;
-    w.m0 = (first_m + int32_t(r % rows_in_group)) * tile_m;
-    w.n0 = int32_t(r / rows_in_group) * bn;
+    w.split = 0;
+    w.s = 0;
+    w.red_tile = 0;
+    if (p.fused) {
+        int64_t tg;  // tile index over all matrices of the batch
+        if (u < p.dp_units) {
+            tg = u;
+            w.kb0 = 0;
+            w.kb1 = p.k_blocks;
+        } else {
+            const int64_t j = u - p.dp_units;
+            w.red_tile = j / p.split_k;
+            w.s = int32_t(j - w.red_tile * p.split_k);
+            tg = p.dp_units + w.red_tile;
+            w.split = 1;
+            w.kb0 = int32_t(int64_t(w.s) * p.k_blocks / p.split_k);
+            w.kb1 = int32_t(int64_t(w.s + 1) * p.k_blocks / p.split_k);
+        }
+        const int64_t b = tg / tiles;
+        raster(tg - b * tiles, p, tile_m, bn, w.m0, w.n0);
+        w.z_in = int32_t(b);
+        w.z_out = w.split ? int32_t(u - p.dp_units) : int32_t(b);
+        return w;
+    }
+    const int64_t z = u / tiles;
+    const int64_t t = u - z * tiles;
+    const int32_t b = int32_t(z / p.split_k);
+    const int32_t s = int32_t(z - int64_t(b) * p.split_k);
+    raster(t, p, tile_m, bn, w.m0, w.n0);
     w.z_in = b;
     w.z_out = int32_t(z);  // == b when split_k == 1
     w.kb0 = int32_t(int64_t(s) * p.k_blocks / p.split_k);
@@ -192,6 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tsm_gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a,
                             const __grid_constant__ CUtensorMap map_b,
                             const __grid_constant__ CUtensorMap map_out,
+                            const __grid_constant__ CUtensorMap map_ws,
                             const __grid_constant__ CUtensorMap map_red, const KernelParams p)
 {
     using Cfg = TileCfg<BN, PAIR>;
@@ -245,8 +283,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tensormap(&map_a);
         ptx::prefetch_tensormap(&map_b);
         ptx::prefetch_tensormap(&map_out);
-        if (p.fused)
+        if (p.fused) {
+            ptx::prefetch_tensormap(&map_ws);
             ptx::prefetch_tensormap(&map_red);
+        }
     }
     __syncwarp();
     if constexpr (PAIR)
@@ -435,6 +475,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 const int32_t col0 = w.n0 + 32 * c;
+                if (w.split) {
+                    // Fused split unit: the partial tile goes to the compact workspace.
+                    if (lane == 0)
+                        ptx::bulk_wait_group_read<1>();
+                    __syncwarp();
+                    const uint32_t buf = bufs + sbuf * Cfg::EPI_BUF_BYTES;
+                    const uint32_t row_addr = buf + uint32_t(lane) * 128u;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        ptx::st_shared_v4(row_addr + (uint32_t(j ^ (lane & 7)) << 4), r[4 * j],
+                                          r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::tma_store_3d(&map_ws, buf, 32 * c, row_off + 32 * q, w.z_out);
+                        ptx::bulk_commit_group();
+                    }
+                    sbuf ^= 1u;
+                    continue;
+                }
                 if (col0 < p.n_tma) {
                     if (lane == 0)
                         ptx::bulk_wait_group_read<1>();  // the store that used this buffer has read it
@@ -490,36 +550,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (warp == 2 && lane == 0)
             trace_stamp(p, kTraceStored);
 
-        if (p.fused) {
+        // The CTA's last assigned unit decides whether it takes part in an
+        // in-kernel split-K sum (computed from the assignment, not from how
+        // far the loop got, so all four warps agree even after an abort).
+        int64_t last_u = -1;
+        if (cluster < p.num_units)
+            last_u = cluster + (p.num_units - 1 - cluster) / nclusters * nclusters;
+        const Unit w = last_u >= 0 ? decode_unit(last_u, p, Cfg::TILE_M, BN) : Unit{};
+        if (p.fused && last_u >= 0 && w.split) {
             // ---------------- in-kernel split-K sum
-            // Every cluster owns one unit.  Each CTA's partial is in the
-            // workspace (its TMA stores completed above); the CTA arrives on
-            // its tile's counter, waits (bounded) until all reducers =
-            // split_k x CTAs-per-unit have arrived, fetches rows_per rows of
-            // every split of the tile with one TMA load into the idle ring, sums
-            // them in ascending split order (the order of the separate reduce
-            // kernel, so the sums are bitwise the same) and writes C.  All four
-            // epilogue warps pass the three named barriers on every path.
+            // The CTA's partial is in the workspace (its TMA stores completed
+            // above); the CTA arrives on its tile's counter, waits (bounded)
+            // until all reducers = split_k x CTAs-per-unit have arrived, fetches
+            // rows_per rows of every split of the tile with one TMA load into
+            // the idle ring, sums them in ascending split order (the order of
+            // the separate reduce kernel, so the sums are bitwise the same) and
+            // writes C.  All four epilogue warps pass the three named barriers
+            // on every path.
             const int et = int(threadIdx.x) - 64;  // 0..127
             if (lane == 0) {
                 ptx::fence_proxy_async_global();  // this warp's TMA stores, before the release
                 __threadfence();
             }
             ptx::named_bar_sync(1, 128);
-            const Unit w = decode_unit(cluster, p, Cfg::TILE_M, BN);
-            const int64_t tiles = int64_t(p.tiles_m) * p.tiles_n;
-            const int64_t z = cluster / tiles;
-            const int64_t t = cluster - z * tiles;
-            const int64_t bz = z / p.split_k;
-            const int32_t sp = int32_t(z - bz * p.split_k);
-            const int32_t ri = sp * (PAIR ? 2 : 1) + int32_t(rank);
+            const int64_t bz = w.z_in;
+            const int32_t ri = w.s * (PAIR ? 2 : 1) + int32_t(rank);
             const int32_t r0 = ri * p.rows_per;               // first tile row this CTA sums
             const bool active = r0 < Cfg::TILE_M && w.m0 + r0 < p.M;
             const uint32_t box_bytes = uint32_t(p.rows_per) * BN * 4u * uint32_t(p.split_k);
             if (et == 0) {
                 uint32_t okv = 0;
                 if (!*abort_flag) {
-                    uint32_t *count = p.counters + (bz * tiles + t);
+                    uint32_t *count = p.counters + w.red_tile;
                     __threadfence();
                     atomicAdd(count, 1u);  // arrive
                     const uint32_t target = uint32_t(p.reducers);
@@ -550,9 +612,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         __threadfence();
                         ptx::fence_proxy_async_global();
                         ptx::mbar_arrive_expect_tx(red_bar, box_bytes);
-                        // box {BN columns, rows_per rows, split_k splits}
-                        ptx::tma_load_3d(base, &map_red, red_bar, w.n0, w.m0 + r0,
-                                         int32_t(bz * p.split_k));
+                        // box {BN columns, rows_per rows, split_k splits} of the
+                        // compact workspace, starting at this tile's first split
+                        ptx::tma_load_3d(base, &map_red, red_bar, 0, r0,
+                                         int32_t(w.red_tile * p.split_k));
                     }
                 }
                 *red_ok = okv;
@@ -716,8 +779,8 @@ cudaError_t set_kernel_attributes(int tile_m, int tile_n)
 
 template <int BN, bool PAIR>
 static cudaError_t launch_bn(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o,
-                             const CUtensorMap &r, const KernelParams &p, int grid,
-                             cudaStream_t stream)
+                             const CUtensorMap &ws, const CUtensorMap &r, const KernelParams &p,
+                             int grid, cudaStream_t stream)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(grid), 1, 1);
@@ -736,27 +799,27 @@ static cudaError_t launch_bn(const CUtensorMap &a, const CUtensorMap &b, const C
         cfg.attrs = nullptr;
         cfg.numAttrs = 0;
     }
-    return cudaLaunchKernelEx(&cfg, tsm_gemm_tcgen05_kernel<BN, PAIR>, a, b, o, r, p);
+    return cudaLaunchKernelEx(&cfg, tsm_gemm_tcgen05_kernel<BN, PAIR>, a, b, o, ws, r, p);
 }
 
 cudaError_t launch_tcgen05_gemm(int tile_m, int tile_n, const CUtensorMap &map_a,
                                 const CUtensorMap &map_b, const CUtensorMap &map_out,
-                                const CUtensorMap &map_red, const KernelParams &p, int grid,
-                                cudaStream_t stream)
+                                const CUtensorMap &map_ws, const CUtensorMap &map_red,
+                                const KernelParams &p, int grid, cudaStream_t stream)
 {
     if (tile_m == 2 * kTileM) {
         if (grid % 2)
             return cudaErrorInvalidValue;
         switch (tile_n) {
-        case 128: return launch_bn<128, true>(map_a, map_b, map_out, map_red, p, grid, stream);
-        case 256: return launch_bn<256, true>(map_a, map_b, map_out, map_red, p, grid, stream);
+        case 128: return launch_bn<128, true>(map_a, map_b, map_out, map_ws, map_red, p, grid, stream);
+        case 256: return launch_bn<256, true>(map_a, map_b, map_out, map_ws, map_red, p, grid, stream);
         default: return cudaErrorInvalidValue;
         }
     }
     switch (tile_n) {
-    case 64: return launch_bn<64, false>(map_a, map_b, map_out, map_red, p, grid, stream);
-    case 128: return launch_bn<128, false>(map_a, map_b, map_out, map_red, p, grid, stream);
-    case 256: return launch_bn<256, false>(map_a, map_b, map_out, map_red, p, grid, stream);
+    case 64: return launch_bn<64, false>(map_a, map_b, map_out, map_ws, map_red, p, grid, stream);
+    case 128: return launch_bn<128, false>(map_a, map_b, map_out, map_ws, map_red, p, grid, stream);
+    case 256: return launch_bn<256, false>(map_a, map_b, map_out, map_ws, map_red, p, grid, stream);
     default: return cudaErrorInvalidValue;
     }
 }
