@@ -135,7 +135,8 @@ typedef struct gemm_plan_info {
     int32_t group_m;      /* tiles of M walked together in the raster order */
     int64_t stage_bytes;  /* shared memory of one k-block: A tile + B tile */
     int64_t smem_bytes;   /* dynamic shared memory of one CTA */
-    int64_t workspace_bytes; /* split-K partials (0 when split_k == 1) */
+    int64_t workspace_bytes; /* split-K partials, plus arrival counters and a launch tag
+                                when summed in-kernel (0 when split_k == 1) */
     int32_t fused_reduce; /* 1: split partials are summed inside the GEMM kernel */
     int32_t tail_tiles;   /* with gemm_options_t.split_tail: the tiles of the partial last wave,
                              each split into tail_split K ranges summed in the kernel; 0: none */

@@ -161,14 +161,14 @@ def test_plan_invariants(b, M, N, K):
     ldw = -(-N // 4) * 4
     tile_bytes = p["tile_m"] * p["tile_n"] * 4
     if p["tail_split"]:
-        counters = -(-(p["tail_tiles"] * 4) // 16) * 16
+        counters = -(-(p["tail_tiles"] * 4) // 16) * 16 + 16  # + launch tag
         assert p["workspace_bytes"] == p["tail_tiles"] * p["tail_split"] * tile_bytes + counters
     elif p["split_k"] == 1:
         assert p["workspace_bytes"] == 0 and not p["fused_reduce"]
     elif p["fused_reduce"]:
         # one compact partial tile per split unit, one arrival counter per tile;
         # every cluster owns exactly one unit
-        counters = -(-(tiles * 4) // 16) * 16
+        counters = -(-(tiles * 4) // 16) * 16 + 16  # + launch tag
         assert p["workspace_bytes"] == tiles * p["split_k"] * tile_bytes + counters
         assert p["units"] * (2 if p["tile_m"] == 256 else 1) == p["grid"]
     else:

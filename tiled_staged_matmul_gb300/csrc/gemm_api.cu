@@ -17,6 +17,8 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
+#include <chrono>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -27,6 +29,24 @@ namespace tsm {
 namespace {
 
 thread_local std::string g_last_error;
+
+// A 64-bit value unique to each launch of this process (a bijective mix of a
+// per-process start value and a call counter), never 0, and unlikely to
+// equal any word another process or earlier data left in recycled memory.
+uint64_t next_launch_epoch()
+{
+    static const uint64_t start = uint64_t(std::chrono::steady_clock::now().time_since_epoch().count()) ^
+                                  (uint64_t(reinterpret_cast<uintptr_t>(&g_last_error)) << 17);
+    static std::atomic<uint64_t> calls{0};
+    for (;;) {
+        uint64_t z = start + 0x9e3779b97f4a7c15ull * (calls.fetch_add(1) + 1);
+        z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+        z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+        z ^= z >> 31;
+        if (z != 0)
+            return z;
+    }
+}
 
 gemm_status_t fail(gemm_status_t st, const char *fmt, ...)
 {
@@ -405,14 +425,15 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const ge
         }
     }
     // Split partials: in-kernel sums use a compact [split unit][tile_m][tile_n]
-    // workspace plus a counter per split tile; the reduce kernel reads
+    // workspace plus a counter per split tile and a 16-byte launch tag; the
+    // reduce kernel reads
     // [batch * split][M][ldw].
     const int64_t split_tiles = pl->tail_split ? pl->tail_tiles : (split > 1 ? tiles : 0);
     const int64_t split_units = pl->tail_split ? split_tiles * pl->tail_split : split_tiles * split;
     if (split == 1 && !pl->tail_split)
         pl->workspace_bytes = 0;
     else if (pl->fused_reduce)
-        pl->workspace_bytes = split_units * tile_elems_of(tm, bn) * 4 + (split_tiles * 4 + 15) / 16 * 16;
+        pl->workspace_bytes = split_units * tile_elems_of(tm, bn) * 4 + (split_tiles * 4 + 15) / 16 * 16 + 16;
     else
         pl->workspace_bytes = batch * int64_t(split) * M * ldw * 4;
     return GEMM_OK;
@@ -569,6 +590,10 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
         kp.reducers = int32_t(S * cpu);
         kp.rows_per = int32_t((pl.tile_m + kp.reducers - 1) / kp.reducers);
         kp.counters = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + split_units * tile_elems * 4);
+        kp.counter_words = int32_t(split_tiles);
+        kp.epoch_tag = reinterpret_cast<unsigned long long *>(
+            static_cast<char *>(ws) + split_units * tile_elems * 4 + (split_tiles * 4 + 15) / 16 * 16);
+        kp.epoch = next_launch_epoch();
         kp.timeout_ns = uint64_t(timeout_ns_for(o, pl));
         alignas(64) CUtensorMap map_ws, map_red;
         // C itself for the whole tiles (and as a valid map to prefetch).
@@ -588,9 +613,6 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
                            split_units, pl.tile_n, tile_elems, uint32_t(pl.tile_n),
                            uint32_t(kp.rows_per), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                            "split-K workspace (reduce)", uint32_t(S), CU_TENSOR_MAP_SWIZZLE_NONE);
-        if (st == GEMM_OK &&
-            (e = cudaMemsetAsync(kp.counters, 0, size_t(split_tiles) * 4, stream)) != cudaSuccess)
-            st = fail_cuda(e, "zeroing the split-K arrival counters");
         if (st == GEMM_OK &&
             (e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, map_a, map_b, map_out, map_ws, map_red, kp,
                                      pl.grid, stream)) != cudaSuccess)

@@ -45,7 +45,10 @@ struct KernelParams {
     // split_k x (CTAs per unit) reducers of a tile each own rows_per rows of
     // it, fetch those rows of every split with one TMA load (the reduce map)
     // and sum them in ascending split order.  counters holds one arrival
-    // count per tile, zeroed before the launch.
+    // count per split tile (counter_words of them); the workspace holds
+    // whatever its last user left there, so CTA 0 zeroes the counters at the
+    // start of the launch and then publishes `epoch` (unique to this launch)
+    // in *epoch_tag, and a CTA arrives only after it has read that epoch.
     int32_t fused;
     int32_t reducers;
     int32_t rows_per;
@@ -57,6 +60,9 @@ struct KernelParams {
     int64_t dp_units;
     int32_t prefetch_l2;  // 1: the producer first asks L2 for its unit's whole K range
     uint32_t *counters;
+    int32_t counter_words;
+    unsigned long long *epoch_tag;
+    unsigned long long epoch;  // never 0
     // Optional per-CTA timeline (kTraceSlots globaltimer stamps per CTA), or null.
     unsigned long long *trace;
 };

@@ -72,6 +72,9 @@ struct TileCfg {
     static constexpr uint32_t TMEM_COLS = 2 * BN;
     static constexpr uint32_t TEMPTY_ARRIVALS = PAIR ? 2 * EPI_WARPS : EPI_WARPS;
     static_assert(SMEM_BYTES > SMEM_LIMIT / 2, "one CTA per SM keeps TMEM allocation uncontended");
+    // The CTA's last unit stages all its output boxes in the idle ring at once.
+    static_assert(STAGES * STAGE_BYTES >= EPI_WARPS * (BN / 32) * EPI_BUF_BYTES,
+                  "the ring holds a whole output tile of one CTA");
 };
 
 // Instruction descriptor of tcgen05.mma.kind::f16: D f32 (bits 4-5 = 1),
@@ -214,6 +217,53 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
             }
         }
     }
+}
+
+// Bounded poll of a global word (acquire, GPU scope) until it equals `want`.
+// Returns false if the CTA's abort flag is raised or `timeout_ns` passes; a
+// timeout raises the flags and ORs `who` into the device status word.  Every
+// waiter polls the same word, so each poll backs off first.
+template <typename T>
+__device__ __forceinline__ bool poll_bounded(const T *word, T want, const AbortFlags &af,
+                                             uint32_t who)
+{
+    auto load = [word]() -> T {
+        if constexpr (sizeof(T) == 8)
+            return T(ptx::ld_acquire_gpu(reinterpret_cast<const unsigned long long *>(word)));
+        else
+            return T(ptx::ld_acquire_gpu_u32(reinterpret_cast<const uint32_t *>(word)));
+    };
+    if (load() == want)
+        return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        __nanosleep(64);
+        if (load() == want)
+            return true;
+        if ((it & 7u) == 0) {
+            if (*af.local)
+                return false;
+            if (ptx::globaltimer_ns() - t0 > af.timeout_ns) {
+                *af.local = 1u;
+                if (af.peer)
+                    ptx::st_cluster_u32(af.peer, 1u);
+                atomicOr(af.status, who);
+                return false;
+            }
+        }
+    }
+}
+
+// In-kernel split-K, run by one thread of CTA 0 at the start: zero this
+// launch's arrival counters, then publish the launch's epoch.  Kept out of
+// line: the kernels that do not sum in-kernel only pay for the call site.
+__device__ __noinline__ void publish_counters(uint32_t *counters, int32_t words,
+                                              unsigned long long *tag, uint64_t epoch)
+{
+    for (int32_t i = 0; i < words; ++i)
+        counters[i] = 0u;
+    __threadfence();
+    ptx::st_release_gpu(tag, epoch);
 }
 
 __device__ __forceinline__ void trace_stamp(const KernelParams &p, int slot)
@@ -442,6 +492,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;
         const uint32_t bufs = epi0 + uint32_t(e) * 2u * Cfg::EPI_BUF_BYTES;
         uint32_t abuf = 0, aphase = 0, sbuf = 0;
+        if (p.fused && blockIdx.x == 0 && threadIdx.x == 64)
+            publish_counters(p.counters, p.counter_words, p.epoch_tag, p.epoch);
         for (int64_t u = cluster; u < p.num_units; u += nclusters) {
             const Unit w = decode_unit(u, p, Cfg::TILE_M, BN);
             bool got = wait_bounded(tfull0 + 8u * abuf, aphase, af, kStatusEpilogue, true);
@@ -459,77 +511,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                 nch = live < BN / 32 ? live : BN / 32;
             }
             const uint32_t tm_row = tmem_base + (uint32_t(32 * q) << 16) + abuf * uint32_t(BN);
-            for (int c = 0; c < nch; ++c) {
-                uint32_t r[32];
-                ptx::tmem_ld_32x32b_x32(tm_row + 32u * c, r);
-                ptx::tmem_wait_ld();
-                if (c == nch - 1) {
-                    // Last read of this accumulator: hand it back to the MMA issuer.
-                    ptx::tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if constexpr (PAIR)
-                            ptx::mbar_arrive_cluster(tempty_lead0 + 8u * abuf);
-                        else
-                            ptx::mbar_arrive(tempty0 + 8u * abuf);
-                    }
-                }
+            const int32_t tail_row = row0 + lane;
+            // Row `lane` of a 32 x 32 box into `buf`, 16-byte chunk j at
+            // (j ^ row % 8): the layout the tensor maps' 128-byte swizzle expects.
+            auto stage_box = [&](uint32_t buf, const uint32_t (&r)[32]) {
+                const uint32_t row_addr = buf + uint32_t(lane) * 128u;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    ptx::st_shared_v4(row_addr + (uint32_t(j ^ (lane & 7)) << 4), r[4 * j],
+                                      r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+            };
+            // Box c goes out by TMA: a split partial to the compact workspace,
+            // or the columns of C below n_tma.
+            auto via_tma = [&](int c) { return w.split || w.n0 + 32 * c < p.n_tma; };
+            auto store_box = [&](int c, uint32_t buf) {  // lane 0
+                if (w.split)
+                    ptx::tma_store_3d(&map_ws, buf, 32 * c, row_off + 32 * q, w.z_out);
+                else
+                    ptx::tma_store_3d(&map_out, buf, w.n0 + 32 * c, row0, w.z_out);
+            };
+            // Columns [n_tma, N) of C: fewer than four, written one by one.
+            auto tail_box = [&](int c, const uint32_t (&r)[32]) {
                 const int32_t col0 = w.n0 + 32 * c;
-                if (w.split) {
-                    // Fused split unit: the partial tile goes to the compact workspace.
-                    if (lane == 0)
-                        ptx::bulk_wait_group_read<1>();
-                    __syncwarp();
-                    const uint32_t buf = bufs + sbuf * Cfg::EPI_BUF_BYTES;
-                    const uint32_t row_addr = buf + uint32_t(lane) * 128u;
+                if (!w.split && p.tail && col0 + 32 > p.n_tma && tail_row < p.M) {
+                    float *dst = p.c_direct + int64_t(w.z_out) * p.stride_c + int64_t(tail_row) * p.ldc;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        ptx::st_shared_v4(row_addr + (uint32_t(j ^ (lane & 7)) << 4), r[4 * j],
-                                          r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
-                    ptx::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        ptx::tma_store_3d(&map_ws, buf, 32 * c, row_off + 32 * q, w.z_out);
-                        ptx::bulk_commit_group();
-                    }
-                    sbuf ^= 1u;
-                    continue;
-                }
-                if (col0 < p.n_tma) {
-                    if (lane == 0)
-                        ptx::bulk_wait_group_read<1>();  // the store that used this buffer has read it
-                    __syncwarp();
-                    // Row `lane` of the 32 x 32 box, 16-byte chunk j at (j ^ row % 8):
-                    // the layout the tensor map's 128-byte swizzle expects.
-                    const uint32_t buf = bufs + sbuf * Cfg::EPI_BUF_BYTES;
-                    const uint32_t row_addr = buf + uint32_t(lane) * 128u;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        ptx::st_shared_v4(row_addr + (uint32_t(j ^ (lane & 7)) << 4), r[4 * j],
-                                          r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
-                    ptx::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        ptx::tma_store_3d(&map_out, buf, col0, row0, w.z_out);
-                        ptx::bulk_commit_group();
-                    }
-                    sbuf ^= 1u;
-                }
-                if (p.tail && col0 + 32 > p.n_tma) {
-                    // Columns [n_tma, N): fewer than four, written one by one.
-                    const int32_t row = row0 + lane;
-                    if (row < p.M) {
-                        float *dst = p.c_direct + int64_t(w.z_out) * p.stride_c + int64_t(row) * p.ldc;
-#pragma unroll
-                        for (int t = 0; t < 32; ++t) {
-                            const int32_t col = col0 + t;
-                            if (col >= p.n_tma && col < p.N)
-                                dst[col] = __uint_as_float(r[t]);
-                        }
+                    for (int t = 0; t < 32; ++t) {
+                        const int32_t col = col0 + t;
+                        if (col >= p.n_tma && col < p.N)
+                            dst[col] = __uint_as_float(r[t]);
                     }
                 }
-            }
-            if (nch == 0) {
+            };
+            // Last read of this accumulator: hand it back to the MMA issuer.
+            auto release_acc = [&]() {
                 ptx::tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) {
@@ -538,7 +553,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                     else
                         ptx::mbar_arrive(tempty0 + 8u * abuf);
                 }
+            };
+            // On the CTA's last unit the operand ring is idle: each box gets
+            // a buffer of its own there and no store waits for another.
+            const bool drain = u + nclusters >= p.num_units;
+            for (int c = 0; c < nch; ++c) {
+                uint32_t r[32];
+                ptx::tmem_ld_32x32b_x32(tm_row + 32u * c, r);
+                ptx::tmem_wait_ld();
+                if (c == nch - 1)
+                    release_acc();
+                if (via_tma(c)) {
+                    uint32_t buf;
+                    if (drain) {
+                        buf = base + (uint32_t(e) * uint32_t(BN / 32) + uint32_t(c)) * Cfg::EPI_BUF_BYTES;
+                    } else {
+                        if (lane == 0)
+                            ptx::bulk_wait_group_read<1>();
+                        __syncwarp();
+                        buf = bufs + sbuf * Cfg::EPI_BUF_BYTES;
+                        sbuf ^= 1u;
+                    }
+                    stage_box(buf, r);
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        store_box(c, buf);
+                        ptx::bulk_commit_group();
+                    }
+                }
+                tail_box(c, r);
             }
+            if (nch == 0)
+                release_acc();
             if (++abuf == 2) {
                 abuf = 0;
                 aphase ^= 1u;
@@ -568,10 +615,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             // writes C.  All four epilogue warps pass the three named barriers
             // on every path.
             const int et = int(threadIdx.x) - 64;  // 0..127
-            if (lane == 0) {
-                ptx::fence_proxy_async_global();  // this warp's TMA stores, before the release
-                __threadfence();
-            }
+            // The counters belong to this launch once CTA 0 has published the
+            // epoch, normally long before now: read it early (relaxed) and
+            // check it after the barrier; the GPU-scope fence before the
+            // arrival completes the acquire.
+            uint64_t epoch_now = 0;
+            if (et == 0)
+                epoch_now = ptx::ld_relaxed_gpu(p.epoch_tag);
+            // Each warp's TMA stores are complete (waited above); the proxy
+            // fence orders them before the warp's later generic accesses, the
+            // barrier before the arriving thread's, and that thread's
+            // GPU-scope fence (cumulative) before its arrival.
+            if (lane == 0)
+                ptx::fence_proxy_async_global();
             ptx::named_bar_sync(1, 128);
             const int64_t bz = w.z_in;
             const int32_t ri = w.s * (PAIR ? 2 : 1) + int32_t(rank);
@@ -580,36 +636,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t box_bytes = uint32_t(p.rows_per) * BN * 4u * uint32_t(p.split_k);
             if (et == 0) {
                 uint32_t okv = 0;
-                if (!*abort_flag) {
+                const bool epoch_ok = epoch_now == p.epoch ||
+                    poll_bounded<unsigned long long>(p.epoch_tag, p.epoch, af, kStatusReduce);
+                if (!*abort_flag && epoch_ok) {
                     uint32_t *count = p.counters + w.red_tile;
                     __threadfence();
                     atomicAdd(count, 1u);  // arrive
-                    const uint32_t target = uint32_t(p.reducers);
-                    okv = 1;
-                    if (ptx::ld_acquire_gpu_u32(count) != target) {
-                        const uint64_t t0 = ptx::globaltimer_ns();
-                        for (uint32_t it = 1;; ++it) {
-                            __nanosleep(64);  // every waiter polls the same word: back off
-                            if (ptx::ld_acquire_gpu_u32(count) == target)
-                                break;
-                            if ((it & 7u) == 0) {
-                                if (*abort_flag) {
-                                    okv = 0;
-                                    break;
-                                }
-                                if (ptx::globaltimer_ns() - t0 > p.timeout_ns) {
-                                    *abort_flag = 1u;
-                                    if (af.peer)
-                                        ptx::st_cluster_u32(af.peer, 1u);
-                                    atomicOr(p.status, kStatusReduce);
-                                    okv = 0;
-                                    break;
-                                }
-                            }
-                        }
-                    }
+                    okv = poll_bounded<uint32_t>(count, uint32_t(p.reducers), af, kStatusReduce);
                     if (okv && active) {
-                        __threadfence();
+                        // The acquire that saw the count orders this load
+                        // after every split's partial.
                         ptx::fence_proxy_async_global();
                         ptx::mbar_arrive_expect_tx(red_bar, box_bytes);
                         // box {BN columns, rows_per rows, split_k splits} of the
@@ -626,15 +662,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (wait_bounded(red_bar, 0, af, kStatusReduce, false)) {
                     const float4 *stg = reinterpret_cast<const float4 *>(base_ptr);
                     const int32_t per_split = p.rows_per * (BN / 4);  // float4s of one split
-                    for (int32_t f = et; f < per_split; f += 128) {
-                        float4 acc = stg[f];
-                        for (int32_t s2 = 1; s2 < p.split_k; ++s2) {
-                            const float4 v = stg[s2 * per_split + f];
-                            acc.x += v.x;
-                            acc.y += v.y;
-                            acc.z += v.z;
-                            acc.w += v.w;
-                        }
+                    const int32_t nsplit = p.split_k;
+                    auto put = [&](int32_t f, const float4 &acc) {
                         const int32_t row = f / (BN / 4);
                         const int32_t gr = w.m0 + r0 + row;
                         const int32_t gc = w.n0 + (f - row * (BN / 4)) * 4;
@@ -650,6 +679,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     dst[2] = acc.z;
                             }
                         }
+                    };
+                    // Two float4s per thread per pass, splits unrolled: the
+                    // shared-memory loads overlap, while each sum still adds
+                    // the splits one at a time in ascending order.
+                    for (int32_t f0 = et; f0 < per_split; f0 += 256) {
+                        const int32_t f1 = f0 + 128;
+                        const bool two = f1 < per_split;
+                        float4 a0 = stg[f0];
+                        float4 a1 = two ? stg[f1] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+                        for (int32_t s2 = 1; s2 < nsplit; ++s2) {
+                            const float4 v0 = stg[s2 * per_split + f0];
+                            const float4 v1 = two ? stg[s2 * per_split + f1] : v0;
+                            a0.x += v0.x;
+                            a0.y += v0.y;
+                            a0.z += v0.z;
+                            a0.w += v0.w;
+                            a1.x += v1.x;
+                            a1.y += v1.y;
+                            a1.z += v1.z;
+                            a1.w += v1.w;
+                        }
+                        put(f0, a0);
+                        if (two)
+                            put(f1, a1);
                     }
                 }
             }

@@ -178,11 +178,23 @@ __device__ __forceinline__ uint64_t ld_acquire_gpu(const unsigned long long *p)
     return v;
 }
 
+__device__ __forceinline__ uint64_t ld_relaxed_gpu(const unsigned long long *p)
+{
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ uint32_t ld_acquire_gpu_u32(const uint32_t *p)
 {
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(unsigned long long *p, uint64_t v)
+{
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 // Named barrier `id` over `count` threads (a multiple of 32) of this CTA.
