@@ -164,3 +164,35 @@ def exact_gemm(A, B, M: int, N: int, K: int, lda: int | None = None,
             row.append(s)
         out.append(row)
     return out
+
+
+def grouped_gemm_f64(A, B, group_rows, E: int, M: int, N: int, K: int, C=None,
+                     nthreads: int = 0) -> np.ndarray:
+    """Grouped (Mixture-of-Experts) GEMM in fp64.
+
+    The Mixture-of-Experts example of "Intel XPU Backend for Triton", section
+    "Use Tensor Descriptors to load tl.dot arguments and save results": expert
+    ``e`` multiplies only its first ``group_rows[e]`` token rows,
+    ``A[e, :group_rows[e], :] . B[e]``; an expert with no tokens does nothing,
+    and rows at or past its count are masked out, so C keeps whatever it held
+    there.
+
+    ``A`` is E x M x K and ``B`` E x K x N (f16, contiguous), ``group_rows``
+    holds E integers in [0, M].  ``C`` is the output's initial contents
+    (E x M x N; NaN when omitted).  Returns the E x M x N float64 result: for
+    each expert, the rows below its count from ``gemm_f64`` and the others
+    copied from ``C``."""
+    a = _as_u16(A).reshape(E, M, K)
+    b = _as_u16(B).reshape(E, K, N)
+    rows = [int(r) for r in np.asarray(group_rows).reshape(-1)[:E]]
+    if len(rows) != E:
+        raise ValueError("group_rows holds fewer than E counts")
+    out = (np.full((E, M, N), np.nan) if C is None
+           else np.array(C, dtype=np.float64, copy=True).reshape(E, M, N))
+    for e, m in enumerate(rows):
+        if not 0 <= m <= M:
+            raise ValueError(f"group_rows[{e}] = {m} is outside [0, {M}]")
+        if m == 0:
+            continue
+        out[e, :m, :] = gemm_f64(a[e, :m, :], b[e], m, N, K, nthreads=nthreads)
+    return out
