@@ -175,6 +175,44 @@ gemm_status_t gemm_f16_f32acc_opts(const uint16_t *A, const uint16_t *B, float *
                                    int64_t batch, const gemm_options_t *opts,
                                    gemm_stream_t stream);
 
+/* Grouped (Mixture-of-Experts) GEMM: for each group g < groups,
+ *     C[g][i][:] = A[g][i][:] . B[g]   for the rows i < group_rows[g],
+ * the group's matrices strideA, strideB and strideC elements apart like the
+ * batched call.  This is the pages' Mixture-of-Experts example ("Intel XPU
+ * Backend for Triton", section "Use Tensor Descriptors to load tl.dot
+ * arguments and save results": A is [E experts, M tokens, K features],
+ * expert e works on A[e, :e_num_tokens, :], an expert with no tokens does
+ * nothing and rows past its count are masked out).
+ *   group_rows  device memory, `groups` int32 row counts (4-byte aligned),
+ *               read by the kernel when it runs, so a preceding kernel on
+ *               `stream` may write them; each must lie in [0, M] -- a count
+ *               outside is clamped to that range and the next
+ *               gemm_get_device_status reports GEMM_ERR_INVALID_VALUE (with
+ *               K == 0 the counts only limit the rows zeroed)
+ *   A, B        device, as the batched call with batch = groups; rows of A[g]
+ *               at or past group_rows[g] must be readable (they are loaded
+ *               with the tile that crosses the count) but never reach C
+ *   C           device; rows at or past group_rows[g] of C[g] are left
+ *               untouched, as are elements past N
+ * M is the rows every group has room for.  No split-K (the work is known
+ * only on the device); groups of 256 go to one launch each, in stream
+ * order.  groups == 0, M == 0 or N == 0 queue nothing. */
+gemm_status_t gemm_f16_f32acc_grouped(const uint16_t *A, const uint16_t *B, float *C,
+                                      const int32_t *group_rows, int64_t groups,
+                                      int64_t M, int64_t N, int64_t K,
+                                      int64_t lda, int64_t ldb, int64_t ldc,
+                                      int64_t strideA, int64_t strideB, int64_t strideC,
+                                      gemm_stream_t stream);
+
+/* The grouped call with explicit options (NULL = all defaults; split_k and
+ * split_tail are ignored). */
+gemm_status_t gemm_f16_f32acc_grouped_opts(const uint16_t *A, const uint16_t *B, float *C,
+                                           const int32_t *group_rows, int64_t groups,
+                                           int64_t M, int64_t N, int64_t K,
+                                           int64_t lda, int64_t ldb, int64_t ldc,
+                                           int64_t strideA, int64_t strideB, int64_t strideC,
+                                           const gemm_options_t *opts, gemm_stream_t stream);
+
 /* The plan the library would use, computed on the host only (no GPU is
  * touched).  num_sms is the SM count to plan for (0 = the current device's).
  * This is the analogue of the pages' footprint check and K_TILE choice

@@ -92,6 +92,25 @@ def test_batched_strides_checked(b):
     assert b.gemm_status_string(st) == "GEMM_ERR_MISALIGNED"
 
 
+def test_grouped_host_checks(b):
+    G0 = 0x7f0030000000
+    args = (A0, B0, C0)
+    # groups < 0, NULL counts, misaligned counts: rejected on the host
+    st = b.gemm_f16_f32acc_grouped(*args, G0, -1, 4, 4, 4, 8, 8, 4, 32, 32, 16, 0)
+    assert b.gemm_status_string(st) == "GEMM_ERR_INVALID_VALUE"
+    st = b.gemm_f16_f32acc_grouped(*args, 0, 2, 4, 4, 4, 8, 8, 4, 32, 32, 16, 0)
+    assert b.gemm_status_string(st) == "GEMM_ERR_INVALID_VALUE"
+    st = b.gemm_f16_f32acc_grouped(*args, G0 + 2, 2, 4, 4, 4, 8, 8, 4, 32, 32, 16, 0)
+    assert b.gemm_status_string(st) == "GEMM_ERR_MISALIGNED"
+    # the batched rules apply per launch (overlapping groups of C)
+    st = b.gemm_f16_f32acc_grouped(*args, G0, 2, 4, 4, 4, 8, 8, 4, 32, 32, 8, 0)
+    assert b.gemm_status_string(st) == "GEMM_ERR_ALIAS"
+    # nothing to do: no groups, no rows, no columns
+    assert b.gemm_f16_f32acc_grouped(*args, G0, 0, 4, 4, 4, 8, 8, 4, 32, 32, 16, 0) == b.GEMM_OK
+    assert b.gemm_f16_f32acc_grouped(*args, G0, 3, 0, 4, 4, 8, 8, 4, 32, 32, 16, 0) == b.GEMM_OK
+    assert b.gemm_f16_f32acc_grouped(*args, G0, 3, 4, 0, 4, 8, 8, 8, 32, 32, 16, 0) == b.GEMM_OK
+
+
 # ---------------------------------------------------------------- planner
 
 SMS = 152

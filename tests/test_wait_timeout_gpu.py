@@ -56,3 +56,28 @@ def test_stalled_wait_times_out_and_the_next_call_is_exact(b, M, N, K, split_k, 
     b.check(b.gemm_get_device_status(s))
     ref = oracle.gemm_f64(A, B, M, N, K)
     assert np.array_equal(dC.cpu().numpy().astype(np.float64), ref)
+
+
+@pytest.mark.parametrize("tile_m,tile_n", [(128, 128), (256, 256)])
+def test_stalled_grouped_call_times_out_and_the_next_call_is_exact(b, tile_m, tile_n):
+    G, M, N, K = 4, 300, 256, 512
+    rows = [300, 0, 129, 17]
+    A, B = synthetic.operands(M, N, K, "int4", seed=41, batch=G)
+    dA, dB = A.cuda(), B.cuda()
+    dC = torch.zeros((G, M, N), dtype=torch.float32, device="cuda")
+    counts = torch.tensor(rows, dtype=torch.int32, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+
+    def call(stall, timeout_ms):
+        return b.gemm_f16_f32acc_grouped_opts(dA.data_ptr(), dB.data_ptr(), dC.data_ptr(),
+                                              counts.data_ptr(), G, M, N, K, K, N, N, M * K, K * N,
+                                              M * N, b.GemmOptions(0, tile_n, timeout_ms, stall,
+                                                                   tile_m), s)
+    assert b.gemm_get_device_status(s) == b.GEMM_OK
+    assert call(1, 200) == b.GEMM_OK
+    assert b.gemm_get_device_status(s) == b.GEMM_ERR_DEVICE_TIMEOUT
+    assert b.gemm_get_device_status(s) == b.GEMM_OK
+    b.check(call(0, 0))
+    b.check(b.gemm_get_device_status(s))
+    ref = oracle.grouped_gemm_f64(A, B, rows, G, M, N, K, C=np.zeros((G, M, N)))
+    assert np.array_equal(dC.cpu().numpy().astype(np.float64), ref)

@@ -81,6 +81,13 @@ def _load() -> ctypes.CDLL:
     lib.gemm_status_string.argtypes = [ctypes.c_int]
     lib.gemm_version.restype = ctypes.c_int32
     lib.gemm_version.argtypes = []
+    lib.gemm_f16_f32acc_grouped.restype = ctypes.c_int
+    lib.gemm_f16_f32acc_grouped.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64,
+                                            i64, i64, i64, vp]
+    lib.gemm_f16_f32acc_grouped_opts.restype = ctypes.c_int
+    lib.gemm_f16_f32acc_grouped_opts.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64,
+                                                 i64, i64, i64, i64, ctypes.POINTER(GemmOptions),
+                                                 vp]
     lib.gemm_f16_f32acc_splitk_noalloc.restype = ctypes.c_int
     lib.gemm_f16_f32acc_splitk_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64,
                                                    i32, vp]
@@ -112,6 +119,20 @@ def gemm_f16_f32acc_opts(A, B, C, M, N, K, lda, ldb, ldc, strideA, strideB, stri
     p = ctypes.byref(opts) if opts is not None else None
     return _lib.gemm_f16_f32acc_opts(A, B, C, M, N, K, lda, ldb, ldc, strideA, strideB,
                                      strideC, batch, p, stream)
+
+
+def gemm_f16_f32acc_grouped(A, B, C, group_rows, groups, M, N, K, lda, ldb, ldc, strideA,
+                            strideB, strideC, stream=0) -> int:
+    return _lib.gemm_f16_f32acc_grouped(A, B, C, group_rows, groups, M, N, K, lda, ldb, ldc,
+                                        strideA, strideB, strideC, stream)
+
+
+def gemm_f16_f32acc_grouped_opts(A, B, C, group_rows, groups, M, N, K, lda, ldb, ldc, strideA,
+                                 strideB, strideC, opts: GemmOptions | None = None,
+                                 stream=0) -> int:
+    p = ctypes.byref(opts) if opts is not None else None
+    return _lib.gemm_f16_f32acc_grouped_opts(A, B, C, group_rows, groups, M, N, K, lda, ldb, ldc,
+                                             strideA, strideB, strideC, p, stream)
 
 
 def gemm_f16_f32acc_splitk_noalloc(A, B, C, M, N, K, lda, ldb, ldc, split_k=0, stream=0) -> int:
@@ -204,6 +225,43 @@ def gemm(A, B, out=None, *, split_k=0, tile_n=0, tile_m=0, timeout_ms=0, inject_
     opts = _opts(split_k, tile_n, timeout_ms, inject_stall, tile_m)
     st = gemm_f16_f32acc_opts(A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K, lda, ldb,
                               ldc, sA, sB, sC, batch, opts, _stream_handle(stream))
+    check(st)
+    return out
+
+
+def grouped_gemm(A, B, group_rows, out=None, *, tile_n=0, tile_m=0, stream=None):
+    """Grouped (Mixture-of-Experts) GEMM on CUDA tensors: for each group g,
+    ``out[g, :group_rows[g]] = A[g, :group_rows[g]] @ B[g]``.
+
+    A is groups x M x K and B groups x K x N (f16), ``group_rows`` a CUDA
+    int32 tensor of ``groups`` row counts in [0, M].  Rows at or past a
+    group's count keep the contents of ``out`` (zeros when ``out`` is not
+    given).  Returns ``out`` (groups x M x N, f32)."""
+    import torch
+    if A.dtype != torch.float16 or B.dtype != torch.float16:
+        raise TypeError("A and B must be torch.float16")
+    if A.dim() != 3 or B.dim() != 3 or A.shape[0] != B.shape[0] or A.shape[2] != B.shape[1]:
+        raise ValueError("A must be G x M x K and B G x K x N")
+    if group_rows.dtype != torch.int32 or not group_rows.is_cuda or group_rows.numel() != A.shape[0]:
+        raise ValueError("group_rows must be a CUDA int32 tensor of one count per group")
+    G, M, K = A.shape
+    N = B.shape[2]
+    if out is None:
+        ldc_alloc = max(4, -(-N // 4) * 4)
+        out = torch.zeros((G, M, ldc_alloc), dtype=torch.float32, device=A.device)[..., :N]
+    if out.dtype != torch.float32 or tuple(out.shape) != (G, M, N):
+        raise ValueError("out must be a float32 G x M x N tensor")
+    for t, name, mult in ((A, "A", 8), (B, "B", 8), (out, "out", 4)):
+        if t.numel() and (t.stride(-1) != 1 or t.data_ptr() % 16 or t.stride(-2) % mult
+                          or t.stride(0) % mult):
+            raise ValueError(f"{name} needs a unit last stride, a 16-byte aligned base and row "
+                             f"and group strides that are multiples of {mult} elements")
+    rows = group_rows.contiguous()
+    opts = _opts(0, tile_n, 0, 0, tile_m)
+    st = gemm_f16_f32acc_grouped_opts(A.data_ptr(), B.data_ptr(), out.data_ptr(), rows.data_ptr(),
+                                      G, M, N, K, A.stride(1), B.stride(1), out.stride(1),
+                                      A.stride(0), B.stride(0), out.stride(0), opts,
+                                      _stream_handle(stream))
     check(st)
     return out
 

@@ -164,6 +164,9 @@ struct Problem {
     const uint16_t *B;
     float *C;
     int64_t M, N, K, lda, ldb, ldc, sA, sB, sC, batch;
+    // Grouped launch (at most kMaxGroupsPerLaunch groups = batches): device
+    // array of each group's row count; null for plain and batched GEMMs.
+    const int32_t *group_rows = nullptr;
 };
 
 // Bytes spanned by `batch` matrices of `rows` x `cols` elements of `elem`
@@ -491,11 +494,17 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
         return st;
     const int32_t M = int32_t(pr.M), N = int32_t(pr.N), batch = int32_t(pr.batch);
     const int64_t sC = pr.batch > 1 ? pr.sC : int64_t(pr.M) * pr.ldc;
+    if (pr.group_rows) {
+        if (pr.batch > kMaxGroupsPerLaunch)
+            return fail(GEMM_ERR_INVALID_VALUE, "at most %d groups per launch", kMaxGroupsPerLaunch);
+        if ((st = check_device_pointer(pr.group_rows, pr.batch * 4, dev, "group_rows")) != GEMM_OK)
+            return st;
+    }
 
     if (pr.K == 0) {
         const int64_t total = int64_t(M) * N * batch;
         const int grid = int(std::min<int64_t>((total + 255) / 256, int64_t(ds->sms) * 8));
-        if ((e = launch_zero_fill(pr.C, M, N, batch, pr.ldc, sC, grid, stream)) != cudaSuccess)
+        if ((e = launch_zero_fill(pr.C, M, N, batch, pr.ldc, sC, pr.group_rows, grid, stream)) != cudaSuccess)
             return fail_cuda(e, "zero-fill launch");
         return GEMM_OK;
     }
@@ -505,8 +514,18 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
     if ((st = check_device_pointer(pr.B, span_bytes(pr.batch, pr.sB, pr.K, pr.ldb, pr.N, 2), dev, "B")) != GEMM_OK)
         return st;
 
+    // A grouped launch's units are known only on the device, so it takes no
+    // split: every unit is a whole tile.
+    gemm_options_t og = {};
+    if (o)
+        og = *o;
+    if (pr.group_rows) {
+        og.split_k = 1;
+        og.split_tail = 0;
+    }
     gemm_plan_info_t pl;
-    if ((st = make_plan(pr.M, pr.N, pr.K, pr.batch, o, ds->sms, &pl)) != GEMM_OK)
+    if ((st = make_plan(pr.M, pr.N, pr.K, pr.batch, (o || pr.group_rows) ? &og : nullptr, ds->sms,
+                        &pl)) != GEMM_OK)
         return st;
     if (ds->smem_optin < pl.smem_bytes)
         return fail(GEMM_ERR_UNSUPPORTED_DEVICE, "device allows %d bytes of shared memory per block, the kernel needs %lld",
@@ -543,6 +562,8 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
     kp.timeout_ns = uint64_t(timeout_ns_for(o, pl));
     kp.status = ds->status;
     kp.trace = o ? reinterpret_cast<unsigned long long *>(o->trace) : nullptr;
+    kp.group_rows = pr.group_rows;
+    kp.groups = pr.group_rows ? batch : 0;
 
     kp.n_tma = N;
     kp.tail = 0;
@@ -679,6 +700,41 @@ gemm_status_t gemm_f16_f32acc_opts(const uint16_t *A, const uint16_t *B, float *
     return run(pr, opts, reinterpret_cast<cudaStream_t>(stream));
 }
 
+gemm_status_t gemm_f16_f32acc_grouped_opts(const uint16_t *A, const uint16_t *B, float *C,
+                                           const int32_t *group_rows, int64_t groups, int64_t M,
+                                           int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                                           int64_t strideA, int64_t strideB, int64_t strideC,
+                                           const gemm_options_t *opts, gemm_stream_t stream)
+{
+    g_last_error.clear();
+    if (groups < 0)
+        return fail(GEMM_ERR_INVALID_VALUE, "negative number of groups: %lld", (long long)groups);
+    if (groups > 0 && !group_rows)
+        return fail(GEMM_ERR_INVALID_VALUE, "group_rows is NULL");
+    if (reinterpret_cast<uintptr_t>(group_rows) & 3u)
+        return fail(GEMM_ERR_MISALIGNED, "group_rows must be 4-byte aligned");
+    // Launches of at most kMaxGroupsPerLaunch groups each, in stream order.
+    for (int64_t g0 = 0; g0 < groups; g0 += kMaxGroupsPerLaunch) {
+        const int64_t n = std::min<int64_t>(kMaxGroupsPerLaunch, groups - g0);
+        Problem pr{A ? A + g0 * strideA : A, B ? B + g0 * strideB : B, C ? C + g0 * strideC : C,
+                   M, N, K, lda, ldb, ldc, strideA, strideB, strideC, n};
+        pr.group_rows = group_rows + g0;
+        const gemm_status_t st = run(pr, opts, reinterpret_cast<cudaStream_t>(stream));
+        if (st != GEMM_OK)
+            return st;
+    }
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_f16_f32acc_grouped(const uint16_t *A, const uint16_t *B, float *C,
+                                      const int32_t *group_rows, int64_t groups, int64_t M, int64_t N,
+                                      int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int64_t strideA,
+                                      int64_t strideB, int64_t strideC, gemm_stream_t stream)
+{
+    return gemm_f16_f32acc_grouped_opts(A, B, C, group_rows, groups, M, N, K, lda, ldb, ldc, strideA,
+                                        strideB, strideC, nullptr, stream);
+}
+
 gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const gemm_options_t *opts,
                         int32_t num_sms, gemm_plan_info_t *plan)
 {
@@ -720,6 +776,9 @@ gemm_status_t gemm_get_device_status(gemm_stream_t stream)
         return GEMM_OK;
     const uint32_t zero = 0;
     cudaMemcpy(ds->status, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    if (word == kStatusGroupRows)
+        return fail(GEMM_ERR_INVALID_VALUE,
+                    "a grouped call had a row count outside [0, M]; it was clamped to that range");
     return fail(GEMM_ERR_DEVICE_TIMEOUT,
                 "a bounded device-side wait ran out (roles: %s%s%s%s%s); the output of that call is incomplete",
                 (word & kStatusProducer) ? "producer " : "", (word & kStatusMma) ? "mma " : "",

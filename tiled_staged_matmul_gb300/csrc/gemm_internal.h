@@ -18,6 +18,11 @@ constexpr uint32_t kStatusMma = 2u;
 constexpr uint32_t kStatusEpilogue = 4u;
 constexpr uint32_t kStatusDrain = 8u;
 constexpr uint32_t kStatusReduce = 16u;
+constexpr uint32_t kStatusGroupRows = 32u;  // a group's row count outside [0, M] (clamped)
+
+// Grouped launches: at most this many groups per launch (the per-CTA table of
+// tile offsets lives in the shared-memory control block).
+constexpr int kMaxGroupsPerLaunch = 256;
 
 // Everything the persistent kernel needs besides its three tensor maps.
 struct KernelParams {
@@ -63,6 +68,13 @@ struct KernelParams {
     int32_t counter_words;
     unsigned long long *epoch_tag;
     unsigned long long epoch;  // never 0
+    // Grouped (Mixture-of-Experts) launch: group g = batch index g has
+    // group_rows[g] valid rows (device memory, clamped to [0, M]); its tiles
+    // are ceil(rows / tile) x tiles_n, numbered after those of groups < g, and
+    // rows at or past the count are neither stored nor summed.  Null: every
+    // batch has M rows.  groups <= kMaxGroupsPerLaunch.
+    const int32_t *group_rows;
+    int32_t groups;
     // Optional per-CTA timeline (kTraceSlots globaltimer stamps per CTA), or null.
     unsigned long long *trace;
 };
@@ -99,7 +111,7 @@ cudaError_t launch_splitk_reduce(const float *W, float *C, int32_t M, int32_t N,
                                  int32_t batch, int64_t ldw, int64_t ldc, int64_t strideC,
                                  int grid, cudaStream_t stream);
 cudaError_t launch_zero_fill(float *C, int32_t M, int32_t N, int32_t batch, int64_t ldc,
-                             int64_t strideC, int grid, cudaStream_t stream);
+                             int64_t strideC, const int32_t *group_rows, int grid, cudaStream_t stream);
 cudaError_t device_status_word(uint32_t **ptr);
 
 }  // namespace tsm

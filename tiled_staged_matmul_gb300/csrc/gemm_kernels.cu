@@ -60,13 +60,17 @@ struct TileCfg {
     static constexpr int EPI_WARPS = 4;
     static constexpr int EPI_BUF_BYTES = 32 * 32 * 4;      // one 32 x 32 f32 box
     static constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BUF_BYTES;
-    static constexpr int CTRL_BYTES = 1024;
+    static constexpr int CTRL_BYTES = 2048;      // barriers and slots, then the group table
+    static constexpr int GROUP_TABLE_OFF = 1024; // kMaxGroupsPerLaunch x 4 bytes
     static constexpr int ALIGN_SLACK = 1024;
     static constexpr int SMEM_LIMIT = 232448;              // 227 KiB opt-in per block
     static constexpr int STAGES_FIT =
         (SMEM_LIMIT - ALIGN_SLACK - EPI_BYTES - CTRL_BYTES) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
     static_assert(STAGES >= 2, "the ring needs at least two stages");
+    static_assert(16 * STAGES + 80 <= GROUP_TABLE_OFF &&
+                      GROUP_TABLE_OFF + 4 * kMaxGroupsPerLaunch <= CTRL_BYTES,
+                  "control block layout");
     static constexpr int SMEM_BYTES = ALIGN_SLACK + STAGES * STAGE_BYTES + EPI_BYTES + CTRL_BYTES;
     // Two accumulators of BN f32 columns each per CTA (a power of two >= 32).
     static constexpr uint32_t TMEM_COLS = 2 * BN;
@@ -121,19 +125,20 @@ struct Unit {
     int32_t split;     // fused split unit: 1 (its partial goes to the workspace), else 0
     int32_t s;         // fused split unit: its split index
     int64_t red_tile;  // fused split unit: index of its tile among the split tiles
+    int32_t rows;      // rows of the matrix: M, or the group's count in a grouped launch
 };
 
 // Tile index (within one matrix) -> first row / column, in a grouped raster:
 // group_m rows of tiles are walked column by column, so CTAs running at the
 // same time share A and B panels in L2 ("Intel XPU Backend for Triton",
 // section "Use Proper Type Annotations": GROUP_SIZE_M in the GEMM signature).
-__device__ __forceinline__ void raster(int64_t t, const KernelParams &p, int tile_m, int bn,
-                                       int32_t &m0, int32_t &n0)
+__device__ __forceinline__ void raster(int64_t t, const KernelParams &p, int32_t tiles_m, int tile_m,
+                                       int bn, int32_t &m0, int32_t &n0)
 {
     const int64_t group = int64_t(p.group_m) * p.tiles_n;
     const int64_t g = t / group;
     const int32_t first_m = int32_t(g * p.group_m);
-    const int32_t rows_in_group = min(p.tiles_m - first_m, p.group_m);
+    const int32_t rows_in_group = min(tiles_m - first_m, p.group_m);
     const int64_t r = t - g * group;
     m0 = (first_m + int32_t(r % rows_in_group)) * tile_m;
     n0 = int32_t(r / rows_in_group) * bn;
@@ -142,15 +147,38 @@ __device__ __forceinline__ void raster(int64_t t, const KernelParams &p, int til
 // Work unit -> tile and K range.
 //   fused plans: units below dp_units are whole tiles; the others are split
 //     units, tile-major (the splits of one tile sit on neighbouring clusters).
+//   grouped launches: the group whose tiles hold u (binary search of `gtab`,
+//     the inclusive tile counts per group), then its tiles as in one matrix.
 //   otherwise: (batch, split) outermost, then the tiles of one matrix; split
 //     partials go to [batch * split_k + s][M][ldw] for the reduce kernel.
-__device__ __forceinline__ Unit decode_unit(int64_t u, const KernelParams &p, int tile_m, int bn)
+__device__ __forceinline__ Unit decode_unit(int64_t u, const KernelParams &p, const uint32_t *gtab,
+                                            int tile_m, int bn)
 {
     const int64_t tiles = int64_t(p.tiles_m) * p.tiles_n;
     Unit w;
     w.split = 0;
     w.s = 0;
     w.red_tile = 0;
+    w.rows = p.M;
+    if (p.group_rows) {
+        int32_t lo = 0, hi = p.groups - 1;
+        while (lo < hi) {
+            const int32_t mid = (lo + hi) >> 1;
+            if (int64_t(gtab[mid]) > u)
+                hi = mid;
+            else
+                lo = mid + 1;
+        }
+        const int64_t first = lo ? int64_t(gtab[lo - 1]) : 0;
+        const int32_t tiles_m = int32_t((int64_t(gtab[lo]) - first) / p.tiles_n);
+        raster(u - first, p, tiles_m, tile_m, bn, w.m0, w.n0);
+        w.z_in = lo;
+        w.z_out = lo;
+        w.kb0 = 0;
+        w.kb1 = p.k_blocks;
+        w.rows = min(max(p.group_rows[lo], 0), p.M);
+        return w;
+    }
     if (p.fused) {
         int64_t tg;  // tile index over all matrices of the batch
         if (u < p.dp_units) {
@@ -167,7 +195,7 @@ __device__ __forceinline__ Unit decode_unit(int64_t u, const KernelParams &p, in
             w.kb1 = int32_t(int64_t(w.s + 1) * p.k_blocks / p.split_k);
         }
         const int64_t b = tg / tiles;
-        raster(tg - b * tiles, p, tile_m, bn, w.m0, w.n0);
+        raster(tg - b * tiles, p, p.tiles_m, tile_m, bn, w.m0, w.n0);
         w.z_in = int32_t(b);
         w.z_out = w.split ? int32_t(u - p.dp_units) : int32_t(b);
         return w;
@@ -176,7 +204,7 @@ __device__ __forceinline__ Unit decode_unit(int64_t u, const KernelParams &p, in
     const int64_t t = u - z * tiles;
     const int32_t b = int32_t(z / p.split_k);
     const int32_t s = int32_t(z - int64_t(b) * p.split_k);
-    raster(t, p, tile_m, bn, w.m0, w.n0);
+    raster(t, p, p.tiles_m, tile_m, bn, w.m0, w.n0);
     w.z_in = b;
     w.z_out = int32_t(z);  // == b when split_k == 1
     w.kb0 = int32_t(int64_t(s) * p.k_blocks / p.split_k);
@@ -254,6 +282,49 @@ __device__ __forceinline__ bool poll_bounded(const T *word, T want, const AbortF
     }
 }
 
+// Grouped launch, run by the 32 lanes of one warp before the CTA barrier:
+// table[g] = the number of tiles of groups 0..g, each group having
+// ceil(rows / tile_m) x tiles_n tiles for its row count clamped to [0, M]
+// (a count outside that range raises kStatusGroupRows).  The prefix is an
+// inclusive scan: eight groups per lane, then the lanes' sums by shuffles.
+__device__ __noinline__ void build_group_table(const int32_t *group_rows, int32_t groups, int32_t M,
+                                               int32_t tile_m, int32_t tiles_n, uint32_t *table,
+                                               uint32_t *status)
+{
+    constexpr int PER = kMaxGroupsPerLaunch / 32;
+    const int lane = int(threadIdx.x & 31);
+    uint32_t incl[PER];
+    uint32_t sum = 0;
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int g = lane * PER + i;
+        if (g < groups) {
+            int64_t r = group_rows[g];
+            if (r < 0 || r > M) {
+                bad = true;
+                r = r < 0 ? 0 : M;
+            }
+            sum += uint32_t((r + tile_m - 1) / tile_m) * uint32_t(tiles_n);
+        }
+        incl[i] = sum;
+    }
+    uint32_t scan = sum;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, scan, d);
+        if (lane >= d)
+            scan += v;
+    }
+    const uint32_t before = scan - sum;
+#pragma unroll
+    for (int i = 0; i < PER; ++i)
+        if (lane * PER + i < groups)
+            table[lane * PER + i] = before + incl[i];
+    if (bad)
+        atomicOr(status, kStatusGroupRows);
+}
+
 // In-kernel split-K, run by one thread of CTA 0 at the start: zero this
 // launch's arrival counters, then publish the launch's epoch.  Kept out of
 // line: the kernels that do not sum in-kernel only pay for the call site.
@@ -304,6 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t done_bar = ctrl + 16u * S + 32u;  // all MMAs of this CTA (pair) completed
     const uint32_t stall_bar = ctrl + 16u * S + 40u; // never signalled (test hook)
     uint32_t *const tmem_slot = reinterpret_cast<uint32_t *>(ctrl_ptr + 16 * S + 48);
+    uint32_t *const gtab = reinterpret_cast<uint32_t *>(ctrl_ptr + Cfg::GROUP_TABLE_OFF);
     volatile uint32_t *const abort_flag = tmem_slot + 1;
     volatile uint32_t *const red_ok = tmem_slot + 2;  // in-kernel split-K: go / no-go
     const uint32_t red_bar = ctrl + 16u * S + 64u;    // in-kernel split-K: partial chunks landed
@@ -344,11 +416,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         ptx::tmem_alloc<PAIR>(ptx::smem_addr(tmem_slot), Cfg::TMEM_COLS);
         ptx::tmem_relinquish<PAIR>();
+    } else if (warp == 2 && p.group_rows) {
+        build_group_table(p.group_rows, p.groups, p.M, Cfg::TILE_M, p.tiles_n, gtab, p.status);
     }
     ptx::tc_fence_before_sync();
     ptx::cta_sync();
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // Work units of this launch: fixed, or (grouped) the tiles of all groups.
+    const int64_t num_units = p.group_rows ? int64_t(gtab[p.groups - 1]) : p.num_units;
     if (threadIdx.x == 0)
         trace_stamp(p, kTraceSetup);
 
@@ -370,8 +446,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t stage = 0, phase = 0;
             uint64_t issued = 0;
             bool ok = true;
-            for (int64_t u = cluster; ok && u < p.num_units; u += nclusters) {
-                const Unit w = decode_unit(u, p, Cfg::TILE_M, BN);
+            for (int64_t u = cluster; ok && u < num_units; u += nclusters) {
+                const Unit w = decode_unit(u, p, gtab, Cfg::TILE_M, BN);
                 if (p.prefetch_l2) {
                     // The unit's whole K range of A and B at once: DRAM sees the
                     // requests together (better page locality than the ring's
@@ -441,8 +517,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint16_t both = PAIR ? 3 : 1;
             uint32_t stage = 0, phase = 0, abuf = 0, aphase = 0;
             bool ok = true;
-            for (int64_t u = cluster; ok && u < p.num_units; u += nclusters) {
-                const Unit w = decode_unit(u, p, Cfg::TILE_M, BN);
+            for (int64_t u = cluster; ok && u < num_units; u += nclusters) {
+                const Unit w = decode_unit(u, p, gtab, Cfg::TILE_M, BN);
                 if (!wait_bounded(tempty0 + 8u * abuf, aphase ^ 1u, af, kStatusMma, true)) {
                     ok = false;
                     break;
@@ -494,8 +570,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t abuf = 0, aphase = 0, sbuf = 0;
         if (p.fused && blockIdx.x == 0 && threadIdx.x == 64)
             publish_counters(p.counters, p.counter_words, p.epoch_tag, p.epoch);
-        for (int64_t u = cluster; u < p.num_units; u += nclusters) {
-            const Unit w = decode_unit(u, p, Cfg::TILE_M, BN);
+        for (int64_t u = cluster; u < num_units; u += nclusters) {
+            const Unit w = decode_unit(u, p, gtab, Cfg::TILE_M, BN);
             bool got = wait_bounded(tfull0 + 8u * abuf, aphase, af, kStatusEpilogue, true);
             if (p.inject_stall && got)
                 got = wait_bounded(stall_bar, 0, af, kStatusEpilogue, true);
@@ -506,12 +582,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 trace_stamp(p, kTraceAccReady);
             const int32_t row0 = w.m0 + row_off + 32 * q;
             int nch = 0;
-            if (row0 < p.M) {
+            if (row0 < w.rows) {
                 const int live = (p.N - w.n0 + 31) / 32;
                 nch = live < BN / 32 ? live : BN / 32;
             }
             const uint32_t tm_row = tmem_base + (uint32_t(32 * q) << 16) + abuf * uint32_t(BN);
             const int32_t tail_row = row0 + lane;
+            // A grouped launch's C map spans all M rows, so a warp whose rows
+            // cross the group's count writes its rows below it with plain
+            // stores instead of TMA.
+            const bool rows_partial = p.group_rows != nullptr && row0 + 32 > w.rows;
             // Row `lane` of a 32 x 32 box into `buf`, 16-byte chunk j at
             // (j ^ row % 8): the layout the tensor maps' 128-byte swizzle expects.
             auto stage_box = [&](uint32_t buf, const uint32_t (&r)[32]) {
@@ -522,23 +602,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
             };
             // Box c goes out by TMA: a split partial to the compact workspace,
-            // or the columns of C below n_tma.
-            auto via_tma = [&](int c) { return w.split || w.n0 + 32 * c < p.n_tma; };
+            // or the columns of C below n_tma (whole 32-row boxes only).
+            auto via_tma = [&](int c) { return w.split || (!rows_partial && w.n0 + 32 * c < p.n_tma); };
             auto store_box = [&](int c, uint32_t buf) {  // lane 0
                 if (w.split)
                     ptx::tma_store_3d(&map_ws, buf, 32 * c, row_off + 32 * q, w.z_out);
                 else
                     ptx::tma_store_3d(&map_out, buf, w.n0 + 32 * c, row0, w.z_out);
             };
-            // Columns [n_tma, N) of C: fewer than four, written one by one.
+            // Plain stores: columns [n_tma, N) of C (fewer than four), or the
+            // whole row of a warp that crosses its group's row count.
             auto tail_box = [&](int c, const uint32_t (&r)[32]) {
                 const int32_t col0 = w.n0 + 32 * c;
-                if (!w.split && p.tail && col0 + 32 > p.n_tma && tail_row < p.M) {
+                const int32_t from = rows_partial ? col0 : p.n_tma;
+                if (!w.split && (rows_partial || (p.tail && col0 + 32 > p.n_tma)) && tail_row < w.rows) {
                     float *dst = p.c_direct + int64_t(w.z_out) * p.stride_c + int64_t(tail_row) * p.ldc;
 #pragma unroll
                     for (int t = 0; t < 32; ++t) {
                         const int32_t col = col0 + t;
-                        if (col >= p.n_tma && col < p.N)
+                        if (col >= from && col < p.N)
                             dst[col] = __uint_as_float(r[t]);
                     }
                 }
@@ -556,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             // On the CTA's last unit the operand ring is idle: each box gets
             // a buffer of its own there and no store waits for another.
-            const bool drain = u + nclusters >= p.num_units;
+            const bool drain = u + nclusters >= num_units;
             for (int c = 0; c < nch; ++c) {
                 uint32_t r[32];
                 ptx::tmem_ld_32x32b_x32(tm_row + 32u * c, r);
@@ -601,9 +683,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // in-kernel split-K sum (computed from the assignment, not from how
         // far the loop got, so all four warps agree even after an abort).
         int64_t last_u = -1;
-        if (cluster < p.num_units)
-            last_u = cluster + (p.num_units - 1 - cluster) / nclusters * nclusters;
-        const Unit w = last_u >= 0 ? decode_unit(last_u, p, Cfg::TILE_M, BN) : Unit{};
+        if (cluster < num_units)
+            last_u = cluster + (num_units - 1 - cluster) / nclusters * nclusters;
+        const Unit w = last_u >= 0 ? decode_unit(last_u, p, gtab, Cfg::TILE_M, BN) : Unit{};
         if (p.fused && last_u >= 0 && w.split) {
             // ---------------- in-kernel split-K sum
             // The CTA's partial is in the workspace (its TMA stores completed
@@ -769,10 +851,11 @@ __global__ void __launch_bounds__(256)
     }
 }
 
-// K == 0: every cell is the empty sum.
+// K == 0: every cell is the empty sum (in a grouped launch, every cell of
+// the rows below the group's count, clamped to [0, M]).
 __global__ void __launch_bounds__(256)
     tsm_zero_fill_kernel(float *__restrict__ C, int32_t M, int32_t N, int32_t batch, int64_t ldc,
-                         int64_t strideC)
+                         int64_t strideC, const int32_t *__restrict__ group_rows)
 {
     const int64_t per_mat = int64_t(M) * N;
     const int64_t total = per_mat * batch;
@@ -782,6 +865,8 @@ __global__ void __launch_bounds__(256)
         const int64_t r = idx - b * per_mat;
         const int64_t i = r / N;
         const int64_t j = r - i * N;
+        if (group_rows && i >= group_rows[b])
+            continue;
         C[b * strideC + i * ldc + j] = 0.0f;
     }
 }
@@ -887,9 +972,9 @@ cudaError_t launch_splitk_reduce(const float *W, float *C, int32_t M, int32_t N,
 }
 
 cudaError_t launch_zero_fill(float *C, int32_t M, int32_t N, int32_t batch, int64_t ldc,
-                             int64_t strideC, int grid, cudaStream_t stream)
+                             int64_t strideC, const int32_t *group_rows, int grid, cudaStream_t stream)
 {
-    tsm_zero_fill_kernel<<<grid, 256, 0, stream>>>(C, M, N, batch, ldc, strideC);
+    tsm_zero_fill_kernel<<<grid, 256, 0, stream>>>(C, M, N, batch, ldc, strideC, group_rows);
     return cudaGetLastError();
 }
 

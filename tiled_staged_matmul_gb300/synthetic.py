@@ -119,3 +119,70 @@ def operands(M: int, N: int, K: int, dist: str, seed: int, batch: int = 1,
 
 def workload_operands(w: Workload, **kw):
     return operands(w.M, w.N, w.K, w.dist, w.seed, w.batch, **kw)
+
+
+# ------------------------------------------------------------------ grouped
+
+@dataclass(frozen=True)
+class GroupedWorkload:
+    """A Mixture-of-Experts shape: ``groups`` experts, each with room for M
+    token rows; ``tokens`` routed token slots are spread over the experts by
+    ``group_counts`` (so each expert's row count is known only once drawn)."""
+    name: str
+    groups: int
+    M: int
+    N: int
+    K: int
+    tokens: int
+    dist: str
+    seed: int
+
+    def counts(self) -> torch.Tensor:
+        return group_counts(self.groups, self.M, self.tokens, self.seed)
+
+    def flops(self, counts=None) -> int:
+        c = self.counts() if counts is None else counts
+        return 2 * int(c.sum()) * self.N * self.K
+
+    def algorithmic_bytes(self, counts=None) -> int:
+        """The used rows of A once (f16), every expert's B once (f16), the
+        used rows of C once (f32)."""
+        rows = int((self.counts() if counts is None else counts).sum())
+        return 2 * rows * self.K + 2 * self.groups * self.K * self.N + 4 * rows * self.N
+
+
+def group_counts(groups: int, M: int, tokens: int, seed: int) -> torch.Tensor:
+    """Row counts of a routed batch (int32, CPU): every token slot picks an
+    expert at random, expert e with probability softmax(z)[e] for z ~ N(0, 1)
+    drawn once (some experts popular, some nearly idle); an expert keeps at
+    most M slots (the rest are dropped, as a capacity limit does)."""
+    gen = torch.Generator().manual_seed(int(seed) + 7)
+    z = torch.randn(groups, generator=gen, dtype=torch.float64)
+    probs = torch.softmax(z, dim=0)
+    picks = torch.multinomial(probs, tokens, replacement=True, generator=gen)
+    counts = torch.bincount(picks, minlength=groups).clamp(max=M)
+    return counts.to(torch.int32)
+
+
+def grouped_operands(w: GroupedWorkload):
+    """A (groups x M x K) and B (groups x K x N) f16 CPU tensors: A drawn
+    first, then B, from one generator seeded with the workload's seed."""
+    gen = torch.Generator().manual_seed(int(w.seed))
+    a = draw((w.groups, w.M, w.K), w.dist, gen, w.K)
+    b = draw((w.groups, w.K, w.N), w.dist, gen, w.K)
+    return a, b
+
+
+# Two expert layouts, rows drawn from N(0, 1/sqrt(K)): a few wide experts
+# (8 experts of 4096 x 14336, 16384 routed slots = 8192 tokens x top-2) and
+# many narrow ones (64 experts of 2048 x 1408, 24576 slots = 4096 tokens x
+# top-6), each expert with room for M rows.
+GROUPED_WORKLOADS = {
+    w.name: w
+    for w in (
+        GroupedWorkload("moe_8x4096x14336x4096_normal_invsqrtk", 8, 4096, 14336, 4096, 16384,
+                        "normal_invsqrtk", 2000),
+        GroupedWorkload("moe_64x512x1408x2048_normal_invsqrtk", 64, 512, 1408, 2048, 24576,
+                        "normal_invsqrtk", 2001),
+    )
+}
