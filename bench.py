@@ -45,7 +45,8 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                   help="one of the named workloads in tiled_staged_matmul_gb300.synthetic")
+                   help="one of the named workloads in tiled_staged_matmul_gb300.synthetic "
+                        "(WORKLOADS, or GROUPED_WORKLOADS for the grouped call)")
     p.add_argument("--shape", default=None,
                    help="MxNxK: an ad-hoc shape with N(0, 1/sqrt(K)) operands instead of --workload")
     p.add_argument("--tile-m", type=int, default=0, help="128 or 256 (CTA pair); 0: planner")
@@ -193,6 +194,132 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ our arm
 
+def timed_loop(args, call, flush, stream, world, local_rank):
+    """W untimed warm-up steps, then K steps each bracketed by CUDA events on
+    the launching stream (L2 flushed before every step when ``flush`` is
+    given), a barrier and a device synchronisation on both sides, SM clocks
+    sampled throughout.  Returns (ms per step, wall start, wall end, sampler)."""
+    import torch
+    from tiled_staged_matmul_gb300 import binding
+    for _ in range(max(args.warmup, 3)):
+        if flush:
+            flush()
+        call()
+    binding.check(binding.gemm_get_device_status(stream.cuda_stream))
+    torch.cuda.synchronize()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(args.steps):
+        if flush:
+            flush()
+        starts[i].record(stream)
+        call()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t1 = time.time()
+    time.sleep(0.1)
+    sampler.stop()
+    binding.check(binding.gemm_get_device_status(stream.cuda_stream))
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)], t0, t1, sampler
+
+
+def roofline_of(flops, algorithmic_bytes, ms, traffic, kernel):
+    """Achieved against the slower of the two roofs: dense tensor peak for
+    the flops, HBM bandwidth for the algorithmic bytes (both measured)."""
+    peaks = measured_peaks()
+    tflops_launch = flops / (ms * 1e-3) / 1e12
+    gbs_launch = algorithmic_bytes / (ms * 1e-3) / 1e9
+    t_tensor = flops / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = algorithmic_bytes / (peaks["hbm_gbs"] * 1e9)
+    if t_tensor >= t_hbm:
+        roofline = {"bound": "tensor", "achieved": round(tflops_launch, 2),
+                    "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": round(tflops_launch / peaks["bf16_tflops"], 4)}
+    else:
+        roofline = {"bound": "hbm", "achieved": round(gbs_launch, 1), "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": round(gbs_launch / peaks["hbm_gbs"], 4)}
+    roofline["traffic"] = traffic
+    roofline["peak_source"] = (f"{peaks['source']} (MEASURED_PEAKS.json bf16 burst; f16 dense "
+                               "rate taken equal to bf16, the nominal ratio)"
+                               if roofline["bound"] == "tensor" else
+                               f"{peaks['source']} (MEASURED_PEAKS.json copy bandwidth)")
+    roofline["kernel"] = kernel
+    return roofline
+
+
+def run_grouped(args, rank, local_rank, world):
+    """A grouped (Mixture-of-Experts) workload: one step is one grouped call
+    over every expert's routed rows; the metric counts the flops of those
+    rows only (2 x rows x N x K summed over the experts)."""
+    import torch
+    from tiled_staged_matmul_gb300 import binding, synthetic
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = synthetic.GROUPED_WORKLOADS[args.workload]
+    A_h, B_h = synthetic.grouped_operands(w)
+    counts_h = w.counts()
+    A, B, counts = A_h.to(dev), B_h.to(dev), counts_h.to(dev)
+    C = torch.empty((w.groups, w.M, w.N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    opts = binding.GemmOptions(0, args.tile_n, 0, 0, args.tile_m)
+    per_launch = min(w.groups, 256)
+    plan = binding.gemm_plan(w.M, w.N, w.K, per_launch, binding.GemmOptions(1, args.tile_n, 0, 0,
+                                                                            args.tile_m))
+    launches_per_call = -(-w.groups // 256)
+    flops = w.flops(counts_h)
+    abytes = w.algorithmic_bytes(counts_h)
+    working_set = 2 * A.numel() + 2 * B.numel() + 4 * C.numel()
+    flush = working_set < 2 * L2_BYTES
+    scrub = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    sweep = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    sink = torch.empty(1, dtype=torch.float32, device=dev) if flush else None
+
+    def flush_l2():
+        scrub.zero_()
+        torch.sum(sweep, dim=0, keepdim=True, out=sink)
+
+    def call():
+        binding.check(binding.gemm_f16_f32acc_grouped_opts(
+            A.data_ptr(), B.data_ptr(), C.data_ptr(), counts.data_ptr(), w.groups, w.M, w.N, w.K,
+            w.K, w.N, w.N, w.M * w.K, w.K * w.N, w.M * w.N, opts, stream.cuda_stream))
+
+    per_step_ms, t0, t1, sampler = timed_loop(args, call, flush_l2 if flush else None, stream,
+                                              world, local_rank)
+    ms_local = sum(per_step_ms) / len(per_step_ms)
+    value, ms = replica_throughput(flops, ms_local, world, dev)
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "groups": w.groups, "M": w.M, "N": w.N, "K": w.K,
+                   "routed_rows": int(counts_h.sum()), "tokens": w.tokens, "dist": w.dist,
+                   "seed": w.seed, "accumulate": "f32", "tile_m": plan["tile_m"],
+                   "tile_n": plan["tile_n"], "split_k": 1, "stages": plan["stages"],
+                   "grid": plan["grid"],
+                   "l2": "flushed before every step (write 2xL2, then read 2xL2)" if flush else
+                         f"inputs+output {working_set / 2**20:.0f} MiB > L2, no flush",
+                   "parallelism": f"replicas x{world}"},
+        "gpu_launches": args.steps * launches_per_call,
+        "roofline": roofline_of(flops, abytes, ms_local, recorded_traffic(w.name),
+                                "tsm_gemm_tcgen05_kernel (grouped)"),
+    }
+    clocks = sampler.summary(t0, t1)
+    result["clocks"] = {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = grouped_cpu_baseline(w, A_h, B_h, counts_h, target_s=15.0)
+    return result
+
+
 def run_ours(args, rank, local_rank, world):
     import torch
     from tiled_staged_matmul_gb300 import binding, synthetic
@@ -227,57 +354,13 @@ def run_ours(args, rank, local_rank, world):
                                                    w.M, w.N, w.K, w.K, w.N, w.N, 0, 0, 0, 1,
                                                    o, stream.cuda_stream))
 
-    for _ in range(max(args.warmup, 3)):
-        if flush:
-            flush_l2()
-        call()
-    binding.check(binding.gemm_get_device_status(stream.cuda_stream))
-    torch.cuda.synchronize()
-
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    sampler = ClockSampler(local_rank)
-    sampler.start()
-    time.sleep(0.3)
-    barrier(world)
-    torch.cuda.synchronize()
-    t0 = time.time()
-    for i in range(args.steps):
-        if flush:
-            flush_l2()
-        starts[i].record(stream)
-        call()
-        ends[i].record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    t1 = time.time()
-    time.sleep(0.1)
-    sampler.stop()
-    binding.check(binding.gemm_get_device_status(stream.cuda_stream))
-
-    per_step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    per_step_ms, t0, t1, sampler = timed_loop(args, call, flush_l2 if flush else None, stream,
+                                              world, local_rank)
     ms_local = sum(per_step_ms) / len(per_step_ms)
     value, ms = replica_throughput(w.flops, ms_local, world, dev)
-
-    peaks = measured_peaks()
-    tflops_launch = w.flops / (ms_local * 1e-3) / 1e12
-    gbs_launch = w.algorithmic_bytes / (ms_local * 1e-3) / 1e9
-    t_tensor = w.flops / (peaks["bf16_tflops"] * 1e12)
-    t_hbm = w.algorithmic_bytes / (peaks["hbm_gbs"] * 1e9)
-    if t_tensor >= t_hbm:
-        roofline = {"bound": "tensor", "achieved": round(tflops_launch, 2),
-                    "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                    "frac": round(tflops_launch / peaks["bf16_tflops"], 4)}
-    else:
-        roofline = {"bound": "hbm", "achieved": round(gbs_launch, 1), "peak": peaks["hbm_gbs"],
-                    "unit": "GB/s", "frac": round(gbs_launch / peaks["hbm_gbs"], 4)}
-    roofline["traffic"] = recorded_traffic(w.name)
-    roofline["peak_source"] = (f"{peaks['source']} (MEASURED_PEAKS.json bf16 burst; f16 dense "
-                               "rate taken equal to bf16, the nominal ratio)"
-                               if roofline["bound"] == "tensor" else
-                               f"{peaks['source']} (MEASURED_PEAKS.json copy bandwidth)")
-    roofline["kernel"] = "tsm_gemm_tcgen05_kernel" + (" + tsm_splitk_reduce_kernel"
-                                                      if launches_per_call > 1 else "")
+    roofline = roofline_of(w.flops, w.algorithmic_bytes, ms_local, recorded_traffic(w.name),
+                           "tsm_gemm_tcgen05_kernel" + (" + tsm_splitk_reduce_kernel"
+                                                        if launches_per_call > 1 else ""))
 
     result = {
         "metric": METRIC,
@@ -416,11 +499,40 @@ def cpu_baseline(w, A_h, B_h, target_s: float):
                       f"OpenMP over rows"}
 
 
+def grouped_cpu_baseline(w, A_h, B_h, counts_h, target_s: float):
+    """The oracle on a bounded sample of a grouped workload: the first rows
+    of the busiest experts, in turn, until about ``target_s`` seconds."""
+    import oracle
+    order = sorted(range(w.groups), key=lambda g: -int(counts_h[g]))
+    per_row = 2 * w.N * w.K
+    t_total, flops, used = 0.0, 0, []
+    rows = 1
+    for g in order:
+        r = min(int(counts_h[g]), rows)
+        if r == 0:
+            continue
+        t = time.perf_counter()
+        oracle.gemm_f64(A_h[g, :r].contiguous(), B_h[g], r, w.N, w.K)
+        dt = time.perf_counter() - t
+        t_total += dt
+        flops += r * per_row
+        used.append((g, r))
+        if t_total >= target_s:
+            break
+        rows = max(1, min(w.M, int(r * (target_s - t_total) / max(dt, 1e-6) / 4)))
+    return {"value": round(flops / max(t_total, 1e-9) / 1e12, 6), "unit": "TFLOP/s",
+            "cores": oracle.threads(), "kind": "oracle", "seconds": round(t_total, 2),
+            "sample": f"{sum(r for _, r in used)} routed rows from {len(used)} experts "
+                      f"(x {w.N} x {w.K}), fp64 triple loop, OpenMP over rows"}
+
+
 def run_reference(args, rank, world):
     """The reference arm: the CPU oracle, each step a bounded row sample."""
     import oracle
     from tiled_staged_matmul_gb300 import synthetic
 
+    if args.workload in synthetic.GROUPED_WORKLOADS and not args.shape:
+        return run_grouped_reference(args, world)
     w = pick_workload(args)
     A_h, B_h = synthetic.workload_operands(w)
     rows = max(1, min(w.M, int(4e9 // (2 * w.N * w.K)) or 1))
@@ -445,6 +557,44 @@ def run_reference(args, rank, world):
     }
 
 
+def run_grouped_reference(args, world):
+    """The reference arm on a grouped workload: each step the oracle computes
+    a bounded sample of routed rows (the first rows of the busiest expert)."""
+    import oracle
+    from tiled_staged_matmul_gb300 import synthetic
+
+    w = synthetic.GROUPED_WORKLOADS[args.workload]
+    A_h, B_h = synthetic.grouped_operands(w)
+    counts = w.counts()
+    g = int(max(range(w.groups), key=lambda e: int(counts[e])))
+    rows = max(1, min(int(counts[g]), int(4e9 // (2 * w.N * w.K)) or 1))
+
+    def step():
+        t = time.perf_counter()
+        oracle.gemm_f64(A_h[g, :rows].contiguous(), B_h[g], rows, w.N, w.K)
+        return time.perf_counter() - t
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    times = [step() for _ in range(args.steps)]
+    t = sum(times) / len(times)
+    value = 2 * rows * w.N * w.K / t / 1e12
+    sample = (f"{rows} routed rows of expert {g} per step ({rows} x {w.N} x {w.K}), "
+              "fp64 triple loop")
+    return {
+        "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": w.name, "groups": w.groups, "M": w.M, "N": w.N, "K": w.K,
+                   "dist": w.dist, "seed": w.seed},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
 def main(argv=None):
     args = parse_args(argv)
     rank, local_rank, world = dist_env()
@@ -458,7 +608,11 @@ def main(argv=None):
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-    result = run_ours(args, rank, local_rank, world)
+    from tiled_staged_matmul_gb300 import synthetic
+    if args.workload in synthetic.GROUPED_WORKLOADS:
+        result = run_grouped(args, rank, local_rank, world)
+    else:
+        result = run_ours(args, rank, local_rank, world)
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:
