@@ -54,6 +54,9 @@ def parse_args(argv=None):
     p.add_argument("--split-k", type=int, default=0, help="K ranges; 0: planner")
     p.add_argument("--splitk-reduce", type=int, default=0,
                    help="0/2: in-kernel split-K sum when possible, 1: separate reduce kernel")
+    p.add_argument("--ld-pad", type=int, default=0,
+                   help="lay A, B and C out with lda = K + p, ldb = ldc = N + p elements; an odd p "
+                        "makes every operand unaddressable by the TMA (the repacking path)")
     p.add_argument("--trace", action="store_true",
                    help="add a per-CTA phase timeline (one extra traced step) to the JSON line")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -328,13 +331,22 @@ def run_ours(args, rank, local_rank, world):
     dev = torch.device("cuda", local_rank)
     w = pick_workload(args)
     A_h, B_h = synthetic.workload_operands(w)
-    A = A_h.to(dev)
-    B = B_h.to(dev)
-    C = torch.empty((w.M, w.N), dtype=torch.float32, device=dev)
+    pad = args.ld_pad
+    lda, ldb, ldc = w.K + pad, w.N + pad, w.N + pad
+    A = torch.empty((w.M, lda), dtype=torch.float16, device=dev)[:, :w.K]
+    B = torch.empty((w.K, ldb), dtype=torch.float16, device=dev)[:, :w.N]
+    A.copy_(A_h)
+    B.copy_(B_h)
+    C = torch.empty((w.M, ldc), dtype=torch.float32, device=dev)[:, :w.N]
     stream = torch.cuda.current_stream()
     opts = binding.GemmOptions(args.split_k, args.tile_n, 0, 0, args.tile_m, args.splitk_reduce)
     plan = binding.gemm_plan(w.M, w.N, w.K, 1, opts)
     launches_per_call = 2 if plan["split_k"] > 1 and not plan["fused_reduce"] else 1
+    # Row pitches that are not multiples of 16 bytes: that operand is copied
+    # (A and B in, C out) around the GEMM.
+    copies = int(lda % 8 != 0) + int(ldb % 8 != 0) + int(ldc % 4 != 0)
+    repacked = copies > 0
+    launches_per_call += copies
 
     working_set = 2 * w.M * w.K + 2 * w.K * w.N + 4 * w.M * w.N
     flush = working_set < 2 * L2_BYTES
@@ -351,16 +363,19 @@ def run_ours(args, rank, local_rank, world):
 
     def call(o=opts):
         binding.check(binding.gemm_f16_f32acc_opts(A.data_ptr(), B.data_ptr(), C.data_ptr(),
-                                                   w.M, w.N, w.K, w.K, w.N, w.N, 0, 0, 0, 1,
+                                                   w.M, w.N, w.K, lda, ldb, ldc, 0, 0, 0, 1,
                                                    o, stream.cuda_stream))
 
     per_step_ms, t0, t1, sampler = timed_loop(args, call, flush_l2 if flush else None, stream,
                                               world, local_rank)
     ms_local = sum(per_step_ms) / len(per_step_ms)
     value, ms = replica_throughput(w.flops, ms_local, world, dev)
-    roofline = roofline_of(w.flops, w.algorithmic_bytes, ms_local, recorded_traffic(w.name),
+    roofline = roofline_of(w.flops, w.algorithmic_bytes, ms_local,
+                           recorded_traffic(w.name) if not pad else None,
                            "tsm_gemm_tcgen05_kernel" + (" + tsm_splitk_reduce_kernel"
-                                                        if launches_per_call > 1 else ""))
+                                                        if plan["split_k"] > 1
+                                                        and not plan["fused_reduce"] else "")
+                           + (f" + {copies} x tsm_pitch_copy_kernel" if repacked else ""))
 
     result = {
         "metric": METRIC,
@@ -381,6 +396,9 @@ def run_ours(args, rank, local_rank, world):
                    "splitk_sum": ("in-kernel" if plan["fused_reduce"] else "separate kernel")
                    if plan["split_k"] > 1 else "none",
                    "stages": plan["stages"], "grid": plan["grid"],
+                   "ld": [lda, ldb, ldc],
+                   "layout": (f"repacked ({copies} operand copies: row pitches not multiples "
+                              "of 16 bytes)" if repacked else "TMA-addressable"),
                    "l2": "flushed before every step (write 2xL2, then read 2xL2)" if flush else
                          f"inputs+output {working_set / 2**20:.0f} MiB > L2, no flush",
                    "parallelism": f"replicas x{world}"},

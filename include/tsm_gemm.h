@@ -38,9 +38,18 @@
  * Memory and ownership.  A, B and C are DEVICE pointers on the current CUDA
  * device, owned by the caller (for example torch tensors), and must stay
  * valid until the work queued on `stream` has finished.  The library owns
- * only its split-K workspace, taken from a private stream-ordered memory
- * pool on `stream` and returned to it on the same stream, and a small
- * per-device status word.
+ * only its scratch -- the split-K workspace, and packed copies of operands
+ * the tensor-memory accelerator cannot address (below) -- taken from a
+ * private stream-ordered memory pool on `stream` and returned to it on the
+ * same stream, and a small per-device status word.
+ *
+ * Layout.  The fast path loads A and B and stores C with the tensor-memory
+ * accelerator, which needs 16-byte aligned bases and row (and batch)
+ * pitches that are multiples of 16 bytes: lda, ldb (and strideA, strideB)
+ * multiples of 8 elements, ldc (strideC) a multiple of 4.  Any other pitch
+ * or an otherwise aligned base is accepted too: that operand is first copied
+ * into a packed, aligned scratch layout (C is computed there and copied
+ * out), which costs one extra read and write of it through HBM.
  *
  * Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  * default stream).  Argument errors are found on the host, before anything
@@ -52,9 +61,8 @@
  * Requirements, each checked (the status returned is in brackets):
  *   M, N, K >= 0 and < 2^31                          [INVALID_VALUE]
  *   lda >= K, ldb >= N, ldc >= N (elements)          [INVALID_VALUE]
- *   A, B, C 16-byte aligned; lda and ldb multiples
- *   of 8, ldc a multiple of 4 (16-byte row pitch,
- *   the tensor-memory-accelerator's rule)            [MISALIGNED]
+ *   A, B 2-byte and C 4-byte aligned (elements at
+ *   their natural alignment)                         [MISALIGNED]
  *   A, B, C device memory of the current device,
  *   each spanning the rows it is said to have        [INVALID_VALUE]
  *   C's bytes overlap neither A's nor B's            [ALIAS]
@@ -78,7 +86,8 @@ typedef struct CUstream_st *gemm_stream_t;
 typedef enum gemm_status {
     GEMM_OK = 0,
     GEMM_ERR_INVALID_VALUE = 1,      /* null pointer, bad size or stride, not device memory */
-    GEMM_ERR_MISALIGNED = 2,         /* base not 16-byte aligned, or row pitch not a multiple of 16 bytes */
+    GEMM_ERR_MISALIGNED = 2,         /* an element not at its natural alignment (any call), or a
+                                        layout the no-allocation entry point cannot address */
     GEMM_ERR_ALIAS = 3,              /* C overlaps A or B, or two batches of C overlap */
     GEMM_ERR_UNSUPPORTED_DEVICE = 4, /* not a compute-capability 10.3 device */
     GEMM_ERR_CUDA = 5,               /* a CUDA runtime or driver call failed; see gemm_last_error_string */
@@ -158,9 +167,9 @@ gemm_status_t gemm_f16_f32acc(const uint16_t *A, const uint16_t *B, float *C,
  * `strideB` and `strideC` elements apart (int64; the pages' MoE example
  * indexes a 3-D [E, M, K] tensor by expert with such a stride -- "Intel XPU
  * Backend for Triton", section "Use Tensor Descriptors ...", the A[E, :M, :]
- * slice, and section "Avoid int32 Overflow").  Strides must be multiples of 8
- * (A, B) and 4 (C) elements; with batch > 1 they must be positive and the
- * batches of C must not overlap. */
+ * slice, and section "Avoid int32 Overflow").  With batch > 1 the strides
+ * must be positive and the batches of C must not overlap; strides that are
+ * not multiples of 8 (A, B) or 4 (C) elements take the repacking path. */
 gemm_status_t gemm_f16_f32acc_batched(const uint16_t *A, const uint16_t *B, float *C,
                                       int64_t M, int64_t N, int64_t K,
                                       int64_t lda, int64_t ldb, int64_t ldc,
@@ -238,7 +247,10 @@ gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int64_t batch,
  * instead of the stream-ordered pool.  A plan whose partials need more than
  * 16 MiB (S x M x round_up(N, 4) x 4 bytes) is rejected with
  * GEMM_ERR_INVALID_VALUE and a message naming the size.  K == 0 is rejected
- * too; use gemm_f16_f32acc for it.
+ * too; use gemm_f16_f32acc for it.  Having no scratch to repack into, it
+ * also rejects any layout the tensor-memory accelerator cannot address
+ * (GEMM_ERR_MISALIGNED: A, B, C need 16-byte aligned bases, lda and ldb
+ * multiples of 8, ldc a multiple of 4).
  *
  * The first call on a device resolves the array's device address and
  * queries the device (no allocation); make that first call before any
@@ -255,8 +267,9 @@ gemm_status_t gemm_f16_f32acc_splitk_noalloc(const uint16_t *A, const uint16_t *
 
 /* Waits for `stream`, then reports and clears the current device's status
  * word: GEMM_OK, or GEMM_ERR_DEVICE_TIMEOUT if a bounded wait of an earlier
- * call ran out (that call's output is then incomplete), or GEMM_ERR_CUDA if
- * the stream reported an error. */
+ * call ran out (that call's output is then incomplete), GEMM_ERR_INVALID_VALUE
+ * if a grouped call met a row count outside [0, M] (it was clamped), or
+ * GEMM_ERR_CUDA if the stream reported an error. */
 gemm_status_t gemm_get_device_status(gemm_stream_t stream);
 
 /* The message of the last failed call on this host thread ("" if none). */

@@ -60,11 +60,9 @@ A0, B0, C0 = 0x7f0000000000, 0x7f0010000000, 0x7f0020000000
     ((A0, B0, C0, 4, 16, 4, 8, 8, 16), "GEMM_ERR_INVALID_VALUE"),     # ldb < N
     ((A0, B0, C0, 4, 8, 4, 8, 8, 4), "GEMM_ERR_INVALID_VALUE"),       # ldc < N
     ((0, B0, C0, 4, 4, 4, 8, 8, 4), "GEMM_ERR_INVALID_VALUE"),        # A NULL
-    ((A0 + 2, B0, C0, 4, 4, 4, 8, 8, 4), "GEMM_ERR_MISALIGNED"),      # A not 16-byte aligned
-    ((A0, B0, C0 + 4, 4, 4, 4, 8, 8, 4), "GEMM_ERR_MISALIGNED"),      # C not 16-byte aligned
-    ((A0, B0, C0, 4, 4, 4, 12, 8, 4), "GEMM_ERR_MISALIGNED"),         # lda not a multiple of 8
-    ((A0, B0, C0, 4, 4, 4, 8, 12, 4), "GEMM_ERR_MISALIGNED"),         # ldb not a multiple of 8
-    ((A0, B0, C0, 4, 4, 4, 8, 8, 6), "GEMM_ERR_MISALIGNED"),          # ldc not a multiple of 4
+    ((A0 + 1, B0, C0, 4, 4, 4, 8, 8, 4), "GEMM_ERR_MISALIGNED"),      # A: f16 at an odd address
+    ((A0, B0 + 3, C0, 4, 4, 4, 8, 8, 4), "GEMM_ERR_MISALIGNED"),      # B: f16 at an odd address
+    ((A0, B0, C0 + 2, 4, 4, 4, 8, 8, 4), "GEMM_ERR_MISALIGNED"),      # C: f32 not 4-byte aligned
     ((A0, B0, A0 + 16, 4, 4, 4, 8, 8, 4), "GEMM_ERR_ALIAS"),          # C inside A
     ((A0, B0, B0, 4, 4, 4, 8, 8, 4), "GEMM_ERR_ALIAS"),               # C on B
 ])
@@ -87,9 +85,8 @@ def test_batched_strides_checked(b):
     # non-positive stride with batch > 1
     st = b.gemm_f16_f32acc_batched(A0, B0, C0, 4, 4, 4, 8, 8, 4, 0, 32, 16, 2, 0)
     assert b.gemm_status_string(st) == "GEMM_ERR_INVALID_VALUE"
-    # stride not a multiple of 8 elements
-    st = b.gemm_f16_f32acc_batched(A0, B0, C0, 4, 4, 4, 8, 8, 4, 36, 32, 16, 2, 0)
-    assert b.gemm_status_string(st) == "GEMM_ERR_MISALIGNED"
+    # (a stride that is not a multiple of 8 elements is served by repacking:
+    # tests/test_gemm_gpu.py covers it on the GPU)
 
 
 def test_grouped_host_checks(b):
@@ -246,3 +243,12 @@ def test_split_tail_for_partial_last_waves(b):
     off = b.GemmOptions(0, 0, 0, 0, 0, 1, 0, 1)
     assert b.gemm_plan(8192, 8192, 8192, 1, off, SMS)["tail_split"] == 0
     assert b.gemm_plan(4096, 4096, 4096, 2, on, SMS)["tail_split"] == 0
+
+
+def test_noalloc_entry_rejects_what_it_cannot_repack(b):
+    # host-only: the layout check comes before any CUDA call
+    for args in ((A0 + 2, B0, C0, 4, 4, 4, 8, 8, 4), (A0, B0, C0, 4, 4, 4, 12, 8, 4),
+                 (A0, B0, C0, 4, 4, 4, 8, 8, 6)):
+        st = b.gemm_f16_f32acc_splitk_noalloc(*args, 0, 0)
+        assert b.gemm_status_string(st) == "GEMM_ERR_MISALIGNED", args
+        assert "cannot repack" in b.gemm_last_error_string()

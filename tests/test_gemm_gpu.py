@@ -321,9 +321,12 @@ def test_torch_convenience_wrapper(b):
     torch.cuda.synchronize()
     assert out.shape == (190, 210) and out.stride(0) % 4 == 0
     check_exact(out.cpu().numpy(), ref_of(A, B))
+    # row pitches of 30 and 14 elements: not TMA-addressable, served by repacking
+    A2, B2 = synthetic.operands(8, 14, 30, "int4", seed=11)
+    out = b.gemm(A2.cuda(), B2.cuda(), torch.empty((8, 14), dtype=torch.float32, device="cuda"))
+    check_exact(out.cpu().numpy(), ref_of(A2, B2))
     with pytest.raises(ValueError):
-        b.gemm(torch.zeros((8, 30), dtype=torch.float16, device="cuda"),
-               torch.zeros((30, 8), dtype=torch.float16, device="cuda"))
+        b.gemm(dA.t(), dB)  # a non-unit last stride
 
 
 def test_host_pipeline_results(b):

@@ -212,13 +212,11 @@ def gemm(A, B, out=None, *, split_k=0, tile_n=0, tile_m=0, timeout_ms=0, inject_
     for t, name in ((A, "A"), (B, "B"), (out, "out")):
         if t.numel() and t.stride(-1) != 1:
             raise ValueError(f"{name} must have a unit last stride")
-    for t, name, mult in ((A, "A", 8), (B, "B", 8), (out, "out", 4)):
-        if t.numel() and (t.data_ptr() % 16 or (t.dim() and t.shape[-2] > 1 and t.stride(-2) % mult)):
-            raise ValueError(f"{name} needs a 16-byte aligned base and a row stride that is a "
-                             f"multiple of {mult} elements (pad its rows)")
-    lda = A.stride(-2) if M > 1 else -(-max(K, 1) // 8) * 8
-    ldb = B.stride(-2) if K > 1 else -(-max(N, 1) // 8) * 8
-    ldc = out.stride(-2) if M > 1 else -(-max(N, 1) // 4) * 4
+    # Any row pitch works; pitches that are not multiples of 16 bytes (and
+    # unaligned bases) cost the library a repacking copy.
+    lda = A.stride(-2) if M > 1 else max(K, 1)
+    ldb = B.stride(-2) if K > 1 else max(N, 1)
+    ldc = out.stride(-2) if M > 1 else max(N, 1)
     sA = A.stride(0) if batched else 0
     sB = B.stride(0) if batched else 0
     sC = out.stride(0) if batched else 0
@@ -251,11 +249,9 @@ def grouped_gemm(A, B, group_rows, out=None, *, tile_n=0, tile_m=0, stream=None)
         out = torch.zeros((G, M, ldc_alloc), dtype=torch.float32, device=A.device)[..., :N]
     if out.dtype != torch.float32 or tuple(out.shape) != (G, M, N):
         raise ValueError("out must be a float32 G x M x N tensor")
-    for t, name, mult in ((A, "A", 8), (B, "B", 8), (out, "out", 4)):
-        if t.numel() and (t.stride(-1) != 1 or t.data_ptr() % 16 or t.stride(-2) % mult
-                          or t.stride(0) % mult):
-            raise ValueError(f"{name} needs a unit last stride, a 16-byte aligned base and row "
-                             f"and group strides that are multiples of {mult} elements")
+    for t, name in ((A, "A"), (B, "B"), (out, "out")):
+        if t.numel() and t.stride(-1) != 1:
+            raise ValueError(f"{name} must have a unit last stride")
     rows = group_rows.contiguous()
     opts = _opts(0, tile_n, 0, 0, tile_m)
     st = gemm_f16_f32acc_grouped_opts(A.data_ptr(), B.data_ptr(), out.data_ptr(), rows.data_ptr(),

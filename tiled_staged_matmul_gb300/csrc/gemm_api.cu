@@ -214,19 +214,12 @@ gemm_status_t check_host(const Problem &pr, bool *trivial)
     }
     if (pr.batch > 1 && (pr.sC <= 0 || (pr.K > 0 && (pr.sA <= 0 || pr.sB <= 0))))
         return fail(GEMM_ERR_INVALID_VALUE, "batch strides must be positive when batch > 1");
-    // 16-byte rules of the tensor-memory accelerator: base address and every
-    // row / batch pitch.
-    if ((reinterpret_cast<uintptr_t>(pr.C) & 15u) || (pr.ldc % 4) || (pr.batch > 1 && pr.sC % 4))
-        return fail(GEMM_ERR_MISALIGNED,
-                    "C must be 16-byte aligned with ldc and strideC multiples of 4 elements");
-    if (pr.K > 0) {
-        if ((reinterpret_cast<uintptr_t>(pr.A) & 15u) || (pr.lda % 8) || (pr.batch > 1 && pr.sA % 8))
-            return fail(GEMM_ERR_MISALIGNED,
-                        "A must be 16-byte aligned with lda and strideA multiples of 8 elements");
-        if ((reinterpret_cast<uintptr_t>(pr.B) & 15u) || (pr.ldb % 8) || (pr.batch > 1 && pr.sB % 8))
-            return fail(GEMM_ERR_MISALIGNED,
-                        "B must be 16-byte aligned with ldb and strideB multiples of 8 elements");
-    }
+    // Every element at its natural alignment (any pitch is fine: an operand
+    // the TMA cannot address is repacked, see run_repacked).
+    if (reinterpret_cast<uintptr_t>(pr.C) & 3u)
+        return fail(GEMM_ERR_MISALIGNED, "C must be 4-byte aligned (f32 elements)");
+    if (pr.K > 0 && ((reinterpret_cast<uintptr_t>(pr.A) & 1u) || (reinterpret_cast<uintptr_t>(pr.B) & 1u)))
+        return fail(GEMM_ERR_MISALIGNED, "A and B must be 2-byte aligned (f16 elements)");
     if (pr.batch > 1 && pr.sC < (pr.M - 1) * pr.ldc + pr.N)
         return fail(GEMM_ERR_ALIAS, "batches of C overlap (strideC too small)");
     const int64_t bytesC = span_bytes(pr.batch, pr.sC, pr.M, pr.ldc, pr.N, 4);
@@ -237,6 +230,26 @@ gemm_status_t check_host(const Problem &pr, bool *trivial)
             return fail(GEMM_ERR_ALIAS, "C overlaps A or B");
     }
     return GEMM_OK;
+}
+
+// What the tensor-memory accelerator can address: a 16-byte aligned base and
+// row / batch pitches that are multiples of 16 bytes ("Intel XPU Backend for
+// Triton", section "Use Tensor Descriptors to load tl.dot arguments and save
+// results": a descriptor wants its last stride 1 and the others aligned).
+struct TmaLayout {
+    bool a, b, c;
+    bool all() const { return a && b && c; }
+};
+
+TmaLayout tma_layout(const Problem &pr)
+{
+    TmaLayout t;
+    t.c = !((reinterpret_cast<uintptr_t>(pr.C) & 15u) || (pr.ldc % 4) || (pr.batch > 1 && pr.sC % 4));
+    t.a = pr.K == 0 ||
+          !((reinterpret_cast<uintptr_t>(pr.A) & 15u) || (pr.lda % 8) || (pr.batch > 1 && pr.sA % 8));
+    t.b = pr.K == 0 ||
+          !((reinterpret_cast<uintptr_t>(pr.B) & 15u) || (pr.ldb % 8) || (pr.batch > 1 && pr.sB % 8));
+    return t;
 }
 
 // The pointer is device memory of `dev` and its allocation covers `bytes`.
@@ -474,6 +487,67 @@ int64_t timeout_ns_for(const gemm_options_t *o, const gemm_plan_info_t &pl)
     return base_ms * 1000000ll + kb_per_unit * 10000ll;
 }
 
+gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t stream);
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+// An operand the TMA cannot address (TmaLayout) goes through a packed,
+// aligned copy in the pool: A and B are copied in before the GEMM, C is
+// computed there and copied out after it -- in a grouped call only the rows
+// below each count, so the others stay untouched.  The GEMM between is the
+// normal path, so the result is the one the aligned call would give.
+gemm_status_t run_repacked(const Problem &pr, const gemm_options_t *o, cudaStream_t stream,
+                           DeviceState *ds, const TmaLayout &tl)
+{
+    const int32_t M = int32_t(pr.M), N = int32_t(pr.N), K = int32_t(pr.K), batch = int32_t(pr.batch);
+    const int64_t lda2 = round_up(pr.K, 8), ldb2 = round_up(pr.N, 8), ldc2 = round_up(pr.N, 4);
+    const int64_t bytesA = tl.a ? 0 : round_up(pr.batch * pr.M * lda2 * 2, 256);
+    const int64_t bytesB = tl.b ? 0 : round_up(pr.batch * pr.K * ldb2 * 2, 256);
+    const int64_t bytesC = tl.c ? 0 : round_up(pr.batch * pr.M * ldc2 * 4, 256);
+    void *scratch = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&scratch, size_t(bytesA + bytesB + bytesC), ds->pool, stream);
+    if (e != cudaSuccess)
+        return fail_cuda(e, "scratch for repacked operands");
+    char *p = static_cast<char *>(scratch);
+    const int64_t sA = pr.batch > 1 ? pr.sA : 0, sB = pr.batch > 1 ? pr.sB : 0;
+    const int64_t sC = pr.batch > 1 ? pr.sC : 0;
+    Problem q = pr;
+    gemm_status_t st = GEMM_OK;
+    if (!tl.a) {
+        uint16_t *A2 = reinterpret_cast<uint16_t *>(p);
+        q.A = A2;
+        q.lda = lda2;
+        q.sA = pr.M * lda2;
+        if ((e = launch_pack_f16(pr.A, pr.lda, sA, A2, lda2, q.sA, M, K, batch, ds->sms, stream)) !=
+            cudaSuccess)
+            st = fail_cuda(e, "repacking A");
+    }
+    if (st == GEMM_OK && !tl.b) {
+        uint16_t *B2 = reinterpret_cast<uint16_t *>(p + bytesA);
+        q.B = B2;
+        q.ldb = ldb2;
+        q.sB = pr.K * ldb2;
+        if ((e = launch_pack_f16(pr.B, pr.ldb, sB, B2, ldb2, q.sB, K, N, batch, ds->sms, stream)) !=
+            cudaSuccess)
+            st = fail_cuda(e, "repacking B");
+    }
+    if (!tl.c) {
+        q.C = reinterpret_cast<float *>(p + bytesA + bytesB);
+        q.ldc = ldc2;
+        q.sC = pr.M * ldc2;
+    }
+    if (st == GEMM_OK && !tma_layout(q).all())
+        st = fail(GEMM_ERR_INVALID_VALUE, "internal: a repacked operand is still misaligned");
+    if (st == GEMM_OK)
+        st = run(q, o, stream);
+    if (st == GEMM_OK && !tl.c &&
+        (e = launch_unpack_f32(q.C, ldc2, q.sC, pr.C, pr.ldc, sC, M, N, batch, pr.group_rows,
+                               ds->sms, stream)) != cudaSuccess)
+        st = fail_cuda(e, "copying C out of the repacked layout");
+    cudaFreeAsync(scratch, stream);
+    return st;
+}
+
 gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t stream)
 {
     bool trivial = false;
@@ -513,6 +587,9 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
         return st;
     if ((st = check_device_pointer(pr.B, span_bytes(pr.batch, pr.sB, pr.K, pr.ldb, pr.N, 2), dev, "B")) != GEMM_OK)
         return st;
+    const TmaLayout tl = tma_layout(pr);
+    if (!tl.all())
+        return run_repacked(pr, o, stream, ds, tl);
 
     // A grouped launch's units are known only on the device, so it takes no
     // split: every unit is a whole tile.
@@ -888,6 +965,11 @@ extern "C" gemm_status_t gemm_f16_f32acc_splitk_noalloc(const uint16_t *A, const
         return fail(GEMM_ERR_INVALID_VALUE, "split_k must be >= 0");
     if (K == 0)
         return fail(GEMM_ERR_INVALID_VALUE, "K == 0 is not served by the no-allocation entry point");
+    if (!tma_layout(pr).all())
+        return fail(GEMM_ERR_MISALIGNED,
+                    "the no-allocation entry point cannot repack: A and B need 16-byte aligned bases "
+                    "and lda, ldb multiples of 8 elements, C a 16-byte aligned base and ldc a "
+                    "multiple of 4");
 
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

@@ -110,6 +110,15 @@ cudaError_t launch_tcgen05_gemm(int tile_m, int tile_n, const CUtensorMap &map_a
 cudaError_t launch_splitk_reduce(const float *W, float *C, int32_t M, int32_t N, int32_t S,
                                  int32_t batch, int64_t ldw, int64_t ldc, int64_t strideC,
                                  int grid, cudaStream_t stream);
+// Repack A or B into a packed layout with 16-byte aligned rows, and copy a
+// result out of one (only the rows below each count when group_rows is set).
+cudaError_t launch_pack_f16(const uint16_t *src, int64_t s_ld, int64_t s_stride, uint16_t *dst,
+                            int64_t d_ld, int64_t d_stride, int32_t rows, int32_t cols,
+                            int32_t batch, int sms, cudaStream_t stream);
+cudaError_t launch_unpack_f32(const float *src, int64_t s_ld, int64_t s_stride, float *dst,
+                              int64_t d_ld, int64_t d_stride, int32_t rows, int32_t cols,
+                              int32_t batch, const int32_t *group_rows, int sms,
+                              cudaStream_t stream);
 cudaError_t launch_zero_fill(float *C, int32_t M, int32_t N, int32_t batch, int64_t ldc,
                              int64_t strideC, const int32_t *group_rows, int grid, cudaStream_t stream);
 cudaError_t device_status_word(uint32_t **ptr);

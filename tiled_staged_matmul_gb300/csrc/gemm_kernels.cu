@@ -871,6 +871,69 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// Repacking between a pitched layout the TMA cannot address and a packed
+// one whose rows start on 16-byte boundaries: the repack of an operand
+// before the GEMM (PACK: the destination is the packed side) and the
+// copy-out of a result computed in the packed layout (!PACK: the source is,
+// and with `group_rows` only the rows below each batch's count are written).
+// Each thread moves 16-byte chunks of a row: one vector access on the
+// packed side, element accesses (all of a chunk in flight at once) on the
+// other.  Grid: x walks groups of `rows_per_block` rows, y splits a row's
+// chunks into segments of `seg` chunks, z walks the batch.
+template <typename T, bool PACK>
+__global__ void __launch_bounds__(256)
+    tsm_repack_kernel(const T *__restrict__ src, int64_t s_ld, int64_t s_stride, T *__restrict__ dst,
+                      int64_t d_ld, int64_t d_stride, int32_t rows, int32_t cols, int32_t batch,
+                      int32_t tpr, int32_t seg, const int32_t *__restrict__ group_rows)
+{
+    constexpr int V = 16 / sizeof(T);  // elements per chunk
+    const int32_t chunks = (cols + V - 1) / V;
+    const int32_t rpb = 256 / tpr;
+    const int32_t my_r = int32_t(threadIdx.x) / tpr;
+    const int32_t my_c = int32_t(threadIdx.x) - my_r * tpr;
+    const int32_t c_begin = int32_t(blockIdx.y) * seg;
+    const int32_t c_end = min(chunks, c_begin + seg);
+    for (int32_t b = int32_t(blockIdx.z); b < batch; b += int32_t(gridDim.z)) {
+        const int32_t lim = group_rows ? min(max(group_rows[b], 0), rows) : rows;
+        for (int64_t r = int64_t(blockIdx.x) * rpb + my_r; r < lim; r += int64_t(gridDim.x) * rpb) {
+            const T *srow = src + int64_t(b) * s_stride + r * s_ld;
+            T *drow = dst + int64_t(b) * d_stride + r * d_ld;
+#pragma unroll 2
+            for (int32_t c = c_begin + my_c; c < c_end; c += tpr) {
+                const int32_t e0 = c * V;
+                T v[V];
+                if (PACK) {
+                    if (e0 + V <= cols) {
+#pragma unroll
+                        for (int j = 0; j < V; ++j)
+                            v[j] = srow[e0 + j];
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < V; ++j)
+                            v[j] = e0 + j < cols ? srow[e0 + j] : T(0);
+                    }
+                    uint4 w;
+                    memcpy(&w, v, 16);
+                    *reinterpret_cast<uint4 *>(drow + e0) = w;
+                } else {
+                    const uint4 w = *reinterpret_cast<const uint4 *>(srow + e0);
+                    memcpy(v, &w, 16);
+                    if (e0 + V <= cols) {
+#pragma unroll
+                        for (int j = 0; j < V; ++j)
+                            drow[e0 + j] = v[j];
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < V; ++j)
+                            if (e0 + j < cols)
+                                drow[e0 + j] = v[j];
+                    }
+                }
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------------- host side
 
 template <int BN, bool PAIR>
@@ -976,6 +1039,56 @@ cudaError_t launch_zero_fill(float *C, int32_t M, int32_t N, int32_t batch, int6
 {
     tsm_zero_fill_kernel<<<grid, 256, 0, stream>>>(C, M, N, batch, ldc, strideC, group_rows);
     return cudaGetLastError();
+}
+
+namespace {
+
+// Launch shape of a repack: threads per row (a power of two up to 256, enough
+// for a row's chunks), chunks per thread per row segment at most 4, and
+// enough blocks over the rows to cover the GPU several times.
+template <typename T, bool PACK>
+cudaError_t launch_repack(const T *src, int64_t s_ld, int64_t s_stride, T *dst, int64_t d_ld,
+                          int64_t d_stride, int32_t rows, int32_t cols, int32_t batch,
+                          const int32_t *group_rows, int sms, cudaStream_t stream)
+{
+    constexpr int V = 16 / sizeof(T);
+    const int32_t chunks = (cols + V - 1) / V;
+    int32_t tpr = 1;
+    while (tpr < chunks && tpr < 256)
+        tpr *= 2;
+    // a segment is a multiple of tpr chunks, at least 4 per thread, and
+    // long enough that the segments of a row fit grid.y (65535)
+    const int64_t min_seg = (int64_t(chunks) + 65534) / 65535;
+    const int32_t seg = int32_t(std::max<int64_t>(int64_t(tpr) * 4, (min_seg + tpr - 1) / tpr * tpr));
+    const int32_t rpb = 256 / tpr;
+    const int64_t gy = (chunks + int64_t(seg) - 1) / seg;
+    const int64_t gz = std::min<int64_t>(batch, 65535);
+    const int64_t want = int64_t(sms) * 32;  // blocks in flight over the whole grid
+    const int64_t gx = std::max<int64_t>(
+        1, std::min<int64_t>((rows + rpb - 1) / rpb, (want + gy * gz - 1) / (gy * gz)));
+    tsm_repack_kernel<T, PACK><<<dim3(unsigned(gx), unsigned(gy), unsigned(gz)), 256, 0, stream>>>(
+        src, s_ld, s_stride, dst, d_ld, d_stride, rows, cols, batch, tpr, seg, group_rows);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_pack_f16(const uint16_t *src, int64_t s_ld, int64_t s_stride, uint16_t *dst,
+                            int64_t d_ld, int64_t d_stride, int32_t rows, int32_t cols,
+                            int32_t batch, int sms, cudaStream_t stream)
+{
+    return launch_repack<uint16_t, true>(src, s_ld, s_stride, dst, d_ld, d_stride, rows, cols, batch,
+                                         nullptr, sms, stream);
+}
+
+cudaError_t launch_unpack_f32(const float *src, int64_t s_ld, int64_t s_stride, float *dst,
+                              int64_t d_ld, int64_t d_stride, int32_t rows, int32_t cols,
+                              int32_t batch, const int32_t *group_rows, int sms,
+                              cudaStream_t stream)
+{
+    return launch_repack<uint32_t, false>(reinterpret_cast<const uint32_t *>(src), s_ld, s_stride,
+                                          reinterpret_cast<uint32_t *>(dst), d_ld, d_stride, rows,
+                                          cols, batch, group_rows, sms, stream);
 }
 
 cudaError_t device_status_word(uint32_t **ptr)
