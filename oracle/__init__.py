@@ -18,6 +18,7 @@ Two independent implementations live here:
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 import subprocess
 from fractions import Fraction
@@ -196,3 +197,90 @@ def grouped_gemm_f64(A, B, group_rows, E: int, M: int, N: int, K: int, C=None,
             continue
         out[e, :m, :] = gemm_f64(a[e, :m, :], b[e], m, N, K, nthreads=nthreads)
     return out
+
+
+# ------------------------------------------------------------------ fused epilogue
+
+ACTIVATIONS = ("none", "relu", "leaky_relu", "gelu", "gelu_tanh", "silu")
+OUT_TYPES = ("f32", "f16", "bf16")
+
+
+def activation_f64(x: np.ndarray, name: str, slope: float = 0.01) -> np.ndarray:
+    """The activations a fused epilogue may apply, in fp64, each written from
+    its mathematical definition (the pages name an ``ACTIVATION`` meta-
+    parameter of the GEMM kernel -- "Intel XPU Backend for Triton", section
+    "Use Proper Type Annotations" -- without fixing the set):
+
+    * relu(x)        = x for x > 0, else 0
+    * leaky_relu(x)  = x for x > 0, else slope * x
+    * gelu(x)        = x * Phi(x) = x/2 * (1 + erf(x / sqrt 2))
+    * gelu_tanh(x)   = x/2 * (1 + tanh(sqrt(2/pi) * (x + 0.044715 x^3)))
+    * silu(x)        = x * sigma(x) = x / (1 + exp(-x))"""
+    x = np.asarray(x, dtype=np.float64)
+    if name == "none":
+        return x.copy()
+    if name == "relu":
+        return np.where(x > 0, x, 0.0)
+    if name == "leaky_relu":
+        return np.where(x > 0, x, slope * x)
+    if name == "gelu":
+        erf = np.vectorize(math.erf, otypes=[np.float64])
+        return 0.5 * x * (1.0 + erf(x / math.sqrt(2.0)))
+    if name == "gelu_tanh":
+        return 0.5 * x * (1.0 + np.tanh(math.sqrt(2.0 / math.pi) * (x + 0.044715 * x ** 3)))
+    if name == "silu":
+        with np.errstate(over="ignore"):
+            return x / (1.0 + np.exp(-x))
+    raise ValueError(f"unknown activation {name!r}")
+
+
+def round_to_bf16(x: np.ndarray) -> np.ndarray:
+    """fp64 values rounded once, to nearest with ties to even, to bfloat16
+    (8 significant bits, the exponent range of binary32; subnormal spacing
+    2^-133; overflow to infinity), returned as fp64."""
+    x = np.asarray(x, dtype=np.float64)
+    out = np.empty_like(x)
+    flat, res = x.reshape(-1), out.reshape(-1)
+    max_finite = (2.0 - 2.0 ** -7) * 2.0 ** 127
+    for i, v in enumerate(flat):
+        v = float(v)
+        if v == 0.0 or math.isnan(v) or math.isinf(v):
+            res[i] = v
+            continue
+        m, e = math.frexp(abs(v))           # abs(v) = m * 2^e, m in [0.5, 1)
+        q = max(e - 8, -133)                 # the quantum: 8 significant bits, or the subnormal step
+        scaled = Fraction(abs(v)) / Fraction(2) ** q
+        r = round(scaled)                    # Python rounds exact halves to even
+        y = float(r * Fraction(2) ** q)
+        if y > max_finite:
+            y = math.inf
+        res[i] = math.copysign(y, v)
+    return out
+
+
+def round_to_out(x: np.ndarray, out_type: str) -> np.ndarray:
+    """fp64 values as the output type stores them (returned as fp64): f32 and
+    f16 by numpy's conversion from fp64 (one rounding, to nearest even),
+    bf16 by ``round_to_bf16``."""
+    x = np.asarray(x, dtype=np.float64)
+    if out_type == "f32":
+        return x.astype(np.float32).astype(np.float64)
+    if out_type == "f16":
+        with np.errstate(over="ignore"):
+            return x.astype(np.float16).astype(np.float64)
+    if out_type == "bf16":
+        return round_to_bf16(x)
+    raise ValueError(f"unknown output type {out_type!r}")
+
+
+def epilogue_f64(acc: np.ndarray, alpha: float = 1.0, bias=None, activation: str = "none",
+                 slope: float = 0.01) -> np.ndarray:
+    """The fused epilogue before the output rounding, in fp64:
+    ``activation(alpha * acc + bias[j])`` with ``acc`` the fp64 GEMM result
+    (rows x N, or batch x rows x N) and ``bias`` a length-N vector (or one per
+    batch, batch x N), absent = 0."""
+    v = float(alpha) * np.asarray(acc, dtype=np.float64)
+    if bias is not None:
+        b = np.asarray(bias, dtype=np.float64)
+        v = v + (b[..., None, :] if v.ndim == 3 and b.ndim == 2 else b)
+    return activation_f64(v, activation, slope)
