@@ -222,6 +222,61 @@ gemm_status_t gemm_f16_f32acc_grouped_opts(const uint16_t *A, const uint16_t *B,
                                            int64_t strideA, int64_t strideB, int64_t strideC,
                                            const gemm_options_t *opts, gemm_stream_t stream);
 
+/* Fused epilogue.  The pages' GEMM kernel takes an ACTIVATION meta-parameter
+ * ("Intel XPU Backend for Triton", section "Use Proper Type Annotations")
+ * without fixing the set; these are the activations offered, each applied in
+ * f32 to alpha * (A.B)[i][j] + bias[j] before the value is rounded (to
+ * nearest even) to the output type and stored. */
+typedef enum gemm_activation {
+    GEMM_ACT_NONE = 0,
+    GEMM_ACT_RELU = 1,        /* x > 0 ? x : 0 */
+    GEMM_ACT_LEAKY_RELU = 2,  /* x > 0 ? x : slope * x */
+    GEMM_ACT_GELU = 3,        /* x/2 * (1 + erf(x / sqrt 2)) */
+    GEMM_ACT_GELU_TANH = 4,   /* x/2 * (1 + tanh(sqrt(2/pi) * (x + 0.044715 x^3))) */
+    GEMM_ACT_SILU = 5         /* x / (1 + exp(-x)) */
+} gemm_activation_t;
+
+typedef enum gemm_out_type {
+    GEMM_OUT_F32 = 0,
+    GEMM_OUT_F16 = 1,   /* IEEE binary16 */
+    GEMM_OUT_BF16 = 2   /* bfloat16: the upper half of a binary32 */
+} gemm_out_type_t;
+
+typedef struct gemm_epilogue {
+    float alpha;          /* scale of A.B (1: none) */
+    const float *bias;    /* device, N f32 values per matrix (bias_stride apart), or NULL; 4-byte
+                             aligned; must not overlap C */
+    int64_t bias_stride;  /* elements between the bias vectors of consecutive batches or groups;
+                             0: one vector for all */
+    int32_t activation;   /* gemm_activation_t */
+    float slope;          /* GEMM_ACT_LEAKY_RELU: the slope for x <= 0 */
+    int32_t out_type;     /* gemm_out_type_t: the element type of C; ldc and strideC count
+                             these elements, and C must sit at their natural alignment */
+} gemm_epilogue_t;
+
+/* C = act(alpha * A.B + bias), stored as epi->out_type: the batched call with
+ * a fused epilogue (NULL epi: the plain f32 GEMM).  Everything else --
+ * layouts, repacking, split-K (the split partials stay f32, the epilogue is
+ * applied to their sum), errors -- is as gemm_f16_f32acc_opts.  K == 0 gives
+ * act(bias[j]) in every cell (the epilogue of the empty sum). */
+gemm_status_t gemm_f16_fused(const uint16_t *A, const uint16_t *B, void *C,
+                             int64_t M, int64_t N, int64_t K,
+                             int64_t lda, int64_t ldb, int64_t ldc,
+                             int64_t strideA, int64_t strideB, int64_t strideC,
+                             int64_t batch, const gemm_epilogue_t *epi,
+                             const gemm_options_t *opts, gemm_stream_t stream);
+
+/* The grouped (Mixture-of-Experts) call with a fused epilogue: rows below
+ * each group's count get act(alpha * A.B + bias), bias_stride apart per group;
+ * the other rows stay untouched.  Otherwise as gemm_f16_f32acc_grouped_opts. */
+gemm_status_t gemm_f16_grouped_fused(const uint16_t *A, const uint16_t *B, void *C,
+                                     const int32_t *group_rows, int64_t groups,
+                                     int64_t M, int64_t N, int64_t K,
+                                     int64_t lda, int64_t ldb, int64_t ldc,
+                                     int64_t strideA, int64_t strideB, int64_t strideC,
+                                     const gemm_epilogue_t *epi, const gemm_options_t *opts,
+                                     gemm_stream_t stream);
+
 /* The plan the library would use, computed on the host only (no GPU is
  * touched).  num_sms is the SM count to plan for (0 = the current device's).
  * This is the analogue of the pages' footprint check and K_TILE choice

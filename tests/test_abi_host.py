@@ -252,3 +252,22 @@ def test_noalloc_entry_rejects_what_it_cannot_repack(b):
         st = b.gemm_f16_f32acc_splitk_noalloc(*args, 0, 0)
         assert b.gemm_status_string(st) == "GEMM_ERR_MISALIGNED", args
         assert "cannot repack" in b.gemm_last_error_string()
+
+
+def test_epilogue_host_checks(b):
+    args = (A0, B0, C0, 4, 4, 4, 8, 8, 8, 0, 0, 0, 1)
+    bad_act = b.epilogue(activation=9)
+    assert b.gemm_status_string(b.gemm_f16_fused(*args, bad_act, None, 0)) == "GEMM_ERR_INVALID_VALUE"
+    bad_out = b.epilogue(out_type=7)
+    assert b.gemm_status_string(b.gemm_f16_fused(*args, bad_out, None, 0)) == "GEMM_ERR_INVALID_VALUE"
+    # a 16-bit C at an odd address, a misaligned bias, a bias overlapping C
+    st = b.gemm_f16_fused(A0, B0, C0 + 1, 4, 4, 4, 8, 8, 8, 0, 0, 0, 1, b.epilogue(out_type="bf16"),
+                          None, 0)
+    assert b.gemm_status_string(st) == "GEMM_ERR_MISALIGNED"
+    st = b.gemm_f16_fused(*args, b.epilogue(bias=C0 + 0x1000002), None, 0)
+    assert b.gemm_status_string(st) == "GEMM_ERR_MISALIGNED"
+    st = b.gemm_f16_fused(*args, b.epilogue(bias=C0 + 8), None, 0)
+    assert b.gemm_status_string(st) == "GEMM_ERR_ALIAS"
+    # nothing to do
+    assert b.gemm_f16_fused(A0, B0, C0, 0, 4, 4, 8, 8, 8, 0, 0, 0, 1, b.epilogue(activation="gelu"),
+                            None, 0) == b.GEMM_OK

@@ -34,6 +34,25 @@ class GemmOptions(ctypes.Structure):
                 ("trace", ctypes.c_void_p)]
 
 
+ACTIVATIONS = {"none": 0, "relu": 1, "leaky_relu": 2, "gelu": 3, "gelu_tanh": 4, "silu": 5}
+OUT_TYPES = {"f32": 0, "f16": 1, "bf16": 2}
+
+
+class GemmEpilogue(ctypes.Structure):
+    _fields_ = [("alpha", ctypes.c_float), ("bias", ctypes.c_void_p),
+                ("bias_stride", ctypes.c_int64), ("activation", ctypes.c_int32),
+                ("slope", ctypes.c_float), ("out_type", ctypes.c_int32)]
+
+
+def epilogue(alpha=1.0, bias=0, bias_stride=0, activation="none", slope=0.01, out_type="f32"):
+    """A ``GemmEpilogue``: ``activation`` and ``out_type`` by name or number,
+    ``bias`` a device pointer (0 = none)."""
+    act = ACTIVATIONS.get(activation, activation)
+    out = OUT_TYPES.get(out_type, out_type)
+    return GemmEpilogue(float(alpha), int(bias) or None, int(bias_stride), int(act), float(slope),
+                        int(out))
+
+
 class GemmPlanInfo(ctypes.Structure):
     _fields_ = [("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32),
                 ("tile_k", ctypes.c_int32), ("stages", ctypes.c_int32),
@@ -88,6 +107,13 @@ def _load() -> ctypes.CDLL:
     lib.gemm_f16_f32acc_grouped_opts.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64,
                                                  i64, i64, i64, i64, ctypes.POINTER(GemmOptions),
                                                  vp]
+    lib.gemm_f16_fused.restype = ctypes.c_int
+    lib.gemm_f16_fused.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, i64, i64, i64,
+                                   ctypes.POINTER(GemmEpilogue), ctypes.POINTER(GemmOptions), vp]
+    lib.gemm_f16_grouped_fused.restype = ctypes.c_int
+    lib.gemm_f16_grouped_fused.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, i64,
+                                           i64, i64, ctypes.POINTER(GemmEpilogue),
+                                           ctypes.POINTER(GemmOptions), vp]
     lib.gemm_f16_f32acc_splitk_noalloc.restype = ctypes.c_int
     lib.gemm_f16_f32acc_splitk_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64,
                                                    i32, vp]
@@ -133,6 +159,24 @@ def gemm_f16_f32acc_grouped_opts(A, B, C, group_rows, groups, M, N, K, lda, ldb,
     p = ctypes.byref(opts) if opts is not None else None
     return _lib.gemm_f16_f32acc_grouped_opts(A, B, C, group_rows, groups, M, N, K, lda, ldb, ldc,
                                              strideA, strideB, strideC, p, stream)
+
+
+def gemm_f16_fused(A, B, C, M, N, K, lda, ldb, ldc, strideA, strideB, strideC, batch,
+                   epi: GemmEpilogue | None = None, opts: GemmOptions | None = None,
+                   stream=0) -> int:
+    e = ctypes.byref(epi) if epi is not None else None
+    o = ctypes.byref(opts) if opts is not None else None
+    return _lib.gemm_f16_fused(A, B, C, M, N, K, lda, ldb, ldc, strideA, strideB, strideC, batch,
+                               e, o, stream)
+
+
+def gemm_f16_grouped_fused(A, B, C, group_rows, groups, M, N, K, lda, ldb, ldc, strideA, strideB,
+                           strideC, epi: GemmEpilogue | None = None,
+                           opts: GemmOptions | None = None, stream=0) -> int:
+    e = ctypes.byref(epi) if epi is not None else None
+    o = ctypes.byref(opts) if opts is not None else None
+    return _lib.gemm_f16_grouped_fused(A, B, C, group_rows, groups, M, N, K, lda, ldb, ldc, strideA,
+                                       strideB, strideC, e, o, stream)
 
 
 def gemm_f16_f32acc_splitk_noalloc(A, B, C, M, N, K, lda, ldb, ldc, split_k=0, stream=0) -> int:
@@ -182,12 +226,15 @@ def _stream_handle(stream):
     return stream.cuda_stream
 
 
-def gemm(A, B, out=None, *, split_k=0, tile_n=0, tile_m=0, timeout_ms=0, inject_stall=0,
-         stream=None):
-    """``out = A @ B`` for f16 CUDA tensors A (M x K) and B (K x N), f32 out.
+def gemm(A, B, out=None, *, alpha=1.0, bias=None, activation="none", slope=0.01, out_dtype=None,
+         split_k=0, tile_n=0, tile_m=0, timeout_ms=0, inject_stall=0, stream=None):
+    """``out = activation(alpha * (A @ B) + bias)`` for f16 CUDA tensors A
+    (M x K) and B (K x N); ``out`` is f32 unless ``out_dtype`` (or the given
+    ``out``) says torch.float16 / torch.bfloat16.
 
-    3-D tensors (batch x M x K, batch x K x N) run as one batched call.  Rows
-    may be padded (``stride(-2) >= size(-1)``) but the last stride must be 1.
+    3-D tensors (batch x M x K, batch x K x N) run as one batched call;
+    ``bias`` is an f32 CUDA tensor of N values (or batch x N).  Rows may be
+    padded (``stride(-2) >= size(-1)``) but the last stride must be 1.
     Returns ``out`` (allocated with ``torch.empty`` when not given)."""
     import torch
     if A.dtype != torch.float16 or B.dtype != torch.float16:
@@ -202,13 +249,16 @@ def gemm(A, B, out=None, *, split_k=0, tile_n=0, tile_m=0, timeout_ms=0, inject_
     batch = A.shape[0] if batched else 1
     if batched and B.shape[0] != batch:
         raise ValueError("batch sizes differ")
+    dtype = out.dtype if out is not None else (out_dtype or torch.float32)
+    out_names = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16"}
+    if dtype not in out_names:
+        raise TypeError("out must be torch.float32, torch.float16 or torch.bfloat16")
     if out is None:
         # rows padded to a 16-byte pitch (the TMA's rule); the view hides it
-        ldc_alloc = max(4, -(-N // 4) * 4)
+        per16 = 16 // torch.tensor([], dtype=dtype).element_size()
+        ldc_alloc = max(per16, -(-N // per16) * per16)
         shape = (batch, M, ldc_alloc) if batched else (M, ldc_alloc)
-        out = torch.empty(shape, dtype=torch.float32, device=A.device)[..., :N]
-    if out.dtype != torch.float32:
-        raise TypeError("out must be torch.float32")
+        out = torch.empty(shape, dtype=dtype, device=A.device)[..., :N]
     for t, name in ((A, "A"), (B, "B"), (out, "out")):
         if t.numel() and t.stride(-1) != 1:
             raise ValueError(f"{name} must have a unit last stride")
@@ -221,13 +271,22 @@ def gemm(A, B, out=None, *, split_k=0, tile_n=0, tile_m=0, timeout_ms=0, inject_
     sB = B.stride(0) if batched else 0
     sC = out.stride(0) if batched else 0
     opts = _opts(split_k, tile_n, timeout_ms, inject_stall, tile_m)
-    st = gemm_f16_f32acc_opts(A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K, lda, ldb,
-                              ldc, sA, sB, sC, batch, opts, _stream_handle(stream))
+    if bias is not None:
+        if bias.dtype != torch.float32 or not bias.is_cuda or bias.shape[-1] != N:
+            raise ValueError("bias must be a CUDA float32 tensor of N values (or batch x N)")
+        if bias.stride(-1) != 1:
+            raise ValueError("bias must have a unit last stride")
+    epi = epilogue(alpha, bias.data_ptr() if bias is not None else 0,
+                   bias.stride(0) if bias is not None and bias.dim() == 2 else 0,
+                   activation, slope, out_names[dtype])
+    st = gemm_f16_fused(A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K, lda, ldb, ldc, sA, sB,
+                        sC, batch, epi, opts, _stream_handle(stream))
     check(st)
     return out
 
 
-def grouped_gemm(A, B, group_rows, out=None, *, tile_n=0, tile_m=0, stream=None):
+def grouped_gemm(A, B, group_rows, out=None, *, alpha=1.0, bias=None, activation="none",
+                 slope=0.01, out_dtype=None, tile_n=0, tile_m=0, stream=None):
     """Grouped (Mixture-of-Experts) GEMM on CUDA tensors: for each group g,
     ``out[g, :group_rows[g]] = A[g, :group_rows[g]] @ B[g]``.
 
@@ -244,20 +303,31 @@ def grouped_gemm(A, B, group_rows, out=None, *, tile_n=0, tile_m=0, stream=None)
         raise ValueError("group_rows must be a CUDA int32 tensor of one count per group")
     G, M, K = A.shape
     N = B.shape[2]
+    dtype = out.dtype if out is not None else (out_dtype or torch.float32)
+    out_names = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16"}
+    if dtype not in out_names:
+        raise TypeError("out must be torch.float32, torch.float16 or torch.bfloat16")
     if out is None:
-        ldc_alloc = max(4, -(-N // 4) * 4)
-        out = torch.zeros((G, M, ldc_alloc), dtype=torch.float32, device=A.device)[..., :N]
-    if out.dtype != torch.float32 or tuple(out.shape) != (G, M, N):
-        raise ValueError("out must be a float32 G x M x N tensor")
+        per16 = 16 // torch.tensor([], dtype=dtype).element_size()
+        ldc_alloc = max(per16, -(-N // per16) * per16)
+        out = torch.zeros((G, M, ldc_alloc), dtype=dtype, device=A.device)[..., :N]
+    if tuple(out.shape) != (G, M, N):
+        raise ValueError("out must be a G x M x N tensor")
     for t, name in ((A, "A"), (B, "B"), (out, "out")):
         if t.numel() and t.stride(-1) != 1:
             raise ValueError(f"{name} must have a unit last stride")
     rows = group_rows.contiguous()
     opts = _opts(0, tile_n, 0, 0, tile_m)
-    st = gemm_f16_f32acc_grouped_opts(A.data_ptr(), B.data_ptr(), out.data_ptr(), rows.data_ptr(),
-                                      G, M, N, K, A.stride(1), B.stride(1), out.stride(1),
-                                      A.stride(0), B.stride(0), out.stride(0), opts,
-                                      _stream_handle(stream))
+    if bias is not None and (bias.dtype != torch.float32 or not bias.is_cuda
+                             or bias.shape[-1] != N or bias.stride(-1) != 1):
+        raise ValueError("bias must be a CUDA float32 tensor of N values (or groups x N)")
+    epi = epilogue(alpha, bias.data_ptr() if bias is not None else 0,
+                   bias.stride(0) if bias is not None and bias.dim() == 2 else 0,
+                   activation, slope, out_names[dtype])
+    st = gemm_f16_grouped_fused(A.data_ptr(), B.data_ptr(), out.data_ptr(), rows.data_ptr(),
+                                G, M, N, K, A.stride(1), B.stride(1), out.stride(1),
+                                A.stride(0), B.stride(0), out.stride(0), epi, opts,
+                                _stream_handle(stream))
     check(st)
     return out
 

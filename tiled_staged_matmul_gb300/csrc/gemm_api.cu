@@ -107,7 +107,7 @@ struct DeviceState {
     int sms = 0;
     int cc_major = 0, cc_minor = 0;
     int smem_optin = 0;
-    bool attrs_set[5] = {false, false, false, false, false};  // see config_index
+    bool attrs_set[10] = {};  // see config_index; +5 for the kernels with the fused epilogue
     cudaMemPool_t pool = nullptr;
     uint32_t *status = nullptr;
 };
@@ -162,11 +162,13 @@ int config_index(int tile_m, int tile_n)
 struct Problem {
     const uint16_t *A;
     const uint16_t *B;
-    float *C;
+    void *C;  // epi.out_type elements
     int64_t M, N, K, lda, ldb, ldc, sA, sB, sC, batch;
     // Grouped launch (at most kMaxGroupsPerLaunch groups = batches): device
     // array of each group's row count; null for plain and batched GEMMs.
     const int32_t *group_rows = nullptr;
+    // What the kernels do to each output value before storing it.
+    Epilogue epi;
 };
 
 // Bytes spanned by `batch` matrices of `rows` x `cols` elements of `elem`
@@ -216,13 +218,23 @@ gemm_status_t check_host(const Problem &pr, bool *trivial)
         return fail(GEMM_ERR_INVALID_VALUE, "batch strides must be positive when batch > 1");
     // Every element at its natural alignment (any pitch is fine: an operand
     // the TMA cannot address is repacked, see run_repacked).
-    if (reinterpret_cast<uintptr_t>(pr.C) & 3u)
-        return fail(GEMM_ERR_MISALIGNED, "C must be 4-byte aligned (f32 elements)");
+    const int eb = pr.epi.out_bytes();
+    if (reinterpret_cast<uintptr_t>(pr.C) & uintptr_t(eb - 1))
+        return fail(GEMM_ERR_MISALIGNED, "C must be %d-byte aligned (its elements)", eb);
     if (pr.K > 0 && ((reinterpret_cast<uintptr_t>(pr.A) & 1u) || (reinterpret_cast<uintptr_t>(pr.B) & 1u)))
         return fail(GEMM_ERR_MISALIGNED, "A and B must be 2-byte aligned (f16 elements)");
     if (pr.batch > 1 && pr.sC < (pr.M - 1) * pr.ldc + pr.N)
         return fail(GEMM_ERR_ALIAS, "batches of C overlap (strideC too small)");
-    const int64_t bytesC = span_bytes(pr.batch, pr.sC, pr.M, pr.ldc, pr.N, 4);
+    const int64_t bytesC = span_bytes(pr.batch, pr.sC, pr.M, pr.ldc, pr.N, eb);
+    if (pr.epi.bias) {
+        if (reinterpret_cast<uintptr_t>(pr.epi.bias) & 3u)
+            return fail(GEMM_ERR_MISALIGNED, "bias must be 4-byte aligned (f32)");
+        if (pr.epi.bias_stride < 0)
+            return fail(GEMM_ERR_INVALID_VALUE, "bias_stride must be >= 0");
+        const int64_t bytesBias = span_bytes(pr.batch, pr.epi.bias_stride, 1, pr.N, pr.N, 4);
+        if (overlaps(pr.C, bytesC, pr.epi.bias, bytesBias))
+            return fail(GEMM_ERR_ALIAS, "C overlaps the bias");
+    }
     if (pr.K > 0) {
         const int64_t bytesA = span_bytes(pr.batch, pr.sA, pr.M, pr.lda, pr.K, 2);
         const int64_t bytesB = span_bytes(pr.batch, pr.sB, pr.K, pr.ldb, pr.N, 2);
@@ -244,7 +256,9 @@ struct TmaLayout {
 TmaLayout tma_layout(const Problem &pr)
 {
     TmaLayout t;
-    t.c = !((reinterpret_cast<uintptr_t>(pr.C) & 15u) || (pr.ldc % 4) || (pr.batch > 1 && pr.sC % 4));
+    const int64_t per16 = 16 / pr.epi.out_bytes();  // C elements per 16 bytes
+    t.c = !((reinterpret_cast<uintptr_t>(pr.C) & 15u) || (pr.ldc % per16) ||
+            (pr.batch > 1 && pr.sC % per16));
     t.a = pr.K == 0 ||
           !((reinterpret_cast<uintptr_t>(pr.A) & 15u) || (pr.lda % 8) || (pr.batch > 1 && pr.sA % 8));
     t.b = pr.K == 0 ||
@@ -500,10 +514,11 @@ gemm_status_t run_repacked(const Problem &pr, const gemm_options_t *o, cudaStrea
                            DeviceState *ds, const TmaLayout &tl)
 {
     const int32_t M = int32_t(pr.M), N = int32_t(pr.N), K = int32_t(pr.K), batch = int32_t(pr.batch);
-    const int64_t lda2 = round_up(pr.K, 8), ldb2 = round_up(pr.N, 8), ldc2 = round_up(pr.N, 4);
+    const int eb = pr.epi.out_bytes();
+    const int64_t lda2 = round_up(pr.K, 8), ldb2 = round_up(pr.N, 8), ldc2 = round_up(pr.N, 16 / eb);
     const int64_t bytesA = tl.a ? 0 : round_up(pr.batch * pr.M * lda2 * 2, 256);
     const int64_t bytesB = tl.b ? 0 : round_up(pr.batch * pr.K * ldb2 * 2, 256);
-    const int64_t bytesC = tl.c ? 0 : round_up(pr.batch * pr.M * ldc2 * 4, 256);
+    const int64_t bytesC = tl.c ? 0 : round_up(pr.batch * pr.M * ldc2 * eb, 256);
     void *scratch = nullptr;
     cudaError_t e = cudaMallocFromPoolAsync(&scratch, size_t(bytesA + bytesB + bytesC), ds->pool, stream);
     if (e != cudaSuccess)
@@ -532,7 +547,7 @@ gemm_status_t run_repacked(const Problem &pr, const gemm_options_t *o, cudaStrea
             st = fail_cuda(e, "repacking B");
     }
     if (!tl.c) {
-        q.C = reinterpret_cast<float *>(p + bytesA + bytesB);
+        q.C = p + bytesA + bytesB;
         q.ldc = ldc2;
         q.sC = pr.M * ldc2;
     }
@@ -540,10 +555,16 @@ gemm_status_t run_repacked(const Problem &pr, const gemm_options_t *o, cudaStrea
         st = fail(GEMM_ERR_INVALID_VALUE, "internal: a repacked operand is still misaligned");
     if (st == GEMM_OK)
         st = run(q, o, stream);
-    if (st == GEMM_OK && !tl.c &&
-        (e = launch_unpack_f32(q.C, ldc2, q.sC, pr.C, pr.ldc, sC, M, N, batch, pr.group_rows,
-                               ds->sms, stream)) != cudaSuccess)
-        st = fail_cuda(e, "copying C out of the repacked layout");
+    if (st == GEMM_OK && !tl.c) {
+        e = eb == 4 ? launch_unpack_f32(static_cast<const float *>(q.C), ldc2, q.sC,
+                                        static_cast<float *>(pr.C), pr.ldc, sC, M, N, batch,
+                                        pr.group_rows, ds->sms, stream)
+                    : launch_unpack_u16(static_cast<const uint16_t *>(q.C), ldc2, q.sC,
+                                        static_cast<uint16_t *>(pr.C), pr.ldc, sC, M, N, batch,
+                                        pr.group_rows, ds->sms, stream);
+        if (e != cudaSuccess)
+            st = fail_cuda(e, "copying C out of the repacked layout");
+    }
     cudaFreeAsync(scratch, stream);
     return st;
 }
@@ -563,8 +584,14 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
     if ((st = device_state(dev, &ds)) != GEMM_OK)
         return st;
 
-    const int64_t bytesC = span_bytes(pr.batch, pr.sC, pr.M, pr.ldc, pr.N, 4);
+    const int eb = pr.epi.out_bytes();
+    const bool use_epi = !pr.epi.identity();
+    const int64_t bytesC = span_bytes(pr.batch, pr.sC, pr.M, pr.ldc, pr.N, eb);
     if ((st = check_device_pointer(pr.C, bytesC, dev, "C")) != GEMM_OK)
+        return st;
+    if (pr.epi.bias &&
+        (st = check_device_pointer(pr.epi.bias, span_bytes(pr.batch, pr.epi.bias_stride, 1, pr.N, pr.N, 4),
+                                   dev, "bias")) != GEMM_OK)
         return st;
     const int32_t M = int32_t(pr.M), N = int32_t(pr.N), batch = int32_t(pr.batch);
     const int64_t sC = pr.batch > 1 ? pr.sC : int64_t(pr.M) * pr.ldc;
@@ -578,7 +605,8 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
     if (pr.K == 0) {
         const int64_t total = int64_t(M) * N * batch;
         const int grid = int(std::min<int64_t>((total + 255) / 256, int64_t(ds->sms) * 8));
-        if ((e = launch_zero_fill(pr.C, M, N, batch, pr.ldc, sC, pr.group_rows, grid, stream)) != cudaSuccess)
+        if ((e = launch_zero_fill(pr.C, M, N, batch, pr.ldc, sC, pr.group_rows, pr.epi, grid,
+                                  stream)) != cudaSuccess)
             return fail_cuda(e, "zero-fill launch");
         return GEMM_OK;
     }
@@ -607,9 +635,9 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
     if (ds->smem_optin < pl.smem_bytes)
         return fail(GEMM_ERR_UNSUPPORTED_DEVICE, "device allows %d bytes of shared memory per block, the kernel needs %lld",
                     ds->smem_optin, (long long)pl.smem_bytes);
-    const int ti = config_index(pl.tile_m, pl.tile_n);
+    const int ti = config_index(pl.tile_m, pl.tile_n) + (use_epi ? 5 : 0);
     if (!ds->attrs_set[ti]) {
-        if ((e = set_kernel_attributes(pl.tile_m, pl.tile_n)) != cudaSuccess)
+        if ((e = set_kernel_attributes(pl.tile_m, pl.tile_n, use_epi)) != cudaSuccess)
             return fail_cuda(e, "cudaFuncSetAttribute(max dynamic shared memory)");
         ds->attrs_set[ti] = true;
     }
@@ -641,6 +669,22 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
     kp.trace = o ? reinterpret_cast<unsigned long long *>(o->trace) : nullptr;
     kp.group_rows = pr.group_rows;
     kp.groups = pr.group_rows ? batch : 0;
+    kp.epi = pr.epi;
+    // C's tensor map: f32 boxes of 32 x 32 with the 128-byte swizzle, or
+    // 16-bit boxes of 32 x 32 (64-byte rows) with the 64-byte swizzle.  A TMA
+    // store writes whole 16-byte granules of a row, so the map ends at the
+    // last multiple of 16 bytes and the rest of a row goes by plain stores.
+    const int64_t granule = 16 / eb;
+    auto encode_out = [&](CUtensorMap *m, int64_t cols) {
+        if (eb == 4)
+            return encode_3d(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pr.C, cols, pr.M, pr.batch, pr.ldc,
+                             sC, 32, 32, CU_TENSOR_MAP_L2_PROMOTION_NONE, "C");
+        return encode_3d(m,
+                         pr.epi.out_type == kOutBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                         2, pr.C, cols, pr.M, pr.batch, pr.ldc, sC, 32, 32,
+                         CU_TENSOR_MAP_L2_PROMOTION_NONE, "C", 1, CU_TENSOR_MAP_SWIZZLE_64B);
+    };
 
     kp.n_tma = N;
     kp.tail = 0;
@@ -654,15 +698,15 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
         // TMA stores write whole 16-byte granules: let the map end at the last
         // multiple of 4 columns and write the rest with plain stores, so that
         // C's row padding past N stays untouched.
-        if (N % 4) {
-            kp.n_tma = N & ~3;
+        if (N % granule) {
+            kp.n_tma = int32_t(N & ~(granule - 1));
             kp.tail = 1;
         }
         const int64_t map_cols = kp.n_tma > 0 ? kp.n_tma : pr.N;  // an unused map still needs extent
-        if ((st = encode_3d(&map_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pr.C, map_cols, pr.M, pr.batch,
-                            pr.ldc, sC, 32, 32, CU_TENSOR_MAP_L2_PROMOTION_NONE, "C")) != GEMM_OK)
+        if ((st = encode_out(&map_out, map_cols)) != GEMM_OK)
             return st;
-        if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, map_a, map_b, map_out, map_out, map_out, kp, pl.grid, stream)) != cudaSuccess)
+        if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, use_epi, map_a, map_b, map_out, map_out, map_out, kp,
+                                     pl.grid, stream)) != cudaSuccess)
             return fail_cuda(e, "GEMM kernel launch");
         return GEMM_OK;
     }
@@ -695,13 +739,12 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
         kp.timeout_ns = uint64_t(timeout_ns_for(o, pl));
         alignas(64) CUtensorMap map_ws, map_red;
         // C itself for the whole tiles (and as a valid map to prefetch).
-        if (N % 4) {
-            kp.n_tma = N & ~3;
+        if (N % granule) {
+            kp.n_tma = int32_t(N & ~(granule - 1));
             kp.tail = 1;
         }
         const int64_t map_cols = kp.n_tma > 0 ? kp.n_tma : pr.N;
-        st = encode_3d(&map_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pr.C, map_cols, pr.M, pr.batch,
-                       pr.ldc, sC, 32, 32, CU_TENSOR_MAP_L2_PROMOTION_NONE, "C");
+        st = encode_out(&map_out, map_cols);
         if (st == GEMM_OK)
             st = encode_3d(&map_ws, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ws, pl.tile_n, pl.tile_m,
                            split_units, pl.tile_n, tile_elems, 32, 32,
@@ -712,7 +755,7 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
                            uint32_t(kp.rows_per), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                            "split-K workspace (reduce)", uint32_t(S), CU_TENSOR_MAP_SWIZZLE_NONE);
         if (st == GEMM_OK &&
-            (e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, map_a, map_b, map_out, map_ws, map_red, kp,
+            (e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, use_epi, map_a, map_b, map_out, map_ws, map_red, kp,
                                      pl.grid, stream)) != cudaSuccess)
             st = fail_cuda(e, "GEMM kernel launch");
         cudaFreeAsync(ws, stream);
@@ -727,15 +770,25 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
     st = encode_3d(&map_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ws, pr.N, pr.M,
                    pr.batch * pl.split_k, ldw, int64_t(pr.M) * ldw, 32, 32,
                    CU_TENSOR_MAP_L2_PROMOTION_NONE, "split-K workspace");
+    // The GEMM writes raw partials (the plain kernel); the reduce applies
+    // the epilogue to the sums.
+    kp.epi = Epilogue{};
+    if (st == GEMM_OK && !ds->attrs_set[config_index(pl.tile_m, pl.tile_n)]) {
+        if ((e = set_kernel_attributes(pl.tile_m, pl.tile_n, false)) != cudaSuccess)
+            st = fail_cuda(e, "cudaFuncSetAttribute(max dynamic shared memory)");
+        else
+            ds->attrs_set[config_index(pl.tile_m, pl.tile_n)] = true;
+    }
     if (st == GEMM_OK) {
-        if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, map_a, map_b, map_out, map_out, map_out, kp, pl.grid, stream)) != cudaSuccess)
+        if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, false, map_a, map_b, map_out, map_out, map_out, kp,
+                                     pl.grid, stream)) != cudaSuccess)
             st = fail_cuda(e, "GEMM kernel launch");
     }
     if (st == GEMM_OK) {
         const int64_t threads = int64_t(M) * ((N + 3) / 4) * batch;
         const int grid = int(std::min<int64_t>((threads + 255) / 256, int64_t(ds->sms) * 8));
         if ((e = launch_splitk_reduce(static_cast<const float *>(ws), pr.C, M, N, pl.split_k, batch,
-                                      ldw, pr.ldc, sC, grid, stream)) != cudaSuccess)
+                                      ldw, pr.ldc, sC, pr.epi, grid, stream)) != cudaSuccess)
             st = fail_cuda(e, "split-K reduce launch");
     }
     cudaFreeAsync(ws, stream);
@@ -777,6 +830,63 @@ gemm_status_t gemm_f16_f32acc_opts(const uint16_t *A, const uint16_t *B, float *
     return run(pr, opts, reinterpret_cast<cudaStream_t>(stream));
 }
 
+}  // extern "C"
+
+namespace tsm {
+namespace {
+
+// The public epilogue description, checked, as the kernels' Epilogue.
+gemm_status_t epilogue_of(const gemm_epilogue_t *e, Epilogue *out)
+{
+    *out = Epilogue{};
+    if (!e)
+        return GEMM_OK;
+    if (e->activation < GEMM_ACT_NONE || e->activation > GEMM_ACT_SILU)
+        return fail(GEMM_ERR_INVALID_VALUE, "unknown activation %d", e->activation);
+    if (e->out_type < GEMM_OUT_F32 || e->out_type > GEMM_OUT_BF16)
+        return fail(GEMM_ERR_INVALID_VALUE, "unknown output type %d", e->out_type);
+    out->alpha = e->alpha;
+    out->bias = e->bias;
+    out->bias_stride = e->bias_stride;
+    out->act = e->activation;
+    out->slope = e->slope;
+    out->out_type = e->out_type;
+    return GEMM_OK;
+}
+
+// Grouped calls: launches of at most kMaxGroupsPerLaunch groups, in stream order.
+gemm_status_t grouped(const uint16_t *A, const uint16_t *B, void *C, const int32_t *group_rows,
+                      int64_t groups, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                      int64_t ldc, int64_t strideA, int64_t strideB, int64_t strideC,
+                      const Epilogue &epi, const gemm_options_t *opts, cudaStream_t stream)
+{
+    if (groups < 0)
+        return fail(GEMM_ERR_INVALID_VALUE, "negative number of groups: %lld", (long long)groups);
+    if (groups > 0 && !group_rows)
+        return fail(GEMM_ERR_INVALID_VALUE, "group_rows is NULL");
+    if (reinterpret_cast<uintptr_t>(group_rows) & 3u)
+        return fail(GEMM_ERR_MISALIGNED, "group_rows must be 4-byte aligned");
+    for (int64_t g0 = 0; g0 < groups; g0 += kMaxGroupsPerLaunch) {
+        const int64_t n = std::min<int64_t>(kMaxGroupsPerLaunch, groups - g0);
+        Problem pr{A ? A + g0 * strideA : A, B ? B + g0 * strideB : B,
+                   C ? static_cast<char *>(C) + g0 * strideC * epi.out_bytes() : C,
+                   M, N, K, lda, ldb, ldc, strideA, strideB, strideC, n};
+        pr.group_rows = group_rows + g0;
+        pr.epi = epi;
+        if (epi.bias)
+            pr.epi.bias = epi.bias + g0 * epi.bias_stride;
+        const gemm_status_t st = run(pr, opts, stream);
+        if (st != GEMM_OK)
+            return st;
+    }
+    return GEMM_OK;
+}
+
+}  // namespace
+}  // namespace tsm
+
+extern "C" {
+
 gemm_status_t gemm_f16_f32acc_grouped_opts(const uint16_t *A, const uint16_t *B, float *C,
                                            const int32_t *group_rows, int64_t groups, int64_t M,
                                            int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
@@ -784,23 +894,8 @@ gemm_status_t gemm_f16_f32acc_grouped_opts(const uint16_t *A, const uint16_t *B,
                                            const gemm_options_t *opts, gemm_stream_t stream)
 {
     g_last_error.clear();
-    if (groups < 0)
-        return fail(GEMM_ERR_INVALID_VALUE, "negative number of groups: %lld", (long long)groups);
-    if (groups > 0 && !group_rows)
-        return fail(GEMM_ERR_INVALID_VALUE, "group_rows is NULL");
-    if (reinterpret_cast<uintptr_t>(group_rows) & 3u)
-        return fail(GEMM_ERR_MISALIGNED, "group_rows must be 4-byte aligned");
-    // Launches of at most kMaxGroupsPerLaunch groups each, in stream order.
-    for (int64_t g0 = 0; g0 < groups; g0 += kMaxGroupsPerLaunch) {
-        const int64_t n = std::min<int64_t>(kMaxGroupsPerLaunch, groups - g0);
-        Problem pr{A ? A + g0 * strideA : A, B ? B + g0 * strideB : B, C ? C + g0 * strideC : C,
-                   M, N, K, lda, ldb, ldc, strideA, strideB, strideC, n};
-        pr.group_rows = group_rows + g0;
-        const gemm_status_t st = run(pr, opts, reinterpret_cast<cudaStream_t>(stream));
-        if (st != GEMM_OK)
-            return st;
-    }
-    return GEMM_OK;
+    return grouped(A, B, C, group_rows, groups, M, N, K, lda, ldb, ldc, strideA, strideB, strideC,
+                   Epilogue{}, opts, reinterpret_cast<cudaStream_t>(stream));
 }
 
 gemm_status_t gemm_f16_f32acc_grouped(const uint16_t *A, const uint16_t *B, float *C,
@@ -810,6 +905,36 @@ gemm_status_t gemm_f16_f32acc_grouped(const uint16_t *A, const uint16_t *B, floa
 {
     return gemm_f16_f32acc_grouped_opts(A, B, C, group_rows, groups, M, N, K, lda, ldb, ldc, strideA,
                                         strideB, strideC, nullptr, stream);
+}
+
+gemm_status_t gemm_f16_fused(const uint16_t *A, const uint16_t *B, void *C, int64_t M, int64_t N,
+                             int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int64_t strideA,
+                             int64_t strideB, int64_t strideC, int64_t batch,
+                             const gemm_epilogue_t *epi, const gemm_options_t *opts,
+                             gemm_stream_t stream)
+{
+    g_last_error.clear();
+    Problem pr{A, B, C, M, N, K, lda, ldb, ldc, strideA, strideB, strideC, batch};
+    const gemm_status_t st = epilogue_of(epi, &pr.epi);
+    if (st != GEMM_OK)
+        return st;
+    return run(pr, opts, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_f16_grouped_fused(const uint16_t *A, const uint16_t *B, void *C,
+                                     const int32_t *group_rows, int64_t groups, int64_t M, int64_t N,
+                                     int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                                     int64_t strideA, int64_t strideB, int64_t strideC,
+                                     const gemm_epilogue_t *epi, const gemm_options_t *opts,
+                                     gemm_stream_t stream)
+{
+    g_last_error.clear();
+    Epilogue e;
+    const gemm_status_t st = epilogue_of(epi, &e);
+    if (st != GEMM_OK)
+        return st;
+    return grouped(A, B, C, group_rows, groups, M, N, K, lda, ldb, ldc, strideA, strideB, strideC, e,
+                   opts, reinterpret_cast<cudaStream_t>(stream));
 }
 
 gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const gemm_options_t *opts,
@@ -1009,7 +1134,7 @@ extern "C" gemm_status_t gemm_f16_f32acc_splitk_noalloc(const uint16_t *A, const
                     nd->smem_optin, (long long)pl.smem_bytes);
     const int ti = config_index(pl.tile_m, pl.tile_n);
     if (!nd->attrs_set[ti]) {
-        if ((e = set_kernel_attributes(pl.tile_m, pl.tile_n)) != cudaSuccess)
+        if ((e = set_kernel_attributes(pl.tile_m, pl.tile_n, false)) != cudaSuccess)
             return fail_cuda(e, "cudaFuncSetAttribute(max dynamic shared memory)");
         nd->attrs_set[ti] = true;
     }
@@ -1052,7 +1177,7 @@ extern "C" gemm_status_t gemm_f16_f32acc_splitk_noalloc(const uint16_t *A, const
         if ((st = encode_3d(&map_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, map_cols, M, 1, ldc,
                             M * ldc, 32, 32, CU_TENSOR_MAP_L2_PROMOTION_NONE, "C")) != GEMM_OK)
             return st;
-        if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, map_a, map_b, map_out, map_out, map_out, kp, pl.grid, stream)) != cudaSuccess)
+        if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, false, map_a, map_b, map_out, map_out, map_out, kp, pl.grid, stream)) != cudaSuccess)
             return fail_cuda(e, "GEMM kernel launch");
         return GEMM_OK;
     }
@@ -1064,12 +1189,12 @@ extern "C" gemm_status_t gemm_f16_f32acc_splitk_noalloc(const uint16_t *A, const
                         ldw, M * ldw, 32, 32, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                         "static split-K scratch")) != GEMM_OK)
         return st;
-    if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, map_a, map_b, map_out, map_out, map_out, kp, pl.grid, stream)) != cudaSuccess)
+    if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, false, map_a, map_b, map_out, map_out, map_out, kp, pl.grid, stream)) != cudaSuccess)
         return fail_cuda(e, "GEMM kernel launch");
     const int64_t threads = M * ((N + 3) / 4);
     const int grid = int(std::min<int64_t>((threads + 255) / 256, int64_t(nd->sms) * 8));
     if ((e = launch_splitk_reduce(static_cast<const float *>(nd->scratch), C, int32_t(M), int32_t(N),
-                                  pl.split_k, 1, ldw, ldc, M * ldc, grid, stream)) != cudaSuccess)
+                                  pl.split_k, 1, ldw, ldc, M * ldc, Epilogue{}, grid, stream)) != cudaSuccess)
         return fail_cuda(e, "split-K reduce launch");
     return GEMM_OK;
 }

@@ -12,6 +12,26 @@ constexpr int kTileM = 128;  // rows of C per tile = TMEM lanes of one accumulat
 constexpr int kTileK = 64;   // K depth of one k-block: one 128-byte swizzle row of f16
 constexpr int kThreads = 192;  // warp 0 TMA producer, warp 1 MMA issuer, warps 2..5 epilogue
 
+// Fused epilogue: what the kernels do to an output value before storing it,
+// C = act(alpha * acc + bias[j]), stored as `out_type`.  The identity (alpha
+// 1, no bias, no activation, f32) is the plain GEMM.
+enum : int32_t { kActNone = 0, kActRelu = 1, kActLeakyRelu = 2, kActGelu = 3, kActGeluTanh = 4,
+                 kActSilu = 5 };
+enum : int32_t { kOutF32 = 0, kOutF16 = 1, kOutBF16 = 2 };
+struct Epilogue {
+    float alpha = 1.0f;
+    const float *bias = nullptr;  // N values per batch, bias_stride apart (0: one for all)
+    int64_t bias_stride = 0;
+    int32_t act = kActNone;
+    float slope = 0.0f;           // kActLeakyRelu
+    int32_t out_type = kOutF32;
+    __host__ __device__ bool identity() const
+    {
+        return alpha == 1.0f && !bias && act == kActNone && out_type == kOutF32;
+    }
+    __host__ __device__ int out_bytes() const { return out_type == kOutF32 ? 4 : 2; }
+};
+
 // Bits of the device status word: which role's bounded wait ran out.
 constexpr uint32_t kStatusProducer = 1u;
 constexpr uint32_t kStatusMma = 2u;
@@ -41,7 +61,7 @@ struct KernelParams {
     // epilogue writes columns [n_tma, N) of C with plain stores.
     int32_t n_tma;
     int32_t tail;
-    float *c_direct;      // C itself (tail stores, in-kernel split-K sums)
+    void *c_direct;       // C itself (tail stores, in-kernel split-K sums), epi.out_type elements
     int64_t ldc;
     int64_t stride_c;
     // In-kernel split-K reduction (each cluster owns exactly one unit): the
@@ -75,6 +95,9 @@ struct KernelParams {
     // batch has M rows.  groups <= kMaxGroupsPerLaunch.
     const int32_t *group_rows;
     int32_t groups;
+    // The fused epilogue (identity for the plain GEMM; only the kernels built
+    // with it read it).
+    Epilogue epi;
     // Optional per-CTA timeline (kTraceSlots globaltimer stamps per CTA), or null.
     unsigned long long *trace;
 };
@@ -102,14 +125,16 @@ struct SmemBudget {
 SmemBudget smem_budget(int tile_m, int tile_n);
 
 // Kernel-side entry points (defined in gemm_kernels.cu).
-cudaError_t set_kernel_attributes(int tile_m, int tile_n);
-cudaError_t launch_tcgen05_gemm(int tile_m, int tile_n, const CUtensorMap &map_a, const CUtensorMap &map_b,
-                                const CUtensorMap &map_out, const CUtensorMap &map_ws,
-                                const CUtensorMap &map_red, const KernelParams &p, int grid,
-                                cudaStream_t stream);
-cudaError_t launch_splitk_reduce(const float *W, float *C, int32_t M, int32_t N, int32_t S,
+// `epi`: the kernel built with the fused epilogue (any Epilogue), else the
+// plain one (identity Epilogue only).
+cudaError_t set_kernel_attributes(int tile_m, int tile_n, bool epi);
+cudaError_t launch_tcgen05_gemm(int tile_m, int tile_n, bool epi, const CUtensorMap &map_a,
+                                const CUtensorMap &map_b, const CUtensorMap &map_out,
+                                const CUtensorMap &map_ws, const CUtensorMap &map_red,
+                                const KernelParams &p, int grid, cudaStream_t stream);
+cudaError_t launch_splitk_reduce(const float *W, void *C, int32_t M, int32_t N, int32_t S,
                                  int32_t batch, int64_t ldw, int64_t ldc, int64_t strideC,
-                                 int grid, cudaStream_t stream);
+                                 const Epilogue &epi, int grid, cudaStream_t stream);
 // Repack A or B into a packed layout with 16-byte aligned rows, and copy a
 // result out of one (only the rows below each count when group_rows is set).
 cudaError_t launch_pack_f16(const uint16_t *src, int64_t s_ld, int64_t s_stride, uint16_t *dst,
@@ -119,8 +144,14 @@ cudaError_t launch_unpack_f32(const float *src, int64_t s_ld, int64_t s_stride, 
                               int64_t d_ld, int64_t d_stride, int32_t rows, int32_t cols,
                               int32_t batch, const int32_t *group_rows, int sms,
                               cudaStream_t stream);
-cudaError_t launch_zero_fill(float *C, int32_t M, int32_t N, int32_t batch, int64_t ldc,
-                             int64_t strideC, const int32_t *group_rows, int grid, cudaStream_t stream);
+cudaError_t launch_unpack_u16(const uint16_t *src, int64_t s_ld, int64_t s_stride, uint16_t *dst,
+                              int64_t d_ld, int64_t d_stride, int32_t rows, int32_t cols,
+                              int32_t batch, const int32_t *group_rows, int sms,
+                              cudaStream_t stream);
+// K == 0: every cell is the epilogue of the empty sum, act(bias[j]).
+cudaError_t launch_zero_fill(void *C, int32_t M, int32_t N, int32_t batch, int64_t ldc,
+                             int64_t strideC, const int32_t *group_rows, const Epilogue &epi,
+                             int grid, cudaStream_t stream);
 cudaError_t device_status_word(uint32_t **ptr);
 
 }  // namespace tsm

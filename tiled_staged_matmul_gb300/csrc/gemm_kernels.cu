@@ -34,6 +34,9 @@
 #include "gemm_internal.h"
 #include "ptx.cuh"
 
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
 namespace tsm {
 
 __device__ uint32_t g_status_word;
@@ -116,6 +119,47 @@ __device__ __forceinline__ uint64_t desc_b(uint32_t saddr)
 }
 
 // ------------------------------------------------------------- helpers
+
+// ------------------------------------------------------------- fused epilogue
+
+// The activations, in f32 with CUDA's own erff / tanhf / expf:
+// relu(v) = v > 0 ? v : 0, leaky_relu(v) = v > 0 ? v : slope v,
+// gelu(v) = v/2 (1 + erf(v / sqrt 2)), gelu_tanh(v) = v/2 (1 + tanh(sqrt(2/pi)
+// (v + 0.044715 v^3))), silu(v) = v / (1 + e^-v).
+__device__ __forceinline__ float epi_act(float v, int32_t act, float slope)
+{
+    switch (act) {
+    case kActRelu: return v > 0.f ? v : 0.f;
+    case kActLeakyRelu: return v > 0.f ? v : slope * v;
+    case kActGelu: return 0.5f * v * (1.f + erff(v * 0.70710678118654752f));
+    case kActGeluTanh:
+        return 0.5f * v * (1.f + tanhf(0.79788456080286536f * (v + 0.044715f * v * v * v)));
+    case kActSilu: return v / (1.f + expf(-v));
+    default: return v;
+    }
+}
+
+// act(alpha * acc + bias), the value before the output rounding.
+__device__ __forceinline__ float epi_value(float acc, float bias, const Epilogue &e)
+{
+    return epi_act(e.alpha * acc + bias, e.act, e.slope);
+}
+
+// An f32 value as the 16-bit output type stores it (round to nearest even).
+__device__ __forceinline__ uint32_t epi_out16(float v, int32_t out_type)
+{
+    return out_type == kOutBF16 ? uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(v)))
+                                : uint32_t(__half_as_ushort(__float2half_rn(v)));
+}
+
+// Store one epilogue value at element `idx` of C (f32 or 16-bit).
+__device__ __forceinline__ void epi_store(void *C, int64_t idx, float v, int32_t out_type)
+{
+    if (out_type == kOutF32)
+        static_cast<float *>(C)[idx] = v;
+    else
+        static_cast<uint16_t *>(C)[idx] = uint16_t(epi_out16(v, out_type));
+}
 
 struct Unit {
     int32_t m0, n0;    // first row / column of the tile
@@ -345,7 +389,7 @@ __device__ __forceinline__ void trace_stamp(const KernelParams &p, int slot)
 
 // ------------------------------------------------------------- the GEMM
 
-template <int BN, bool PAIR>
+template <int BN, bool PAIR, bool EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     tsm_gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a,
                             const __grid_constant__ CUtensorMap map_b,
@@ -610,19 +654,55 @@ __global__ void __launch_bounds__(kThreads, 1)
                 else
                     ptx::tma_store_3d(&map_out, buf, w.n0 + 32 * c, row0, w.z_out);
             };
-            // Plain stores: columns [n_tma, N) of C (fewer than four), or the
-            // whole row of a warp that crosses its group's row count.
+            // Plain stores: columns [n_tma, N) of C (fewer than one 16-byte
+            // granule), or the whole row of a warp that crosses its group's
+            // row count.
             auto tail_box = [&](int c, const uint32_t (&r)[32]) {
                 const int32_t col0 = w.n0 + 32 * c;
                 const int32_t from = rows_partial ? col0 : p.n_tma;
                 if (!w.split && (rows_partial || (p.tail && col0 + 32 > p.n_tma)) && tail_row < w.rows) {
-                    float *dst = p.c_direct + int64_t(w.z_out) * p.stride_c + int64_t(tail_row) * p.ldc;
+                    const int64_t row_at = int64_t(w.z_out) * p.stride_c + int64_t(tail_row) * p.ldc;
 #pragma unroll
                     for (int t = 0; t < 32; ++t) {
                         const int32_t col = col0 + t;
-                        if (col >= from && col < p.N)
-                            dst[col] = __uint_as_float(r[t]);
+                        if (col >= from && col < p.N) {
+                            if constexpr (EPI)
+                                epi_store(p.c_direct, row_at + col, __uint_as_float(r[t]), p.epi.out_type);
+                            else
+                                static_cast<float *>(p.c_direct)[row_at + col] = __uint_as_float(r[t]);
+                        }
                     }
+                }
+            };
+            // Fused epilogue: act(alpha * acc + bias[col]) on box c, in place
+            // (split partials stay raw: the sum applies it).
+            auto transform_box = [&](int c, uint32_t (&r)[32]) {
+                if constexpr (EPI) {
+                    const int32_t col0 = w.n0 + 32 * c;
+                    const float *bias =
+                        p.epi.bias ? p.epi.bias + int64_t(w.z_out) * p.epi.bias_stride : nullptr;
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) {
+                        const int32_t col = col0 + t;
+                        const float bv = (bias && col < p.N) ? __ldg(bias + col) : 0.f;
+                        r[t] = __float_as_uint(epi_value(__uint_as_float(r[t]), bv, p.epi));
+                    }
+                }
+            };
+            // Row `lane` of a 32 x 32 box of 16-bit outputs (64 bytes) into
+            // `buf`, 16-byte chunk j at (j ^ (row / 2) % 4): the layout the
+            // tensor map's 64-byte swizzle expects.
+            auto stage_box16 = [&](uint32_t buf, const uint32_t (&r)[32]) {
+                const uint32_t row_addr = buf + uint32_t(lane) * 64u;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t h[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        h[k] = epi_out16(__uint_as_float(r[8 * j + 2 * k]), p.epi.out_type) |
+                               (epi_out16(__uint_as_float(r[8 * j + 2 * k + 1]), p.epi.out_type) << 16);
+                    ptx::st_shared_v4(row_addr + (uint32_t(j ^ ((lane >> 1) & 3)) << 4), h[0], h[1],
+                                      h[2], h[3]);
                 }
             };
             // Last read of this accumulator: hand it back to the MMA issuer.
@@ -645,6 +725,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tmem_wait_ld();
                 if (c == nch - 1)
                     release_acc();
+                if constexpr (EPI) {
+                    if (!w.split)
+                        transform_box(c, r);
+                }
                 if (via_tma(c)) {
                     uint32_t buf;
                     if (drain) {
@@ -656,7 +740,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         buf = bufs + sbuf * Cfg::EPI_BUF_BYTES;
                         sbuf ^= 1u;
                     }
-                    stage_box(buf, r);
+                    if (EPI && !w.split && p.epi.out_type != kOutF32)
+                        stage_box16(buf, r);
+                    else
+                        stage_box(buf, r);
                     ptx::fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
@@ -750,15 +837,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int32_t gr = w.m0 + r0 + row;
                         const int32_t gc = w.n0 + (f - row * (BN / 4)) * 4;
                         if (row < p.rows_per && r0 + row < Cfg::TILE_M && gr < p.M && gc < p.N) {
-                            float *dst = p.c_direct + bz * p.stride_c + int64_t(gr) * p.ldc + gc;
-                            if (gc + 3 < p.N) {
-                                *reinterpret_cast<float4 *>(dst) = acc;
+                            const int64_t at = bz * p.stride_c + int64_t(gr) * p.ldc + gc;
+                            if constexpr (EPI) {
+                                const float *bias =
+                                    p.epi.bias ? p.epi.bias + bz * p.epi.bias_stride : nullptr;
+                                float v[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+                                for (int k = 0; k < 4; ++k)
+                                    v[k] = epi_value(v[k], (bias && gc + k < p.N) ? __ldg(bias + gc + k) : 0.f,
+                                                     p.epi);
+                                if (gc + 3 < p.N && p.epi.out_type == kOutF32) {
+                                    *reinterpret_cast<float4 *>(static_cast<float *>(p.c_direct) + at) =
+                                        make_float4(v[0], v[1], v[2], v[3]);
+                                } else if (gc + 3 < p.N) {
+                                    *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(p.c_direct) + at) =
+                                        make_uint2(epi_out16(v[0], p.epi.out_type) |
+                                                       (epi_out16(v[1], p.epi.out_type) << 16),
+                                                   epi_out16(v[2], p.epi.out_type) |
+                                                       (epi_out16(v[3], p.epi.out_type) << 16));
+                                } else {
+#pragma unroll
+                                    for (int k = 0; k < 3; ++k)
+                                        if (gc + k < p.N)
+                                            epi_store(p.c_direct, at + k, v[k], p.epi.out_type);
+                                }
                             } else {
-                                dst[0] = acc.x;
-                                if (gc + 1 < p.N)
-                                    dst[1] = acc.y;
-                                if (gc + 2 < p.N)
-                                    dst[2] = acc.z;
+                                float *dst = static_cast<float *>(p.c_direct) + at;
+                                if (gc + 3 < p.N) {
+                                    *reinterpret_cast<float4 *>(dst) = acc;
+                                } else {
+                                    dst[0] = acc.x;
+                                    if (gc + 1 < p.N)
+                                        dst[1] = acc.y;
+                                    if (gc + 2 < p.N)
+                                        dst[2] = acc.z;
+                                }
                             }
                         }
                     };
@@ -814,10 +927,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // W[b*S + s][i][j].  Four adjacent columns per thread; W's rows are ldw
 // floats (ldw a multiple of 4), so the loads are aligned float4s.
 __global__ void __launch_bounds__(256)
-    tsm_splitk_reduce_kernel(const float *__restrict__ W, float *__restrict__ C, int32_t M,
+    tsm_splitk_reduce_kernel(const float *__restrict__ W, void *__restrict__ C, int32_t M,
                              int32_t N, int32_t S, int32_t batch, int64_t ldw, int64_t ldc,
-                             int64_t strideC)
+                             int64_t strideC, Epilogue epi)
 {
+    const bool plain = epi.identity();
     const int64_t n4 = (N + 3) / 4;
     const int64_t per_mat = int64_t(M) * n4;
     const int64_t total = per_mat * batch;
@@ -838,24 +952,36 @@ __global__ void __launch_bounds__(256)
             acc.z += v.z;
             acc.w += v.w;
         }
-        float *c = C + b * strideC + i * ldc + j;
-        if (j + 3 < N) {
-            *reinterpret_cast<float4 *>(c) = acc;
-        } else {
-            c[0] = acc.x;
-            if (j + 1 < N)
-                c[1] = acc.y;
-            if (j + 2 < N)
-                c[2] = acc.z;
+        const int64_t at = b * strideC + i * ldc + j;
+        if (plain) {
+            float *c = static_cast<float *>(C) + at;
+            if (j + 3 < N) {
+                *reinterpret_cast<float4 *>(c) = acc;
+            } else {
+                c[0] = acc.x;
+                if (j + 1 < N)
+                    c[1] = acc.y;
+                if (j + 2 < N)
+                    c[2] = acc.z;
+            }
+            continue;
         }
+        const float *bias = epi.bias ? epi.bias + b * epi.bias_stride : nullptr;
+        const float v[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (j + k < N)
+                epi_store(C, at + k, epi_value(v[k], bias ? __ldg(bias + j + k) : 0.f, epi),
+                          epi.out_type);
     }
 }
 
-// K == 0: every cell is the empty sum (in a grouped launch, every cell of
-// the rows below the group's count, clamped to [0, M]).
+// K == 0: every cell is the empty sum, through the epilogue: act(bias[j])
+// (in a grouped launch, every cell of the rows below the group's count,
+// clamped to [0, M]).
 __global__ void __launch_bounds__(256)
-    tsm_zero_fill_kernel(float *__restrict__ C, int32_t M, int32_t N, int32_t batch, int64_t ldc,
-                         int64_t strideC, const int32_t *__restrict__ group_rows)
+    tsm_zero_fill_kernel(void *__restrict__ C, int32_t M, int32_t N, int32_t batch, int64_t ldc,
+                         int64_t strideC, const int32_t *__restrict__ group_rows, Epilogue epi)
 {
     const int64_t per_mat = int64_t(M) * N;
     const int64_t total = per_mat * batch;
@@ -867,7 +993,8 @@ __global__ void __launch_bounds__(256)
         const int64_t j = r - i * N;
         if (group_rows && i >= group_rows[b])
             continue;
-        C[b * strideC + i * ldc + j] = 0.0f;
+        const float bv = epi.bias ? __ldg(epi.bias + b * epi.bias_stride + j) : 0.f;
+        epi_store(C, b * strideC + i * ldc + j, epi_value(0.f, bv, epi), epi.out_type);
     }
 }
 
@@ -954,32 +1081,38 @@ SmemBudget smem_budget(int tile_m, int tile_n)
     }
 }
 
-template <int BN, bool PAIR>
+template <int BN, bool PAIR, bool EPI>
 static cudaError_t set_attr()
 {
-    return cudaFuncSetAttribute(tsm_gemm_tcgen05_kernel<BN, PAIR>,
+    return cudaFuncSetAttribute(tsm_gemm_tcgen05_kernel<BN, PAIR, EPI>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 TileCfg<BN, PAIR>::SMEM_BYTES);
 }
 
-cudaError_t set_kernel_attributes(int tile_m, int tile_n)
+template <bool EPI>
+static cudaError_t set_attrs_of(int tile_m, int tile_n)
 {
     if (tile_m == 2 * kTileM) {
         switch (tile_n) {
-        case 128: return set_attr<128, true>();
-        case 256: return set_attr<256, true>();
+        case 128: return set_attr<128, true, EPI>();
+        case 256: return set_attr<256, true, EPI>();
         default: return cudaErrorInvalidValue;
         }
     }
     switch (tile_n) {
-    case 64: return set_attr<64, false>();
-    case 128: return set_attr<128, false>();
-    case 256: return set_attr<256, false>();
+    case 64: return set_attr<64, false, EPI>();
+    case 128: return set_attr<128, false, EPI>();
+    case 256: return set_attr<256, false, EPI>();
     default: return cudaErrorInvalidValue;
     }
 }
 
-template <int BN, bool PAIR>
+cudaError_t set_kernel_attributes(int tile_m, int tile_n, bool epi)
+{
+    return epi ? set_attrs_of<true>(tile_m, tile_n) : set_attrs_of<false>(tile_m, tile_n);
+}
+
+template <int BN, bool PAIR, bool EPI>
 static cudaError_t launch_bn(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o,
                              const CUtensorMap &ws, const CUtensorMap &r, const KernelParams &p,
                              int grid, cudaStream_t stream)
@@ -1001,43 +1134,54 @@ static cudaError_t launch_bn(const CUtensorMap &a, const CUtensorMap &b, const C
         cfg.attrs = nullptr;
         cfg.numAttrs = 0;
     }
-    return cudaLaunchKernelEx(&cfg, tsm_gemm_tcgen05_kernel<BN, PAIR>, a, b, o, ws, r, p);
+    return cudaLaunchKernelEx(&cfg, tsm_gemm_tcgen05_kernel<BN, PAIR, EPI>, a, b, o, ws, r, p);
 }
 
-cudaError_t launch_tcgen05_gemm(int tile_m, int tile_n, const CUtensorMap &map_a,
-                                const CUtensorMap &map_b, const CUtensorMap &map_out,
-                                const CUtensorMap &map_ws, const CUtensorMap &map_red,
-                                const KernelParams &p, int grid, cudaStream_t stream)
+template <bool EPI>
+static cudaError_t launch_of(int tile_m, int tile_n, const CUtensorMap &map_a,
+                             const CUtensorMap &map_b, const CUtensorMap &map_out,
+                             const CUtensorMap &map_ws, const CUtensorMap &map_red,
+                             const KernelParams &p, int grid, cudaStream_t stream)
 {
     if (tile_m == 2 * kTileM) {
         if (grid % 2)
             return cudaErrorInvalidValue;
         switch (tile_n) {
-        case 128: return launch_bn<128, true>(map_a, map_b, map_out, map_ws, map_red, p, grid, stream);
-        case 256: return launch_bn<256, true>(map_a, map_b, map_out, map_ws, map_red, p, grid, stream);
+        case 128: return launch_bn<128, true, EPI>(map_a, map_b, map_out, map_ws, map_red, p, grid, stream);
+        case 256: return launch_bn<256, true, EPI>(map_a, map_b, map_out, map_ws, map_red, p, grid, stream);
         default: return cudaErrorInvalidValue;
         }
     }
     switch (tile_n) {
-    case 64: return launch_bn<64, false>(map_a, map_b, map_out, map_ws, map_red, p, grid, stream);
-    case 128: return launch_bn<128, false>(map_a, map_b, map_out, map_ws, map_red, p, grid, stream);
-    case 256: return launch_bn<256, false>(map_a, map_b, map_out, map_ws, map_red, p, grid, stream);
+    case 64: return launch_bn<64, false, EPI>(map_a, map_b, map_out, map_ws, map_red, p, grid, stream);
+    case 128: return launch_bn<128, false, EPI>(map_a, map_b, map_out, map_ws, map_red, p, grid, stream);
+    case 256: return launch_bn<256, false, EPI>(map_a, map_b, map_out, map_ws, map_red, p, grid, stream);
     default: return cudaErrorInvalidValue;
     }
 }
 
-cudaError_t launch_splitk_reduce(const float *W, float *C, int32_t M, int32_t N, int32_t S,
-                                 int32_t batch, int64_t ldw, int64_t ldc, int64_t strideC,
-                                 int grid, cudaStream_t stream)
+cudaError_t launch_tcgen05_gemm(int tile_m, int tile_n, bool epi, const CUtensorMap &map_a,
+                                const CUtensorMap &map_b, const CUtensorMap &map_out,
+                                const CUtensorMap &map_ws, const CUtensorMap &map_red,
+                                const KernelParams &p, int grid, cudaStream_t stream)
 {
-    tsm_splitk_reduce_kernel<<<grid, 256, 0, stream>>>(W, C, M, N, S, batch, ldw, ldc, strideC);
+    return epi ? launch_of<true>(tile_m, tile_n, map_a, map_b, map_out, map_ws, map_red, p, grid, stream)
+               : launch_of<false>(tile_m, tile_n, map_a, map_b, map_out, map_ws, map_red, p, grid, stream);
+}
+
+cudaError_t launch_splitk_reduce(const float *W, void *C, int32_t M, int32_t N, int32_t S,
+                                 int32_t batch, int64_t ldw, int64_t ldc, int64_t strideC,
+                                 const Epilogue &epi, int grid, cudaStream_t stream)
+{
+    tsm_splitk_reduce_kernel<<<grid, 256, 0, stream>>>(W, C, M, N, S, batch, ldw, ldc, strideC, epi);
     return cudaGetLastError();
 }
 
-cudaError_t launch_zero_fill(float *C, int32_t M, int32_t N, int32_t batch, int64_t ldc,
-                             int64_t strideC, const int32_t *group_rows, int grid, cudaStream_t stream)
+cudaError_t launch_zero_fill(void *C, int32_t M, int32_t N, int32_t batch, int64_t ldc,
+                             int64_t strideC, const int32_t *group_rows, const Epilogue &epi,
+                             int grid, cudaStream_t stream)
 {
-    tsm_zero_fill_kernel<<<grid, 256, 0, stream>>>(C, M, N, batch, ldc, strideC, group_rows);
+    tsm_zero_fill_kernel<<<grid, 256, 0, stream>>>(C, M, N, batch, ldc, strideC, group_rows, epi);
     return cudaGetLastError();
 }
 
@@ -1089,6 +1233,15 @@ cudaError_t launch_unpack_f32(const float *src, int64_t s_ld, int64_t s_stride, 
     return launch_repack<uint32_t, false>(reinterpret_cast<const uint32_t *>(src), s_ld, s_stride,
                                           reinterpret_cast<uint32_t *>(dst), d_ld, d_stride, rows,
                                           cols, batch, group_rows, sms, stream);
+}
+
+cudaError_t launch_unpack_u16(const uint16_t *src, int64_t s_ld, int64_t s_stride, uint16_t *dst,
+                              int64_t d_ld, int64_t d_stride, int32_t rows, int32_t cols,
+                              int32_t batch, const int32_t *group_rows, int sms,
+                              cudaStream_t stream)
+{
+    return launch_repack<uint16_t, false>(src, s_ld, s_stride, dst, d_ld, d_stride, rows, cols, batch,
+                                          group_rows, sms, stream);
 }
 
 cudaError_t device_status_word(uint32_t **ptr)
