@@ -57,6 +57,11 @@ def parse_args(argv=None):
     p.add_argument("--ld-pad", type=int, default=0,
                    help="lay A, B and C out with lda = K + p, ldb = ldc = N + p elements; an odd p "
                         "makes every operand unaddressable by the TMA (the repacking path)")
+    p.add_argument("--act", default="none",
+                   help="fused epilogue activation: none, relu, leaky_relu, gelu, gelu_tanh, silu")
+    p.add_argument("--bias", action="store_true", help="fused epilogue: add a per-column f32 bias")
+    p.add_argument("--out", default="f32", choices=("f32", "f16", "bf16"),
+                   help="fused epilogue: the element type of C")
     p.add_argument("--trace", action="store_true",
                    help="add a per-CTA phase timeline (one extra traced step) to the JSON line")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -332,23 +337,29 @@ def run_ours(args, rank, local_rank, world):
     w = pick_workload(args)
     A_h, B_h = synthetic.workload_operands(w)
     pad = args.ld_pad
+    out_dtype = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[args.out]
+    out_bytes = 4 if args.out == "f32" else 2
     lda, ldb, ldc = w.K + pad, w.N + pad, w.N + pad
     A = torch.empty((w.M, lda), dtype=torch.float16, device=dev)[:, :w.K]
     B = torch.empty((w.K, ldb), dtype=torch.float16, device=dev)[:, :w.N]
     A.copy_(A_h)
     B.copy_(B_h)
-    C = torch.empty((w.M, ldc), dtype=torch.float32, device=dev)[:, :w.N]
+    C = torch.empty((w.M, ldc), dtype=out_dtype, device=dev)[:, :w.N]
+    bias = (torch.linspace(-1, 1, w.N, dtype=torch.float32, device=dev) if args.bias else None)
+    fused = args.act != "none" or args.bias or args.out != "f32"
+    epi = binding.epilogue(1.0, bias.data_ptr() if bias is not None else 0, 0, args.act, 0.01,
+                           args.out) if fused else None
     stream = torch.cuda.current_stream()
     opts = binding.GemmOptions(args.split_k, args.tile_n, 0, 0, args.tile_m, args.splitk_reduce)
     plan = binding.gemm_plan(w.M, w.N, w.K, 1, opts)
     launches_per_call = 2 if plan["split_k"] > 1 and not plan["fused_reduce"] else 1
     # Row pitches that are not multiples of 16 bytes: that operand is copied
     # (A and B in, C out) around the GEMM.
-    copies = int(lda % 8 != 0) + int(ldb % 8 != 0) + int(ldc % 4 != 0)
+    copies = int(lda % 8 != 0) + int(ldb % 8 != 0) + int(ldc % (16 // out_bytes) != 0)
     repacked = copies > 0
     launches_per_call += copies
 
-    working_set = 2 * w.M * w.K + 2 * w.K * w.N + 4 * w.M * w.N
+    working_set = 2 * w.M * w.K + 2 * w.K * w.N + out_bytes * w.M * w.N
     flush = working_set < 2 * L2_BYTES
     scrub = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
     sweep = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
@@ -362,16 +373,22 @@ def run_ours(args, rank, local_rank, world):
         torch.sum(sweep, dim=0, keepdim=True, out=sink)
 
     def call(o=opts):
-        binding.check(binding.gemm_f16_f32acc_opts(A.data_ptr(), B.data_ptr(), C.data_ptr(),
-                                                   w.M, w.N, w.K, lda, ldb, ldc, 0, 0, 0, 1,
-                                                   o, stream.cuda_stream))
+        if fused:
+            binding.check(binding.gemm_f16_fused(A.data_ptr(), B.data_ptr(), C.data_ptr(), w.M, w.N,
+                                                 w.K, lda, ldb, ldc, 0, 0, 0, 1, epi, o,
+                                                 stream.cuda_stream))
+        else:
+            binding.check(binding.gemm_f16_f32acc_opts(A.data_ptr(), B.data_ptr(), C.data_ptr(),
+                                                       w.M, w.N, w.K, lda, ldb, ldc, 0, 0, 0, 1,
+                                                       o, stream.cuda_stream))
 
     per_step_ms, t0, t1, sampler = timed_loop(args, call, flush_l2 if flush else None, stream,
                                               world, local_rank)
     ms_local = sum(per_step_ms) / len(per_step_ms)
     value, ms = replica_throughput(w.flops, ms_local, world, dev)
-    roofline = roofline_of(w.flops, w.algorithmic_bytes, ms_local,
-                           recorded_traffic(w.name) if not pad else None,
+    abytes = 2 * w.M * w.K + 2 * w.K * w.N + out_bytes * w.M * w.N + (4 * w.N if args.bias else 0)
+    roofline = roofline_of(w.flops, abytes, ms_local,
+                           recorded_traffic(w.name) if not pad and not fused else None,
                            "tsm_gemm_tcgen05_kernel" + (" + tsm_splitk_reduce_kernel"
                                                         if plan["split_k"] > 1
                                                         and not plan["fused_reduce"] else "")
@@ -397,6 +414,8 @@ def run_ours(args, rank, local_rank, world):
                    if plan["split_k"] > 1 else "none",
                    "stages": plan["stages"], "grid": plan["grid"],
                    "ld": [lda, ldb, ldc],
+                   "epilogue": ({"activation": args.act, "bias": bool(args.bias), "out": args.out}
+                                if fused else "none (f32 store)"),
                    "layout": (f"repacked ({copies} operand copies: row pitches not multiples "
                               "of 16 bytes)" if repacked else "TMA-addressable"),
                    "l2": "flushed before every step (write 2xL2, then read 2xL2)" if flush else
@@ -410,7 +429,7 @@ def run_ours(args, rank, local_rank, world):
     if args.trace:
         result["trace"] = traced_step(args, binding, call, plan, flush_l2 if flush else None, dev)
 
-    if not args.no_e2e:
+    if not args.no_e2e and not fused:
         result["e2e"] = run_e2e(args, w, A_h, B_h, dev, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, A_h, B_h, target_s=15.0)

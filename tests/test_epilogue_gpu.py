@@ -201,3 +201,22 @@ def test_torch_wrapper(b):
     assert out.dtype == torch.float16 and out.shape == (64, 80)
     check_epilogue(as_f64(out), oracle.gemm_f64(A, B, 64, 80, 96), 2.0, bias.cpu().double().numpy(),
                    "gelu", "f16", 96)
+
+
+@pytest.mark.parametrize("act", ["gelu", "gelu_tanh", "silu", "relu", "leaky_relu"])
+def test_activation_accuracy_on_its_own(b, act):
+    """K = 1 and B = 1: C = act(a) for a grid of f16 values a, against the
+    fp64 definition, within 2e-6 x max(1, |a|) (the product is exact here,
+    so this bounds the activation's own f32 evaluation)."""
+    xs = np.unique(np.concatenate([np.linspace(-12, 12, 3001), np.linspace(-1, 1, 2001),
+                                   [0.0, -0.0, 1e-4, -1e-4, 30.0, -30.0, 80.0, -80.0]]).astype(np.float16))
+    M = xs.size
+    A = torch.from_numpy(xs.reshape(M, 1).copy())
+    B = torch.ones((1, 8), dtype=torch.float16)
+    C, _ = run_fused(b, A, B, act=act, out="f32", slope=0.125)
+    got = C[:, 0]
+    want = oracle.activation_f64(xs.astype(np.float64), act, 0.125)
+    err = np.abs(got - want)
+    bound = 2e-6 * np.maximum(1.0, np.abs(xs.astype(np.float64)))
+    worst = int(np.argmax(err - bound))
+    assert np.all(err <= bound), (act, float(xs[worst]), float(got[worst]), float(want[worst]))

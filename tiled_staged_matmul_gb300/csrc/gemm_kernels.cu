@@ -122,19 +122,41 @@ __device__ __forceinline__ uint64_t desc_b(uint32_t saddr)
 
 // ------------------------------------------------------------- fused epilogue
 
-// The activations, in f32 with CUDA's own erff / tanhf / expf:
-// relu(v) = v > 0 ? v : 0, leaky_relu(v) = v > 0 ? v : slope v,
-// gelu(v) = v/2 (1 + erf(v / sqrt 2)), gelu_tanh(v) = v/2 (1 + tanh(sqrt(2/pi)
-// (v + 0.044715 v^3))), silu(v) = v / (1 + e^-v).
+// erf(x) by Abramowitz & Stegun, Handbook of Mathematical Functions, formula
+// 7.1.26: for x >= 0, erf(x) = 1 - t (a1 + t (a2 + t (a3 + t (a4 + t a5))))
+// e^(-x^2) with t = 1 / (1 + p x), absolute error below 1.5e-7; odd in x.
+__device__ __forceinline__ float erf_as(float x)
+{
+    const float ax = fabsf(x);
+    const float t = __fdividef(1.f, fmaf(0.3275911f, ax, 1.f));
+    float poly = fmaf(1.061405429f, t, -1.453152027f);
+    poly = fmaf(poly, t, 1.421413741f);
+    poly = fmaf(poly, t, -0.284496736f);
+    poly = fmaf(poly, t, 0.254829592f);
+    const float y = 1.f - poly * t * __expf(-ax * ax);
+    return copysignf(y, x);
+}
+
+// The activations, in f32:
+//   relu(v) = v > 0 ? v : 0            leaky_relu(v) = v > 0 ? v : slope v
+//   gelu(v) = v/2 (1 + erf(v / sqrt 2))   (erf as above)
+//   gelu_tanh(v) = v/2 (1 + tanh u), u = sqrt(2/pi) (v + 0.044715 v^3),
+//     tanh u = 1 - 2 / (1 + e^(2u))   (saturates to +-1 for large |u|)
+//   silu(v) = v / (1 + e^-v)
+// with CUDA's __expf and __fdividef; the errors these add are far below the
+// product's own rounding bound.
 __device__ __forceinline__ float epi_act(float v, int32_t act, float slope)
 {
     switch (act) {
     case kActRelu: return v > 0.f ? v : 0.f;
     case kActLeakyRelu: return v > 0.f ? v : slope * v;
-    case kActGelu: return 0.5f * v * (1.f + erff(v * 0.70710678118654752f));
-    case kActGeluTanh:
-        return 0.5f * v * (1.f + tanhf(0.79788456080286536f * (v + 0.044715f * v * v * v)));
-    case kActSilu: return v / (1.f + expf(-v));
+    case kActGelu: return 0.5f * v * (1.f + erf_as(v * 0.70710678118654752f));
+    case kActGeluTanh: {
+        const float u = 0.79788456080286536f * fmaf(0.044715f * v, v * v, v);
+        const float th = 1.f - __fdividef(2.f, 1.f + __expf(2.f * u));
+        return 0.5f * v * (1.f + th);
+    }
+    case kActSilu: return __fdividef(v, 1.f + __expf(-v));
     default: return v;
     }
 }
@@ -150,6 +172,74 @@ __device__ __forceinline__ uint32_t epi_out16(float v, int32_t out_type)
 {
     return out_type == kOutBF16 ? uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(v)))
                                 : uint32_t(__half_as_ushort(__float2half_rn(v)));
+}
+
+// The fused epilogue on four consecutive values of one row (columns col ...
+// col + 3): v = act(alpha * v + bias[col]); the activation is chosen once,
+// outside the four.
+__device__ __forceinline__ void epi_apply4(float4 &v, int32_t col, int32_t N, const float *bias,
+                                           const Epilogue &e)
+{
+    float b[4] = {0.f, 0.f, 0.f, 0.f};
+    if (bias) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            b[k] = col + k < N ? __ldg(bias + col + k) : 0.f;
+    }
+    v.x = e.alpha * v.x + b[0];
+    v.y = e.alpha * v.y + b[1];
+    v.z = e.alpha * v.z + b[2];
+    v.w = e.alpha * v.w + b[3];
+    switch (e.act) {
+    case kActNone: break;
+    case kActRelu:
+        v.x = v.x > 0.f ? v.x : 0.f;
+        v.y = v.y > 0.f ? v.y : 0.f;
+        v.z = v.z > 0.f ? v.z : 0.f;
+        v.w = v.w > 0.f ? v.w : 0.f;
+        break;
+    case kActLeakyRelu:
+        v.x = v.x > 0.f ? v.x : e.slope * v.x;
+        v.y = v.y > 0.f ? v.y : e.slope * v.y;
+        v.z = v.z > 0.f ? v.z : e.slope * v.z;
+        v.w = v.w > 0.f ? v.w : e.slope * v.w;
+        break;
+    default:
+        v.x = epi_act(v.x, e.act, e.slope);
+        v.y = epi_act(v.y, e.act, e.slope);
+        v.z = epi_act(v.z, e.act, e.slope);
+        v.w = epi_act(v.w, e.act, e.slope);
+        break;
+    }
+}
+
+// One row of a staged 32 x 32 f32 box (this lane's, 128-byte swizzled) through
+// the epilogue in place, the activation fixed at compile time: eight values
+// per step, so a warp keeps several activations in flight.
+template <int ACT>
+__device__ __forceinline__ void epi_row(uint32_t row_addr, uint32_t swz, int32_t col0, int32_t N,
+                                        const float *bias, float alpha, float slope)
+{
+#pragma unroll 1
+    for (int j = 0; j < 8; j += 2) {
+        const uint32_t a0 = row_addr + (uint32_t(j ^ swz) << 4);
+        const uint32_t a1 = row_addr + (uint32_t((j + 1) ^ swz) << 4);
+        const uint4 u0 = ptx::ld_shared_v4(a0);
+        const uint4 u1 = ptx::ld_shared_v4(a1);
+        float v[8] = {__uint_as_float(u0.x), __uint_as_float(u0.y), __uint_as_float(u0.z),
+                      __uint_as_float(u0.w), __uint_as_float(u1.x), __uint_as_float(u1.y),
+                      __uint_as_float(u1.z), __uint_as_float(u1.w)};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int32_t col = col0 + 4 * j + k;
+            const float b = (bias && col < N) ? __ldg(bias + col) : 0.f;
+            v[k] = epi_act(fmaf(alpha, v[k], b), ACT, slope);
+        }
+        ptx::st_shared_v4(a0, __float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
+                          __float_as_uint(v[3]));
+        ptx::st_shared_v4(a1, __float_as_uint(v[4]), __float_as_uint(v[5]), __float_as_uint(v[6]),
+                          __float_as_uint(v[7]));
+    }
 }
 
 // Store one epilogue value at element `idx` of C (f32 or 16-bit).
@@ -665,44 +755,67 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int t = 0; t < 32; ++t) {
                         const int32_t col = col0 + t;
-                        if (col >= from && col < p.N) {
-                            if constexpr (EPI)
-                                epi_store(p.c_direct, row_at + col, __uint_as_float(r[t]), p.epi.out_type);
-                            else
-                                static_cast<float *>(p.c_direct)[row_at + col] = __uint_as_float(r[t]);
-                        }
+                        if (col >= from && col < p.N)
+                            static_cast<float *>(p.c_direct)[row_at + col] = __uint_as_float(r[t]);
                     }
                 }
             };
-            // Fused epilogue: act(alpha * acc + bias[col]) on box c, in place
-            // (split partials stay raw: the sum applies it).
-            auto transform_box = [&](int c, uint32_t (&r)[32]) {
-                if constexpr (EPI) {
-                    const int32_t col0 = w.n0 + 32 * c;
-                    const float *bias =
-                        p.epi.bias ? p.epi.bias + int64_t(w.z_out) * p.epi.bias_stride : nullptr;
-#pragma unroll
-                    for (int t = 0; t < 32; ++t) {
-                        const int32_t col = col0 + t;
-                        const float bv = (bias && col < p.N) ? __ldg(bias + col) : 0.f;
-                        r[t] = __float_as_uint(epi_value(__uint_as_float(r[t]), bv, p.epi));
-                    }
+            // Fused epilogue, on a box staged (f32, swizzled) in shared memory:
+            // each lane rewrites its own row in place, act(alpha * v + bias),
+            // four values at a time; a 16-bit output is then packed into the
+            // same buffer as 64-byte rows in the tensor map's 64-byte swizzle
+            // (16-byte chunk k of row r at k ^ (r / 2) % 4).
+            auto epi_box = [&](uint32_t buf, int c) {
+                const uint32_t row_addr = buf + uint32_t(lane) * 128u;
+                const int32_t col0 = w.n0 + 32 * c;
+                const float *bias =
+                    p.epi.bias ? p.epi.bias + int64_t(w.z_out) * p.epi.bias_stride : nullptr;
+                const uint32_t swz = uint32_t(lane & 7);
+                const float al = p.epi.alpha, sl = p.epi.slope;
+                switch (p.epi.act) {
+                case kActRelu: epi_row<kActRelu>(row_addr, swz, col0, p.N, bias, al, sl); break;
+                case kActLeakyRelu: epi_row<kActLeakyRelu>(row_addr, swz, col0, p.N, bias, al, sl); break;
+                case kActGelu: epi_row<kActGelu>(row_addr, swz, col0, p.N, bias, al, sl); break;
+                case kActGeluTanh: epi_row<kActGeluTanh>(row_addr, swz, col0, p.N, bias, al, sl); break;
+                case kActSilu: epi_row<kActSilu>(row_addr, swz, col0, p.N, bias, al, sl); break;
+                default: epi_row<kActNone>(row_addr, swz, col0, p.N, bias, al, sl); break;
                 }
-            };
-            // Row `lane` of a 32 x 32 box of 16-bit outputs (64 bytes) into
-            // `buf`, 16-byte chunk j at (j ^ (row / 2) % 4): the layout the
-            // tensor map's 64-byte swizzle expects.
-            auto stage_box16 = [&](uint32_t buf, const uint32_t (&r)[32]) {
-                const uint32_t row_addr = buf + uint32_t(lane) * 64u;
+                if (p.epi.out_type != kOutF32) {
+                    uint32_t h[16];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint32_t h[4];
+                    for (int j = 0; j < 8; ++j) {
+                        const uint4 u = ptx::ld_shared_v4(row_addr + (uint32_t(j ^ (lane & 7)) << 4));
+                        h[2 * j] = epi_out16(__uint_as_float(u.x), p.epi.out_type) |
+                                   (epi_out16(__uint_as_float(u.y), p.epi.out_type) << 16);
+                        h[2 * j + 1] = epi_out16(__uint_as_float(u.z), p.epi.out_type) |
+                                       (epi_out16(__uint_as_float(u.w), p.epi.out_type) << 16);
+                    }
+                    __syncwarp();  // every f32 row is read before any 16-bit row lands on it
+                    const uint32_t row16 = buf + uint32_t(lane) * 64u;
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        h[k] = epi_out16(__uint_as_float(r[8 * j + 2 * k]), p.epi.out_type) |
-                               (epi_out16(__uint_as_float(r[8 * j + 2 * k + 1]), p.epi.out_type) << 16);
-                    ptx::st_shared_v4(row_addr + (uint32_t(j ^ ((lane >> 1) & 3)) << 4), h[0], h[1],
-                                      h[2], h[3]);
+                        ptx::st_shared_v4(row16 + (uint32_t(k ^ ((lane >> 1) & 3)) << 4), h[4 * k],
+                                          h[4 * k + 1], h[4 * k + 2], h[4 * k + 3]);
+                }
+            };
+            // Plain stores of an epilogue box from shared memory: the columns
+            // the TMA store does not cover, or the rows below a group's count.
+            auto epi_tail = [&](uint32_t buf, int c) {
+                const int32_t col0 = w.n0 + 32 * c;
+                const int32_t from = rows_partial ? col0 : p.n_tma;
+                if (!(rows_partial || (p.tail && col0 + 32 > p.n_tma)) || tail_row >= w.rows)
+                    return;
+                const int64_t row_at = int64_t(w.z_out) * p.stride_c + int64_t(tail_row) * p.ldc;
+                const int32_t t0 = max(from - col0, 0);
+                const int32_t t1 = min(p.N - col0, 32);
+#pragma unroll 1
+                for (int32_t t = t0; t < t1; ++t) {
+                    if (p.epi.out_type == kOutF32)
+                        static_cast<uint32_t *>(p.c_direct)[row_at + col0 + t] = ptx::ld_shared_u32(
+                            buf + uint32_t(lane) * 128u + (uint32_t((t >> 2) ^ (lane & 7)) << 4) + uint32_t(t & 3) * 4u);
+                    else
+                        static_cast<uint16_t *>(p.c_direct)[row_at + col0 + t] = ptx::ld_shared_u16(
+                            buf + uint32_t(lane) * 64u + (uint32_t((t >> 3) ^ ((lane >> 1) & 3)) << 4) + uint32_t(t & 7) * 2u);
                 }
             };
             // Last read of this accumulator: hand it back to the MMA issuer.
@@ -719,31 +832,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             // On the CTA's last unit the operand ring is idle: each box gets
             // a buffer of its own there and no store waits for another.
             const bool drain = u + nclusters >= num_units;
+            auto take_buf = [&](int c) -> uint32_t {
+                if (drain)
+                    return base + (uint32_t(e) * uint32_t(BN / 32) + uint32_t(c)) * Cfg::EPI_BUF_BYTES;
+                if (lane == 0)
+                    ptx::bulk_wait_group_read<1>();  // the store that used this buffer has read it
+                __syncwarp();
+                const uint32_t b = bufs + sbuf * Cfg::EPI_BUF_BYTES;
+                sbuf ^= 1u;
+                return b;
+            };
             for (int c = 0; c < nch; ++c) {
                 uint32_t r[32];
                 ptx::tmem_ld_32x32b_x32(tm_row + 32u * c, r);
                 ptx::tmem_wait_ld();
                 if (c == nch - 1)
                     release_acc();
+                const bool tma = via_tma(c);
                 if constexpr (EPI) {
-                    if (!w.split)
-                        transform_box(c, r);
-                }
-                if (via_tma(c)) {
-                    uint32_t buf;
-                    if (drain) {
-                        buf = base + (uint32_t(e) * uint32_t(BN / 32) + uint32_t(c)) * Cfg::EPI_BUF_BYTES;
-                    } else {
-                        if (lane == 0)
-                            ptx::bulk_wait_group_read<1>();
-                        __syncwarp();
-                        buf = bufs + sbuf * Cfg::EPI_BUF_BYTES;
-                        sbuf ^= 1u;
-                    }
-                    if (EPI && !w.split && p.epi.out_type != kOutF32)
-                        stage_box16(buf, r);
-                    else
+                    if (!w.split) {
+                        const uint32_t buf = take_buf(c);
                         stage_box(buf, r);
+                        epi_box(buf, c);
+                        if (tma) {
+                            ptx::fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                store_box(c, buf);
+                                ptx::bulk_commit_group();
+                            }
+                        }
+                        epi_tail(buf, c);
+                        continue;
+                    }
+                }
+                if (tma) {
+                    const uint32_t buf = take_buf(c);
+                    stage_box(buf, r);
                     ptx::fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
@@ -841,25 +966,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if constexpr (EPI) {
                                 const float *bias =
                                     p.epi.bias ? p.epi.bias + bz * p.epi.bias_stride : nullptr;
-                                float v[4] = {acc.x, acc.y, acc.z, acc.w};
-#pragma unroll
-                                for (int k = 0; k < 4; ++k)
-                                    v[k] = epi_value(v[k], (bias && gc + k < p.N) ? __ldg(bias + gc + k) : 0.f,
-                                                     p.epi);
+                                float4 v = acc;
+                                epi_apply4(v, gc, p.N, bias, p.epi);
                                 if (gc + 3 < p.N && p.epi.out_type == kOutF32) {
-                                    *reinterpret_cast<float4 *>(static_cast<float *>(p.c_direct) + at) =
-                                        make_float4(v[0], v[1], v[2], v[3]);
+                                    *reinterpret_cast<float4 *>(static_cast<float *>(p.c_direct) + at) = v;
                                 } else if (gc + 3 < p.N) {
                                     *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(p.c_direct) + at) =
-                                        make_uint2(epi_out16(v[0], p.epi.out_type) |
-                                                       (epi_out16(v[1], p.epi.out_type) << 16),
-                                                   epi_out16(v[2], p.epi.out_type) |
-                                                       (epi_out16(v[3], p.epi.out_type) << 16));
+                                        make_uint2(epi_out16(v.x, p.epi.out_type) |
+                                                       (epi_out16(v.y, p.epi.out_type) << 16),
+                                                   epi_out16(v.z, p.epi.out_type) |
+                                                       (epi_out16(v.w, p.epi.out_type) << 16));
                                 } else {
+                                    const float vv[3] = {v.x, v.y, v.z};
 #pragma unroll
                                     for (int k = 0; k < 3; ++k)
                                         if (gc + k < p.N)
-                                            epi_store(p.c_direct, at + k, v[k], p.epi.out_type);
+                                            epi_store(p.c_direct, at + k, vv[k], p.epi.out_type);
                                 }
                             } else {
                                 float *dst = static_cast<float *>(p.c_direct) + at;
