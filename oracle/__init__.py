@@ -284,3 +284,58 @@ def epilogue_f64(acc: np.ndarray, alpha: float = 1.0, bias=None, activation: str
         b = np.asarray(bias, dtype=np.float64)
         v = v + (b[..., None, :] if v.ndim == 3 and b.ndim == 2 else b)
     return activation_f64(v, activation, slope)
+
+
+# ------------------------------------------------------------------ row sum and GEMV
+
+ELEM_TYPES = ("f32", "f16", "bf16")
+
+
+def elements_f64(buf, elem: str) -> np.ndarray:
+    """A flat buffer of f32, f16 or bf16 values (numpy array or CPU torch
+    tensor, or raw bit patterns for the 16-bit types) as fp64, exactly: f32
+    and f16 by numpy's conversions, bf16 as the upper half of a binary32."""
+    if hasattr(buf, "detach"):
+        t = buf.detach().contiguous().reshape(-1)
+        import torch
+        if elem == "f32":
+            buf = t.view(torch.int32).numpy().view(np.float32)
+        else:
+            buf = t.view(torch.int16).numpy().view(np.uint16)
+    a = np.ascontiguousarray(buf).reshape(-1)
+    if elem == "f32":
+        return a.view(np.float32).astype(np.float64) if a.dtype != np.float32 else a.astype(np.float64)
+    bits = a.view(np.uint16) if a.dtype != np.uint16 else a
+    if elem == "f16":
+        return bits.view(np.float16).astype(np.float64)
+    if elem == "bf16":
+        return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    raise ValueError(f"unknown element type {elem!r}")
+
+
+def rowsum_f64(X, R: int, C: int, row_stride: int, col_stride: int, elem: str = "f16") -> np.ndarray:
+    """The tiled row sum of "A Dumb Triton Runtime Error" ("The kernel
+    itself"): out[r] = sum over c < C of x[r * row_stride + c * col_stride],
+    every element widened exactly and the row summed with ``math.fsum`` (the
+    correctly rounded fp64 sum of the exact values).  The page's tiles and
+    masks (out-of-range lanes read 0, the additive identity -- section "Step 2")
+    do not change this value; the tests check that separately."""
+    x = elements_f64(X, elem)
+    out = np.empty(R, dtype=np.float64)
+    cols = np.arange(C, dtype=np.int64) * int(col_stride)
+    for r in range(R):
+        idx = r * int(row_stride) + cols
+        if C and (idx.min() < 0 or idx.max() >= x.size):
+            raise ValueError("the strided view reaches outside X")
+        out[r] = math.fsum(x[idx].tolist()) if C else 0.0
+    return out
+
+
+def gemv_f64(A, x, M: int, K: int, lda: int | None = None, incx: int = 1) -> np.ndarray:
+    """y = A . x in fp64 (f16 A: M rows of K, row stride lda; f16 x: K values
+    incx apart): the GEMM oracle with N = 1 on x gathered into a column."""
+    xs = _as_u16(x).reshape(-1)
+    if K and (K - 1) * int(incx) >= xs.size:
+        raise ValueError("x is shorter than K and incx require")
+    col = np.ascontiguousarray(xs[: (K - 1) * int(incx) + 1: int(incx)] if K else xs[:0])
+    return gemm_f64(A, col, M, 1, K, lda=lda, ldb=1)[:, 0]
