@@ -328,6 +328,64 @@ def run_grouped(args, rank, local_rank, world):
     return result
 
 
+def run_rows(args, rank, local_rank, world):
+    """A row-sum or GEMV workload: one step is one call over the whole matrix;
+    the metric counts one add (row sum) or multiply-add (GEMV) per element,
+    the roofline is HBM-bound: every element read once."""
+    import torch
+    from tiled_staged_matmul_gb300 import binding, synthetic
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = synthetic.ROW_WORKLOADS[args.workload]
+    X_h, x_h = w.operands()
+    X = X_h.to(dev)
+    x = x_h.to(dev) if x_h is not None else None
+    out = torch.empty(w.R, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    working_set = w.algorithmic_bytes
+    flush = working_set < 2 * L2_BYTES
+    scrub = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    sweep = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    sink = torch.empty(1, dtype=torch.float32, device=dev) if flush else None
+
+    def flush_l2():
+        scrub.zero_()
+        torch.sum(sweep, dim=0, keepdim=True, out=sink)
+
+    def call():
+        if w.kind == "gemv":
+            binding.check(binding.gemv_f16_f32acc(X.data_ptr(), x.data_ptr(), out.data_ptr(), w.R,
+                                                  w.C, w.C, 1, stream.cuda_stream))
+        else:
+            binding.check(binding.rowsum_f32acc(X.data_ptr(), w.elem, out.data_ptr(), w.R, w.C, w.C,
+                                                1, stream.cuda_stream))
+
+    per_step_ms, t0, t1, sampler = timed_loop(args, call, flush_l2 if flush else None, stream,
+                                              world, local_rank)
+    ms_local = sum(per_step_ms) / len(per_step_ms)
+    value, ms = replica_throughput(w.flops, ms_local, world, dev)
+    roofline = roofline_of(w.flops, w.algorithmic_bytes, ms_local, recorded_traffic(w.name),
+                           "tsm_row_reduce_kernel")
+    result = {
+        "metric": METRIC, "value": round(value, 4), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.elem, "data": "synthetic",
+        "config": {"workload": w.name, "kind": w.kind, "R": w.R, "C": w.C, "elem": w.elem,
+                   "seed": w.seed, "accumulate": "f32",
+                   "l2": "flushed before every step (write 2xL2, then read 2xL2)" if flush else
+                         f"inputs {working_set / 2**20:.0f} MiB > L2, no flush",
+                   "parallelism": f"replicas x{world}"},
+        "gpu_launches": args.steps,
+        "roofline": roofline,
+        "hbm_gbs": round(w.algorithmic_bytes / (ms_local * 1e-3) / 1e9, 1),
+    }
+    clocks = sampler.summary(t0, t1)
+    result["clocks"] = {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")}
+    return result
+
+
 def run_ours(args, rank, local_rank, world):
     import torch
     from tiled_staged_matmul_gb300 import binding, synthetic
@@ -648,6 +706,8 @@ def main(argv=None):
     from tiled_staged_matmul_gb300 import synthetic
     if args.workload in synthetic.GROUPED_WORKLOADS:
         result = run_grouped(args, rank, local_rank, world)
+    elif args.workload in synthetic.ROW_WORKLOADS:
+        result = run_rows(args, rank, local_rank, world)
     else:
         result = run_ours(args, rank, local_rank, world)
     if rank == 0:

@@ -277,6 +277,33 @@ gemm_status_t gemm_f16_grouped_fused(const uint16_t *A, const uint16_t *B, void 
                                      const gemm_epilogue_t *epi, const gemm_options_t *opts,
                                      gemm_stream_t stream);
 
+/* The tiled row sum of "A Dumb Triton Runtime Error" (section "The kernel
+ * itself"): for r < R,
+ *     out[r] = sum over c < C of X[r * row_stride + c * col_stride],
+ * every element widened to f32 and the sum accumulated in f32.
+ *   X      device, elements of type elem_type (GEMM_OUT_F32, GEMM_OUT_F16 or
+ *          GEMM_OUT_BF16 -- the page's input may be any of the three) at
+ *          their natural alignment; strides in elements, row_stride >= 0,
+ *          col_stride >= 1 (any view of a tensor: no copy is made)
+ *   out    device, R f32 values, written, never read; must not overlap X
+ * Lanes past the end of a row contribute 0, the additive identity (the
+ * page's "Step 2" and its -inf padding trap), and the lanes' partial sums
+ * are combined by a fixed-order tree on the chip, not by atomics onto out
+ * (the page's closing argument), so a call is bitwise reproducible.  C == 0
+ * writes zeros; R == 0 queues nothing.  Errors as for gemm_f16_f32acc. */
+gemm_status_t rowsum_f32acc(const void *X, int32_t elem_type, float *out, int64_t R, int64_t C,
+                            int64_t row_stride, int64_t col_stride, gemm_stream_t stream);
+
+/* y = A . x, the product with N = 1, by the row-sum kernels (each element of
+ * a row of A times the matching element of x):
+ *   A  device, M rows of K f16 values, row stride lda >= K
+ *   x  device, K f16 values incx >= 1 apart
+ *   y  device, M f32 values, written; must not overlap A or x
+ * f32 accumulation, fixed-order reduce as rowsum_f32acc.  K == 0 writes
+ * zeros. */
+gemm_status_t gemv_f16_f32acc(const uint16_t *A, const uint16_t *x, float *y, int64_t M, int64_t K,
+                              int64_t lda, int64_t incx, gemm_stream_t stream);
+
 /* The plan the library would use, computed on the host only (no GPU is
  * touched).  num_sms is the SM count to plan for (0 = the current device's).
  * This is the analogue of the pages' footprint check and K_TILE choice

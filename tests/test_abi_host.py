@@ -271,3 +271,20 @@ def test_epilogue_host_checks(b):
     # nothing to do
     assert b.gemm_f16_fused(A0, B0, C0, 0, 4, 4, 8, 8, 8, 0, 0, 0, 1, b.epilogue(activation="gelu"),
                             None, 0) == b.GEMM_OK
+
+
+def test_rowsum_and_gemv_host_checks(b):
+    X0, O0 = 0x7f0040000000, 0x7f0050000000
+    bad = lambda st: b.gemm_status_string(st)
+    assert bad(b.rowsum_f32acc(X0, 7, O0, 4, 4, 4, 1, 0)) == "GEMM_ERR_INVALID_VALUE"   # element type
+    assert bad(b.rowsum_f32acc(X0, "f32", O0, -1, 4, 4, 1, 0)) == "GEMM_ERR_INVALID_VALUE"
+    assert bad(b.rowsum_f32acc(X0, "f32", O0, 4, 4, -4, 1, 0)) == "GEMM_ERR_INVALID_VALUE"
+    assert bad(b.rowsum_f32acc(X0, "f32", O0, 4, 4, 4, 0, 0)) == "GEMM_ERR_INVALID_VALUE"
+    assert bad(b.rowsum_f32acc(X0 + 2, "f32", O0, 4, 4, 4, 1, 0)) == "GEMM_ERR_MISALIGNED"
+    assert bad(b.rowsum_f32acc(X0 + 1, "bf16", O0, 4, 4, 4, 1, 0)) == "GEMM_ERR_MISALIGNED"
+    assert bad(b.rowsum_f32acc(X0, "f16", X0 + 8, 4, 4, 4, 1, 0)) == "GEMM_ERR_ALIAS"
+    assert b.rowsum_f32acc(X0, "f16", O0, 0, 4, 4, 1, 0) == b.GEMM_OK
+    assert bad(b.gemv_f16_f32acc(X0, O0, O0 + 64, 4, 8, 4, 1, 0)) == "GEMM_ERR_INVALID_VALUE"  # lda < K
+    assert bad(b.gemv_f16_f32acc(X0, O0, X0 + 8, 4, 8, 8, 1, 0)) == "GEMM_ERR_ALIAS"
+    assert bad(b.gemv_f16_f32acc(X0, O0 + 1, O0 + 64, 4, 8, 8, 1, 0)) == "GEMM_ERR_MISALIGNED"
+    assert b.gemv_f16_f32acc(X0, O0, O0 + 64, 0, 8, 8, 1, 0) == b.GEMM_OK

@@ -114,6 +114,10 @@ def _load() -> ctypes.CDLL:
     lib.gemm_f16_grouped_fused.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, i64,
                                            i64, i64, ctypes.POINTER(GemmEpilogue),
                                            ctypes.POINTER(GemmOptions), vp]
+    lib.rowsum_f32acc.restype = ctypes.c_int
+    lib.rowsum_f32acc.argtypes = [vp, i32, vp, i64, i64, i64, i64, vp]
+    lib.gemv_f16_f32acc.restype = ctypes.c_int
+    lib.gemv_f16_f32acc.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp]
     lib.gemm_f16_f32acc_splitk_noalloc.restype = ctypes.c_int
     lib.gemm_f16_f32acc_splitk_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64,
                                                    i32, vp]
@@ -177,6 +181,15 @@ def gemm_f16_grouped_fused(A, B, C, group_rows, groups, M, N, K, lda, ldb, ldc, 
     o = ctypes.byref(opts) if opts is not None else None
     return _lib.gemm_f16_grouped_fused(A, B, C, group_rows, groups, M, N, K, lda, ldb, ldc, strideA,
                                        strideB, strideC, e, o, stream)
+
+
+def rowsum_f32acc(X, elem_type, out, R, C, row_stride, col_stride, stream=0) -> int:
+    return _lib.rowsum_f32acc(X, OUT_TYPES.get(elem_type, elem_type), out, R, C, row_stride,
+                              col_stride, stream)
+
+
+def gemv_f16_f32acc(A, x, y, M, K, lda, incx=1, stream=0) -> int:
+    return _lib.gemv_f16_f32acc(A, x, y, M, K, lda, incx, stream)
 
 
 def gemm_f16_f32acc_splitk_noalloc(A, B, C, M, N, K, lda, ldb, ldc, split_k=0, stream=0) -> int:
@@ -329,6 +342,42 @@ def grouped_gemm(A, B, group_rows, out=None, *, alpha=1.0, bias=None, activation
                                 A.stride(0), B.stride(0), out.stride(0), epi, opts,
                                 _stream_handle(stream))
     check(st)
+    return out
+
+
+def rowsum(X, out=None, *, stream=None):
+    """Row sums of a 2-D CUDA tensor (f32, f16 or bf16; any strides): an f32
+    tensor of X.shape[0] values, summed in f32 in a fixed order."""
+    import torch
+    names = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16"}
+    if X.dtype not in names or X.dim() != 2 or not X.is_cuda:
+        raise ValueError("X must be a 2-D CUDA tensor of float32, float16 or bfloat16")
+    R, C = X.shape
+    if out is None:
+        out = torch.empty(R, dtype=torch.float32, device=X.device)
+    if out.dtype != torch.float32 or out.numel() != R or (R and out.stride(0) != 1):
+        raise ValueError("out must be a contiguous float32 tensor of X.shape[0] values")
+    check(rowsum_f32acc(X.data_ptr(), names[X.dtype], out.data_ptr(), R, C, X.stride(0),
+                        X.stride(1), _stream_handle(stream)))
+    return out
+
+
+def gemv(A, x, out=None, *, stream=None):
+    """``A @ x`` for an f16 CUDA matrix A (unit last stride) and f16 vector x
+    (any stride): an f32 vector."""
+    import torch
+    if A.dtype != torch.float16 or x.dtype != torch.float16 or A.dim() != 2 or x.dim() != 1:
+        raise ValueError("A must be a 2-D and x a 1-D torch.float16 CUDA tensor")
+    M, K = A.shape
+    if x.numel() != K:
+        raise ValueError("x must hold A.shape[1] values")
+    if K and A.stride(1) != 1:
+        raise ValueError("A must have a unit last stride")
+    if out is None:
+        out = torch.empty(M, dtype=torch.float32, device=A.device)
+    check(gemv_f16_f32acc(A.data_ptr(), x.data_ptr(), out.data_ptr(), M, K,
+                          A.stride(0) if M > 1 else max(K, 1), x.stride(0) if K > 1 else 1,
+                          _stream_handle(stream)))
     return out
 
 

@@ -1,7 +1,7 @@
 """Build ``libtsm_gemm.so`` in-tree with nvcc for sm_103a only.
 
-Two translation units (kernels, host API) compile in parallel; the kernel
-unit is compiled with ``-Xptxas -v`` and the build fails if ptxas reports any
+Three translation units (the GEMM kernels, the row-reduction kernels, the
+host API) compile in parallel; the kernel units are compiled with ``-Xptxas -v`` and the build fails if ptxas reports any
 spill stores or loads (only ptxas's printed summary is read).
 """
 from __future__ import annotations
@@ -21,7 +21,7 @@ LIB_NAME = "libtsm_gemm.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
 PTXAS_LOG = os.path.join(BUILD_DIR, "ptxas.log")
 
-SOURCES = ["gemm_kernels.cu", "gemm_api.cu"]
+SOURCES = ["gemm_kernels.cu", "rowsum_kernels.cu", "gemm_api.cu"]
 HEADERS = ["gemm_internal.h", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -73,10 +73,10 @@ def build(force: bool = False, quiet: bool = True) -> str:
     objs = [os.path.join(BUILD_DIR, os.path.splitext(s)[0] + ".o") for s in SOURCES]
     with ThreadPoolExecutor(len(SOURCES)) as ex:
         logs = list(ex.map(lambda a: _compile(*a),
-                           [(s, o, s == "gemm_kernels.cu") for s, o in zip(SOURCES, objs)]))
+                           [(s, o, s.endswith("_kernels.cu")) for s, o in zip(SOURCES, objs)]))
     with open(PTXAS_LOG, "w") as f:
-        f.write(logs[0])
-    check_spills(logs[0])
+        f.write(logs[0] + logs[1])
+    check_spills(logs[0] + logs[1])
     tmp = LIB_PATH + f".tmp{os.getpid()}"
     r = subprocess.run([_nvcc(), *ARCH, "-shared", "-o", tmp, *objs],
                        capture_output=True, text=True)

@@ -835,6 +835,148 @@ gemm_status_t gemm_f16_f32acc_opts(const uint16_t *A, const uint16_t *B, float *
 namespace tsm {
 namespace {
 
+// A row reduction (rowsum_kernels.cu): the launch shape from (R, C) and the
+// layout alone, so that the summation order -- and the result -- is the same
+// on every call.  16-byte vector loads when the rows are contiguous and
+// 16-byte aligned; each lane takes at least 32 chunks (or elements) of a
+// row where the row is long enough; rows too few to fill the GPU are cut
+// into segments whose partial sums a second kernel adds in order.
+gemm_status_t row_reduce(const void *X, int elem, int64_t R, int64_t C, int64_t row_stride,
+                         int64_t col_stride, const uint16_t *xv, int64_t incx, float *out,
+                         cudaStream_t stream)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return fail_cuda(e, "cudaGetDevice");
+    DeviceState *ds = nullptr;
+    gemm_status_t st = device_state(dev, &ds);
+    if (st != GEMM_OK)
+        return st;
+    const int eb = elem == kOutF32 ? 4 : 2;
+    const int64_t V = 16 / eb;
+    const int64_t span = C > 0 ? ((R - 1) * row_stride + (C - 1) * col_stride + 1) * eb : 0;
+    if (C > 0 && (st = check_device_pointer(X, span, dev, xv ? "A" : "X")) != GEMM_OK)
+        return st;
+    if (xv && C > 0 && (st = check_device_pointer(xv, ((C - 1) * incx + 1) * 2, dev, "x")) != GEMM_OK)
+        return st;
+    if ((st = check_device_pointer(out, R * 4, dev, xv ? "y" : "out")) != GEMM_OK)
+        return st;
+
+    bool vec = C >= V && col_stride == 1 && !(reinterpret_cast<uintptr_t>(X) & 15u) &&
+               (R == 1 || (row_stride * eb) % 16 == 0);
+    if (xv)
+        vec = vec && incx == 1 && !(reinterpret_cast<uintptr_t>(xv) & 15u);
+    const int64_t units = vec ? C / V : C;  // per row
+    int tpr = 1;
+    while (tpr < 32 && int64_t(tpr) * 32 <= units)
+        tpr *= 2;
+    const int64_t per_block = 8 * (32 / tpr);  // workers in a block of 8 warps
+    const int64_t resident = int64_t(ds->sms) * row_reduce_blocks_per_sm(elem, vec, xv != nullptr);
+    const int64_t max_workers = resident * per_block;  // workers that run at once
+    int64_t segs = 1;
+    if (R < max_workers && C > 0)
+        segs = std::max<int64_t>(1, std::min<int64_t>((max_workers + R - 1) / R,
+                                                      std::min<int64_t>(units / (16 * tpr), 65536)));
+    int64_t seg = C > 0 ? (C + segs - 1) / segs : 0;
+    if (vec)
+        seg = (seg + V - 1) / V * V;
+    if (C > 0)
+        segs = (C + seg - 1) / seg;
+    // As many workers as give every one the same number of items: the items
+    // in `rounds` even passes, not a last pass half empty.
+    const int64_t items = R * segs;
+    const int64_t rounds = (items + max_workers - 1) / max_workers;
+    const int64_t want = (items + rounds - 1) / rounds;
+    const int grid = int(std::max<int64_t>(1, (want + per_block - 1) / per_block));
+
+    RowReduceParams p = {};
+    p.X = X;
+    p.row_stride = row_stride;
+    p.col_stride = col_stride;
+    p.xv = xv;
+    p.incx = incx;
+    p.out = out;
+    p.R = R;
+    p.C = C;
+    p.seg = std::max<int64_t>(seg, 1);
+    p.segs = int32_t(segs);
+    p.tpr = tpr;
+    void *ws = nullptr;
+    if (segs > 1) {
+        if ((e = cudaMallocFromPoolAsync(&ws, size_t(R * segs * 4), ds->pool, stream)) != cudaSuccess)
+            return fail_cuda(e, "row-reduction partials");
+        p.partial = static_cast<float *>(ws);
+    }
+    if ((e = launch_row_reduce(p, elem, vec, xv != nullptr, grid, stream)) != cudaSuccess)
+        st = fail_cuda(e, "row-reduction launch");
+    if (st == GEMM_OK && segs > 1 &&
+        (e = launch_row_partials(p.partial, out, R, int32_t(segs),
+                                 int(std::min<int64_t>((R + 7) / 8, int64_t(ds->sms) * 8)), stream)) !=
+            cudaSuccess)
+        st = fail_cuda(e, "row-partials launch");
+    if (ws)
+        cudaFreeAsync(ws, stream);
+    return st;
+}
+
+}  // namespace
+}  // namespace tsm
+
+extern "C" {
+
+gemm_status_t rowsum_f32acc(const void *X, int32_t elem_type, float *out, int64_t R, int64_t C,
+                            int64_t row_stride, int64_t col_stride, gemm_stream_t stream)
+{
+    g_last_error.clear();
+    if (elem_type != GEMM_OUT_F32 && elem_type != GEMM_OUT_F16 && elem_type != GEMM_OUT_BF16)
+        return fail(GEMM_ERR_INVALID_VALUE, "unknown element type %d", elem_type);
+    if (R < 0 || C < 0 || R > (int64_t(1) << 40) || C > (int64_t(1) << 40))
+        return fail(GEMM_ERR_INVALID_VALUE, "bad size: R=%lld C=%lld", (long long)R, (long long)C);
+    if (R == 0)
+        return GEMM_OK;
+    if (!out || (C > 0 && !X))
+        return fail(GEMM_ERR_INVALID_VALUE, "X or out is NULL");
+    if (row_stride < 0 || (C > 1 && col_stride < 1))
+        return fail(GEMM_ERR_INVALID_VALUE, "row_stride must be >= 0 and col_stride >= 1");
+    const int eb = elem_type == GEMM_OUT_F32 ? 4 : 2;
+    if ((reinterpret_cast<uintptr_t>(X) & uintptr_t(eb - 1)) || (reinterpret_cast<uintptr_t>(out) & 3u))
+        return fail(GEMM_ERR_MISALIGNED, "X and out must sit at their elements' natural alignment");
+    const int64_t span = C > 0 ? ((R - 1) * row_stride + (C - 1) * col_stride + 1) * eb : 0;
+    if (overlaps(out, R * 4, X, span))
+        return fail(GEMM_ERR_ALIAS, "out overlaps X");
+    return row_reduce(X, elem_type, R, C, row_stride, C > 1 ? col_stride : 1, nullptr, 0, out,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemv_f16_f32acc(const uint16_t *A, const uint16_t *x, float *y, int64_t M, int64_t K,
+                              int64_t lda, int64_t incx, gemm_stream_t stream)
+{
+    g_last_error.clear();
+    if (M < 0 || K < 0 || M > (int64_t(1) << 40) || K > (int64_t(1) << 40))
+        return fail(GEMM_ERR_INVALID_VALUE, "bad size: M=%lld K=%lld", (long long)M, (long long)K);
+    if (M == 0)
+        return GEMM_OK;
+    if (!y || (K > 0 && (!A || !x)))
+        return fail(GEMM_ERR_INVALID_VALUE, "A, x or y is NULL");
+    if (lda < K || (K > 1 && incx < 1))
+        return fail(GEMM_ERR_INVALID_VALUE, "lda must be >= K and incx >= 1");
+    if ((reinterpret_cast<uintptr_t>(A) & 1u) || (reinterpret_cast<uintptr_t>(x) & 1u) ||
+        (reinterpret_cast<uintptr_t>(y) & 3u))
+        return fail(GEMM_ERR_MISALIGNED, "A and x must be 2-byte and y 4-byte aligned");
+    const int64_t spanA = K > 0 ? ((M - 1) * lda + K) * 2 : 0;
+    const int64_t spanx = K > 0 ? ((K - 1) * incx + 1) * 2 : 0;
+    if (overlaps(y, M * 4, A, spanA) || overlaps(y, M * 4, x, spanx))
+        return fail(GEMM_ERR_ALIAS, "y overlaps A or x");
+    return row_reduce(A, GEMM_OUT_F16, M, K, lda, 1, x, K > 1 ? incx : 1, y,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"
+
+namespace tsm {
+namespace {
+
 // The public epilogue description, checked, as the kernels' Epilogue.
 gemm_status_t epilogue_of(const gemm_epilogue_t *e, Epilogue *out)
 {

@@ -154,4 +154,25 @@ cudaError_t launch_zero_fill(void *C, int32_t M, int32_t N, int32_t batch, int64
                              int grid, cudaStream_t stream);
 cudaError_t device_status_word(uint32_t **ptr);
 
+// Row reductions (rowsum_kernels.cu): the tiled row sum and the GEMV.
+struct RowReduceParams {
+    const void *X;        // element type per the launch (f32, f16, bf16; f16 for the GEMV)
+    int64_t row_stride;   // elements
+    int64_t col_stride;   // elements (1 on the vector path)
+    const uint16_t *xv;   // GEMV: x (f16), incx apart; else null
+    int64_t incx;
+    float *out;           // R results
+    float *partial;       // R * segs partial sums when segs > 1
+    int64_t R, C;
+    int64_t seg;          // columns per item (a multiple of 16 bytes of elements on the vector path)
+    int32_t segs;         // items per row
+    int32_t tpr;          // lanes per worker: 1, 2, 4, ..., 32
+};
+cudaError_t launch_row_reduce(const RowReduceParams &p, int elem, bool vec, bool gemv, int grid,
+                              cudaStream_t stream);
+// Blocks of 256 threads of that row-reduction kernel one SM holds at once.
+int row_reduce_blocks_per_sm(int elem, bool vec, bool gemv);
+cudaError_t launch_row_partials(const float *partial, float *out, int64_t R, int32_t segs, int grid,
+                                cudaStream_t stream);
+
 }  // namespace tsm

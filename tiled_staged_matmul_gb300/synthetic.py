@@ -186,3 +186,50 @@ GROUPED_WORKLOADS = {
                         "normal_invsqrtk", 2001),
     )
 }
+
+
+# ------------------------------------------------------------------ row reductions
+
+@dataclass(frozen=True)
+class RowReduceWorkload:
+    """A row sum (out[r] = sum_c x[r, c]) of an R x C matrix of `elem`
+    values, or a GEMV (y = A x, A R x C f16) -- memory-bound: every element is
+    read once.  Values U[-1, 1) drawn like the GEMM operands."""
+    name: str
+    kind: str   # "rowsum" or "gemv"
+    R: int
+    C: int
+    elem: str   # "f32", "f16" or "bf16" (the GEMV is f16)
+    seed: int
+
+    @property
+    def flops(self) -> int:
+        return (2 if self.kind == "gemv" else 1) * self.R * self.C
+
+    @property
+    def algorithmic_bytes(self) -> int:
+        eb = 4 if self.elem == "f32" else 2
+        return self.R * self.C * eb + 4 * self.R + (2 * self.C if self.kind == "gemv" else 0)
+
+    def operands(self):
+        """(X or A as an R x C CPU tensor, x or None)."""
+        gen = torch.Generator().manual_seed(int(self.seed))
+        dt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[self.elem]
+        X = (torch.rand((self.R, self.C), generator=gen, dtype=torch.float32) * 2.0 - 1.0).to(dt)
+        x = None
+        if self.kind == "gemv":
+            x = (torch.rand(self.C, generator=gen, dtype=torch.float32) * 2.0 - 1.0).to(torch.float16)
+        return X, x
+
+
+# Sizes above the L2 (every element comes from HBM): many medium rows, a few
+# very long rows (cut into segments), and the f16 GEMV.
+ROW_WORKLOADS = {
+    w.name: w
+    for w in (
+        RowReduceWorkload("rowsum_8192x32768_f16", "rowsum", 8192, 32768, "f16", 3000),
+        RowReduceWorkload("rowsum_4x33554432_f32", "rowsum", 4, 33554432, "f32", 3001),
+        RowReduceWorkload("rowsum_262144x1024_bf16", "rowsum", 262144, 1024, "bf16", 3002),
+        RowReduceWorkload("gemv_16384x16384_f16", "gemv", 16384, 16384, "f16", 3003),
+    )
+}
