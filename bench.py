@@ -35,6 +35,8 @@ DEFAULT_WORKLOAD = "gemm_8192x8192x8192_normal_invsqrtk"
 METRIC = "GEMM TFLOP/s (f16 in, f32 acc) and % of GB300 dense-f16 / HBM roofline"
 L2_BYTES = 129 * 1024 * 1024
 KERNEL_SOURCES = ["tiled_staged_matmul_gb300/csrc/gemm_kernels.cu",
+                  "tiled_staged_matmul_gb300/csrc/rowsum_kernels.cu",
+                  "tiled_staged_matmul_gb300/csrc/gemm_internal.h",
                   "tiled_staged_matmul_gb300/csrc/ptx.cuh"]
 
 
