@@ -114,11 +114,12 @@ typedef struct gemm_options {
                               count are bitwise the same. */
     int32_t l2_prefetch; /* 0 or 1: off; 2: on -- each unit first asks L2 for its whole K
                             range of A and B (measured slower on GB300, kept for study) */
-    int32_t split_tail; /* 0: off; 1: when there are more tiles than slots and the last wave is
-                           at most half full, split each of its tiles into K ranges summed in
-                           the kernel so that wave keeps every slot busy.  Measured on GB300 at
-                           4096^3 and 8192^3: no gain (only two-way splits fit, and storing and
-                           summing the partials costs about as much as half a tile saves). */
+    int32_t split_tail; /* when there are more tiles than slots and the last wave is at most half
+                           full, split each of its tiles into K ranges summed in the kernel so
+                           that wave keeps every slot busy.  0: the planner decides -- only when
+                           the time taken off the last wave clearly outweighs storing and summing
+                           the partials (about 6 us); 1: whenever it applies; 2: never.  Never
+                           for batches, grouped calls or with splitk_reduce = 1. */
     uint64_t *trace;    /* NULL, or a device buffer of grid x 8 uint64 (grid from gemm_plan):
                            per CTA, %globaltimer stamps (ns) of kernel entry, setup done,
                            first k-block landed, last MMA issued, last accumulator ready,
@@ -147,7 +148,7 @@ typedef struct gemm_plan_info {
     int64_t workspace_bytes; /* split-K partials, plus arrival counters and a launch tag
                                 when summed in-kernel (0 when split_k == 1) */
     int32_t fused_reduce; /* 1: split partials are summed inside the GEMM kernel */
-    int32_t tail_tiles;   /* with gemm_options_t.split_tail: the tiles of the partial last wave,
+    int32_t tail_tiles;   /* with a split tail: the tiles of the partial last wave,
                              each split into tail_split K ranges summed in the kernel; 0: none */
     int32_t tail_split;
 } gemm_plan_info_t;

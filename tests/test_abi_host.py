@@ -230,8 +230,7 @@ def test_more_units_than_clusters_never_fuses(b):
 
 def test_split_tail_for_partial_last_waves(b):
     on = b.GemmOptions(0, 0, 0, 0, 0, 0, 0, 1)
-    # off unless asked for
-    assert b.gemm_plan(8192, 8192, 8192, 1, None, SMS)["tail_split"] == 0
+    never = b.GemmOptions(0, 0, 0, 0, 0, 0, 0, 2)
     # 1024 pair tiles on 76 clusters: 13 full waves, 36 tiles left, split 2 ways
     p = b.gemm_plan(8192, 8192, 8192, 1, on, SMS)
     assert (p["tail_tiles"], p["tail_split"]) == (36, 2)
@@ -239,10 +238,21 @@ def test_split_tail_for_partial_last_waves(b):
     # a last wave more than half full keeps whole tiles
     p = b.gemm_plan(6144, 6144, 6144, 1, on, SMS)
     assert p["tail_split"] == 0 and not p["fused_reduce"]
-    # never with the separate-reduce option, nor for batches
+    # never with the separate-reduce option, nor for batches, nor when asked not to
     off = b.GemmOptions(0, 0, 0, 0, 0, 1, 0, 1)
     assert b.gemm_plan(8192, 8192, 8192, 1, off, SMS)["tail_split"] == 0
     assert b.gemm_plan(4096, 4096, 4096, 2, on, SMS)["tail_split"] == 0
+    assert b.gemm_plan(4096, 4096, 4096, 1, never, SMS)["tail_split"] == 0
+
+
+def test_split_tail_by_default_only_when_it_pays(b):
+    # the planner's choice (options absent or split_tail 0): long enough tiles split ...
+    assert b.gemm_plan(4096, 4096, 4096, 1, None, SMS)["tail_split"] == 2
+    assert b.gemm_plan(2304, 2304, 8192, 1, None, SMS)["tail_split"] == 15
+    assert b.gemm_plan(6144, 4096, 4096, 1, b.GemmOptions(), SMS)["tail_split"] == 16
+    # ... short ones stay whole (storing and summing the partials would cost more)
+    assert b.gemm_plan(4096, 4096, 1024, 1, None, SMS)["tail_split"] == 0
+    assert b.gemm_plan(8192, 8192, 2048, 1, None, SMS)["tail_split"] == 0
 
 
 def test_noalloc_entry_rejects_what_it_cannot_repack(b):

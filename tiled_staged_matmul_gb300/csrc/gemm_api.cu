@@ -349,13 +349,14 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const ge
             return 1;
         return int(std::max<int64_t>(1, std::min<int64_t>(slots_of(tm) / tiles, k_blocks / 4)));
     };
-    // Split tail (opt-in, gemm_options_t.split_tail): with more tiles than
-    // slots, the R tiles of a partial last wave are each split into
+    // Split tail (gemm_options_t.split_tail: 0 auto, 1 on, 2 off): with more
+    // tiles than slots, the R tiles of a partial last wave are each split into
     // tail_split K ranges (summed in the kernel), so the last wave keeps every
     // slot busy for a fraction of a tile.  Returns that split (0: none).
     auto tail_split_of = [&](int tm, int tn) -> int {
+        const int mode = o ? o->split_tail : 0;
         const int req_r0 = o ? o->splitk_reduce : 0;
-        if (!o || o->split_tail != 1 || req_s != 0 || req_r0 == 1 || batch != 1 || K == 0)
+        if (mode == 2 || req_s != 0 || req_r0 == 1 || batch != 1 || K == 0)
             return 0;
         const int64_t slots = slots_of(tm), tiles = tiles_of(tm, tn);
         const int64_t rem = tiles % slots;
@@ -369,6 +370,18 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const ge
         const SmemBudget b = smem_budget(tm, tn);
         if (rows_per * tn * 4 * st > int64_t(b.stages) * b.stage_bytes || st > 256)
             return 0;
+        if (mode == 0) {
+            // Auto: only when the part of a tile the split takes off the last
+            // wave outweighs storing and summing the partials (about 6 us,
+            // measured), a tile's k-block taking 2 x 128 x tile_n x 64 flops
+            // at ~15 TFLOP/s per SM.  Measured on GB300 (interleaved runs):
+            // +3 % at 4096^3, +7 % at 5120^3, +10 % at 3000 x 5000 x 4096,
+            // x1.95 at 2304 x 2304 x 8192; 4096^2 x 1024 (-12 %) and
+            // 8192^2 x 2048 (-0.5 %) stay whole.
+            const double kb_us = 2.0 * kTileM * tn * kTileK / 15e12 * 1e6;
+            if (double(k_blocks) * kb_us * (1.0 - 1.0 / double(st)) < 6.0)
+                return 0;
+        }
         return int(st);
     };
     // Long K on a small output: the split-K regime.  Pick the tile that moves
@@ -626,7 +639,7 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
         og = *o;
     if (pr.group_rows) {
         og.split_k = 1;
-        og.split_tail = 0;
+        og.split_tail = 2;
     }
     gemm_plan_info_t pl;
     if ((st = make_plan(pr.M, pr.N, pr.K, pr.batch, (o || pr.group_rows) ? &og : nullptr, ds->sms,
