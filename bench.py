@@ -34,10 +34,13 @@ if ROOT not in sys.path:
 DEFAULT_WORKLOAD = "gemm_8192x8192x8192_normal_invsqrtk"
 METRIC = "GEMM TFLOP/s (f16 in, f32 acc) and % of GB300 dense-f16 / HBM roofline"
 L2_BYTES = 129 * 1024 * 1024
+# The kernels and the host code that plans their launches: recorded DRAM
+# traffic is valid only for the exact code that produced it.
 KERNEL_SOURCES = ["tiled_staged_matmul_gb300/csrc/gemm_kernels.cu",
                   "tiled_staged_matmul_gb300/csrc/rowsum_kernels.cu",
                   "tiled_staged_matmul_gb300/csrc/gemm_internal.h",
-                  "tiled_staged_matmul_gb300/csrc/ptx.cuh"]
+                  "tiled_staged_matmul_gb300/csrc/ptx.cuh",
+                  "tiled_staged_matmul_gb300/csrc/gemm_api.cu"]
 
 
 def parse_args(argv=None):
@@ -470,8 +473,10 @@ def run_ours(args, rank, local_rank, world):
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
                    "dist": w.dist, "seed": w.seed, "accumulate": "f32",
                    "tile_m": plan["tile_m"], "tile_n": plan["tile_n"], "split_k": plan["split_k"],
+                   "split_tail": (f"{plan['tail_tiles']} tiles of the last wave split "
+                                  f"{plan['tail_split']} ways" if plan["tail_split"] else "none"),
                    "splitk_sum": ("in-kernel" if plan["fused_reduce"] else "separate kernel")
-                   if plan["split_k"] > 1 else "none",
+                   if plan["split_k"] > 1 or plan["tail_split"] else "none",
                    "stages": plan["stages"], "grid": plan["grid"],
                    "ld": [lda, ldb, ldc],
                    "epilogue": ({"activation": args.act, "bias": bool(args.bias), "out": args.out}
