@@ -474,9 +474,12 @@ def run_ours(args, rank, local_rank, world):
                    "dist": w.dist, "seed": w.seed, "accumulate": "f32",
                    "tile_m": plan["tile_m"], "tile_n": plan["tile_n"], "split_k": plan["split_k"],
                    "split_tail": (f"{plan['tail_tiles']} tiles of the last wave split "
-                                  f"{plan['tail_split']} ways" if plan["tail_split"] else "none"),
+                                  f"{plan['tail_split']} ways "
+                                  + ("in column slices" if plan["tail_narrow"] else "along K")
+                                  if plan["tail_split"] else "none"),
                    "splitk_sum": ("in-kernel" if plan["fused_reduce"] else "separate kernel")
-                   if plan["split_k"] > 1 or plan["tail_split"] else "none",
+                   if plan["split_k"] > 1 or (plan["tail_split"] and not plan["tail_narrow"])
+                   else "none",
                    "stages": plan["stages"], "grid": plan["grid"],
                    "ld": [lda, ldb, ldc],
                    "epilogue": ({"activation": args.act, "bias": bool(args.bias), "out": args.out}

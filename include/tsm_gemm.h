@@ -115,11 +115,15 @@ typedef struct gemm_options {
     int32_t l2_prefetch; /* 0 or 1: off; 2: on -- each unit first asks L2 for its whole K
                             range of A and B (measured slower on GB300, kept for study) */
     int32_t split_tail; /* when there are more tiles than slots and the last wave is at most half
-                           full, split each of its tiles into K ranges summed in the kernel so
-                           that wave keeps every slot busy.  0: the planner decides -- only when
-                           the time taken off the last wave clearly outweighs storing and summing
-                           the partials (about 6 us); 1: whenever it applies; 2: never.  Never
-                           for batches, grouped calls or with splitk_reduce = 1. */
+                           full, spread that wave's tiles over every slot: either split each into
+                           K ranges summed in the kernel, or cut it into column slices (halves or
+                           quarters, at least 64 columns of B per CTA) each computed over all of K,
+                           with no partial sums.  0: the planner decides, comparing the time each
+                           takes off the last wave with its cost -- about 6 us for storing and
+                           summing K-range partials, the narrower tile's lower efficiency for
+                           slices; 1: K ranges whenever they apply (never for batches or with
+                           splitk_reduce = 1); 2: never; 3: column slices whenever they apply.
+                           Never for grouped calls. */
     uint64_t *trace;    /* NULL, or a device buffer of grid x 8 uint64 (grid from gemm_plan):
                            per CTA, %globaltimer stamps (ns) of kernel entry, setup done,
                            first k-block landed, last MMA issued, last accumulator ready,
@@ -148,9 +152,11 @@ typedef struct gemm_plan_info {
     int64_t workspace_bytes; /* split-K partials, plus arrival counters and a launch tag
                                 when summed in-kernel (0 when split_k == 1) */
     int32_t fused_reduce; /* 1: split partials are summed inside the GEMM kernel */
-    int32_t tail_tiles;   /* with a split tail: the tiles of the partial last wave,
-                             each split into tail_split K ranges summed in the kernel; 0: none */
+    int32_t tail_tiles;   /* with a split tail: the tiles of the partial last wave, each split
+                             into tail_split pieces; 0: none */
     int32_t tail_split;
+    int32_t tail_narrow;  /* 1: the pieces are column slices of tile_n / tail_split columns over
+                             all of K; 0: K ranges summed in the kernel */
 } gemm_plan_info_t;
 
 /* C = A . B for one matrix.

@@ -162,10 +162,15 @@ def test_plan_invariants(b, M, N, K):
     assert 1 <= p["split_k"] <= p["k_blocks"]
     tiles = p["tiles_m"] * p["tiles_n"]
     if p["tail_split"]:
-        # split tail: whole tiles for the full waves, the rest split tail_split ways
+        # split tail: whole tiles for the full waves, the rest split tail_split
+        # ways -- K ranges summed in the kernel, or column slices of at least
+        # 64 B columns per CTA with no partial sums
         slots = SMS // (2 if p["tile_m"] == 256 else 1)
-        assert p["split_k"] == 1 and p["fused_reduce"]
+        assert p["split_k"] == 1 and bool(p["fused_reduce"]) != bool(p["tail_narrow"])
         assert p["tail_tiles"] == tiles % slots and p["tail_split"] >= 2
+        if p["tail_narrow"]:
+            b_cols = p["tile_n"] // (2 if p["tile_m"] == 256 else 1)
+            assert p["tail_split"] in (2, 4) and b_cols // p["tail_split"] >= 64
         assert p["units"] == tiles - p["tail_tiles"] + p["tail_tiles"] * p["tail_split"]
         assert p["tail_tiles"] * p["tail_split"] <= slots
     else:
@@ -176,7 +181,9 @@ def test_plan_invariants(b, M, N, K):
         assert p["grid"] == 2 * min(p["units"], SMS // 2)
     ldw = -(-N // 4) * 4
     tile_bytes = p["tile_m"] * p["tile_n"] * 4
-    if p["tail_split"]:
+    if p["tail_narrow"]:
+        assert p["workspace_bytes"] == 0
+    elif p["tail_split"]:
         counters = -(-(p["tail_tiles"] * 4) // 16) * 16 + 16  # + launch tag
         assert p["workspace_bytes"] == p["tail_tiles"] * p["tail_split"] * tile_bytes + counters
     elif p["split_k"] == 1:
@@ -246,13 +253,42 @@ def test_split_tail_for_partial_last_waves(b):
 
 
 def test_split_tail_by_default_only_when_it_pays(b):
-    # the planner's choice (options absent or split_tail 0): long enough tiles split ...
-    assert b.gemm_plan(4096, 4096, 4096, 1, None, SMS)["tail_split"] == 2
-    assert b.gemm_plan(2304, 2304, 8192, 1, None, SMS)["tail_split"] == 15
-    assert b.gemm_plan(6144, 4096, 4096, 1, b.GemmOptions(), SMS)["tail_split"] == 16
-    # ... short ones stay whole (storing and summing the partials would cost more)
-    assert b.gemm_plan(4096, 4096, 1024, 1, None, SMS)["tail_split"] == 0
-    assert b.gemm_plan(8192, 8192, 2048, 1, None, SMS)["tail_split"] == 0
+    def tail(M, N, K, batch=1, opts=None):
+        p = b.gemm_plan(M, N, K, batch, opts, SMS)
+        return p["tail_split"], "N" if p["tail_narrow"] else ("K" if p["tail_split"] else "-")
+    # the planner's choice (options absent or split_tail 0): long enough tiles
+    # split in K ranges ...
+    assert tail(4096, 4096, 4096) == (2, "K")
+    assert tail(8192, 8192, 8192) == (2, "K")
+    assert tail(2304, 2304, 8192) == (15, "K")
+    assert tail(6144, 4096, 4096, 1, b.GemmOptions()) == (16, "K")
+    # ... short ones in column slices (storing and summing the partials would
+    # cost more than the narrower tiles lose), and batches too
+    assert tail(4096, 4096, 1024) == (2, "N")
+    assert tail(8192, 8192, 2048) == (2, "N")
+    assert tail(8192, 8192, 8192, 3) == (2, "N")
+    # a last wave more than half full stays whole
+    assert tail(6144, 6144, 6144) == (0, "-")
+
+
+def test_column_slice_tail_options(b):
+    narrow = b.GemmOptions(0, 0, 0, 0, 0, 0, 0, 3)
+    kranges = b.GemmOptions(0, 0, 0, 0, 0, 0, 0, 1)
+    # forced either way on 8192^3: 36 tiles left over, halves or two K ranges
+    p = b.gemm_plan(8192, 8192, 8192, 1, narrow, SMS)
+    assert (p["tail_tiles"], p["tail_split"], p["tail_narrow"]) == (36, 2, 1)
+    assert p["units"] == 1024 - 36 + 72 and not p["fused_reduce"] and p["workspace_bytes"] == 0
+    p = b.gemm_plan(8192, 8192, 8192, 1, kranges, SMS)
+    assert (p["tail_tiles"], p["tail_split"], p["tail_narrow"]) == (36, 2, 0)
+    # one CTA per tile: 128 x 256 tiles in quarters when few are left over
+    p = b.gemm_plan(1280, 4096, 256, 1, b.GemmOptions(0, 256, 0, 0, 128, 0, 0, 3), SMS)
+    assert (p["tail_tiles"], p["tail_split"], p["tail_narrow"]) == (8, 4, 1)
+    # a pair tile 128 wide has one 64-column box per CTA: nothing to slice
+    p = b.gemm_plan(2304, 2304, 1024, 1, b.GemmOptions(0, 128, 0, 0, 256, 0, 0, 3), SMS)
+    assert p["tail_split"] == 0
+    # split_tail outside 0..3 is rejected
+    with pytest.raises(b.GemmError):
+        b.gemm_plan(128, 128, 128, 1, b.GemmOptions(0, 0, 0, 0, 0, 0, 0, 4), SMS)
 
 
 def test_noalloc_entry_rejects_what_it_cannot_repack(b):

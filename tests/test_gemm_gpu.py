@@ -117,7 +117,7 @@ def test_in_kernel_and_separate_reduce_agree_bitwise(b, M, N, K, tile_m, tile_n,
     check_tolerance(C_in.numpy(), ref_of(A, B), K)
 
 
-@pytest.mark.parametrize("M,N,K", [(2304, 2304, 1024), (4096, 4096, 512), (2200, 2270, 832)])
+@pytest.mark.parametrize("M,N,K", [(2304, 2304, 1024), (4096, 4096, 1024), (2560, 4096, 1536), (2200, 2270, 832)])
 def test_split_tail(b, M, N, K):
     """Plans whose partial last wave is split across all slots: exact on
     integers, and the same within tolerance as whole tiles on random inputs."""

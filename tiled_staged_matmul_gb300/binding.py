@@ -62,7 +62,7 @@ class GemmPlanInfo(ctypes.Structure):
                 ("group_m", ctypes.c_int32), ("stage_bytes", ctypes.c_int64),
                 ("smem_bytes", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
                 ("fused_reduce", ctypes.c_int32), ("tail_tiles", ctypes.c_int32),
-                ("tail_split", ctypes.c_int32)]
+                ("tail_split", ctypes.c_int32), ("tail_narrow", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}

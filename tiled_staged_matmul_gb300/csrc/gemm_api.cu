@@ -299,15 +299,12 @@ gemm_status_t check_device_pointer(const void *p, int64_t bytes, int dev, const 
 
 int ceil_div(int64_t a, int64_t b) { return int((a + b - 1) / b); }
 
-// Candidate tile shapes with a relative per-SM efficiency (measured on
-// GB300: the 1-CTA 128 x 256 tile keeps the tensor pipe about 72 % busy,
-// bounded by shared-memory bandwidth; a CTA pair halves each SM's B traffic).
+// Candidate tile shapes, in the order ties are broken (a CTA pair per
+// 256-row tile halves each SM's B traffic).
 struct TileChoice {
     int tile_m, tile_n;
-    double eff;
 };
-constexpr TileChoice kChoices[] = {
-    {256, 256, 1.00}, {256, 128, 0.85}, {128, 256, 0.80}, {128, 128, 0.72}, {128, 64, 0.55}};
+constexpr TileChoice kChoices[] = {{256, 256}, {256, 128}, {128, 256}, {128, 128}, {128, 64}};
 
 gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const gemm_options_t *o,
                         int sms, gemm_plan_info_t *pl)
@@ -330,6 +327,8 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const ge
         return fail(GEMM_ERR_INVALID_VALUE, "split_k must be >= 0");
     if (o && (o->splitk_reduce < 0 || o->splitk_reduce > 2))
         return fail(GEMM_ERR_INVALID_VALUE, "splitk_reduce must be 0, 1 or 2");
+    if (o && (o->split_tail < 0 || o->split_tail > 3))
+        return fail(GEMM_ERR_INVALID_VALUE, "split_tail must be 0, 1, 2 or 3");
     const int k_blocks = ceil_div(std::max<int64_t>(K, 1), kTileK);
     const int64_t Mx = std::max<int64_t>(M, 1), Nx = std::max<int64_t>(N, 1);
     const int64_t ldw = (N + 3) / 4 * 4;
@@ -349,40 +348,70 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const ge
             return 1;
         return int(std::max<int64_t>(1, std::min<int64_t>(slots_of(tm) / tiles, k_blocks / 4)));
     };
-    // Split tail (gemm_options_t.split_tail: 0 auto, 1 on, 2 off): with more
-    // tiles than slots, the R tiles of a partial last wave are each split into
-    // tail_split K ranges (summed in the kernel), so the last wave keeps every
-    // slot busy for a fraction of a tile.  Returns that split (0: none).
-    auto tail_split_of = [&](int tm, int tn) -> int {
+    // Tail of a plan with more tiles than slots whose last wave is at most
+    // half full (gemm_options_t.split_tail: 0 auto, 1 K ranges, 2 none,
+    // 3 column slices).  Either each of the R tiles of that wave is split
+    // into `pieces` K ranges summed in the kernel, or it is cut into `pieces`
+    // column slices computed over all of K (no partial sums, any batch).
+    // `frac` is the time of the last wave in whole-tile times.
+    struct Tail {
+        int pieces = 0;
+        bool narrow = false;
+        double frac = 1.0;
+    };
+    // One CTA's time per k-block of a unit `w` columns wide (us): its MMAs at
+    // ~13.1 TFLOP/s per SM, or bringing its A and B boxes into shared memory
+    // at ~87 GB/s per SM, whichever is longer (measured on GB300: 256 x 256
+    // pair tiles run ~15 % over their MMA time, 256 x 128 column slices at
+    // three quarters of a whole tile's time).
+    auto kb_us = [&](int tm, int w) {
+        const double mma = 2.0 * kTileM * w * kTileK / 13.1e12 * 1e6;
+        const double bytes = 2.0 * kTileK * (kTileM + (tm == 2 * kTileM ? w / 2 : w));
+        return std::max(mma, bytes / 87e9 * 1e6);
+    };
+    auto tail_of = [&](int tm, int tn) -> Tail {
         const int mode = o ? o->split_tail : 0;
         const int req_r0 = o ? o->splitk_reduce : 0;
-        if (mode == 2 || req_s != 0 || req_r0 == 1 || batch != 1 || K == 0)
-            return 0;
+        Tail none;
+        if (mode == 2 || req_s != 0 || K == 0)
+            return none;
         const int64_t slots = slots_of(tm), tiles = tiles_of(tm, tn);
         const int64_t rem = tiles % slots;
         if (tiles <= slots || rem == 0)
-            return 0;
-        const int64_t st = std::min<int64_t>(slots / rem, k_blocks / 4);
-        if (st < 2)
-            return 0;
-        const int64_t reducers = st * (tm == 2 * kTileM ? 2 : 1);
-        const int64_t rows_per = (tm + reducers - 1) / reducers;
-        const SmemBudget b = smem_budget(tm, tn);
-        if (rows_per * tn * 4 * st > int64_t(b.stages) * b.stage_bytes || st > 256)
-            return 0;
-        if (mode == 0) {
-            // Auto: only when the part of a tile the split takes off the last
-            // wave outweighs storing and summing the partials (about 6 us,
-            // measured), a tile's k-block taking 2 x 128 x tile_n x 64 flops
-            // at ~15 TFLOP/s per SM.  Measured on GB300 (interleaved runs):
-            // +3 % at 4096^3, +7 % at 5120^3, +10 % at 3000 x 5000 x 4096,
-            // x1.95 at 2304 x 2304 x 8192; 4096^2 x 1024 (-12 %) and
-            // 8192^2 x 2048 (-0.5 %) stay whole.
-            const double kb_us = 2.0 * kTileM * tn * kTileK / 15e12 * 1e6;
-            if (double(k_blocks) * kb_us * (1.0 - 1.0 / double(st)) < 6.0)
-                return 0;
+            return none;
+        const double tile_us = double(k_blocks) * kb_us(tm, tn);
+        Tail ks;  // K ranges: storing and summing the partials costs about 6 us (measured)
+        if (mode != 3 && req_r0 != 1 && batch == 1) {
+            const int64_t st = std::min<int64_t>(slots / rem, k_blocks / 4);
+            const int64_t reducers = st * (tm == 2 * kTileM ? 2 : 1);
+            const int64_t rows_per = (tm + reducers - 1) / reducers;
+            const SmemBudget b = smem_budget(tm, tn);
+            if (st >= 2 && st <= 256 && rows_per * tn * 4 * st <= int64_t(b.stages) * b.stage_bytes)
+                ks = Tail{int(st), false, 1.0 / double(st) + 6.0 / tile_us};
         }
-        return int(st);
+        Tail ns;  // column slices of at least 64 B columns per CTA
+        if (mode != 1) {
+            const int b_cols = tm == 2 * kTileM ? tn / 2 : tn;
+            int n = 1;
+            while (n * 2 <= b_cols / 64 && rem * n * 2 <= slots)
+                n *= 2;
+            if (n >= 2)
+                ns = Tail{n, true, kb_us(tm, tn / n) / kb_us(tm, tn)};
+        }
+        if (mode == 1)
+            return ks;
+        if (mode == 3)
+            return ns;
+        // Auto: the fastest last wave, measured on GB300 in interleaved runs
+        // against whole tiles: K ranges x2.0 at 2304 x 2304 x 8192, +2.6 %
+        // at 8192^3, +6 % at 5120^3; column slices +25 % at 2304 x 2304 x
+        // 1024, +5 % at 4096^2 x 1024, +2 % at 8192^2 x 2048.
+        Tail best = none;
+        if (ks.pieces && ks.frac < best.frac)
+            best = ks;
+        if (ns.pieces && ns.frac < best.frac)
+            best = ns;
+        return best;
     };
     // Long K on a small output: the split-K regime.  Pick the tile that moves
     // the fewest bytes from L2 into shared memory, partials included.
@@ -408,16 +437,20 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const ge
             cost = double(tiles) * sk * ceil_div(k_blocks, sk) * stage +
                    (sk > 1 ? 4.0 * 2.0 * sk * double(M) * ldw * 4 * batch : 0.0);
         } else {
-            // Fewest waves of persistent CTAs, weighted by the per-SM efficiency
-            // of the tile (a wave does tile_n columns of 128 rows on every SM).
-            // A partial last wave split across all slots (see tail_split_of)
-            // costs a fraction of a wave plus the partial sums.
+            // Full waves of persistent CTAs at the tile's time per k-block
+            // (kb_us), and the last wave: whole, or spread over every slot by
+            // the tail that tail_of picks for this tile.  CTA pairs carry a
+            // fixed ~8 us more: measured on GB300 they are 2-8 us slower than
+            // one CTA per tile where both take the same time per k-block
+            // (19.6 against 12.3 us at 1024 x 1024 x 512), and with 8 us this
+            // choice came within 0.4 % (geometric mean) of the fastest tile on
+            // 156 timed shapes.
             const int64_t slots = slots_of(c.tile_m);
-            double waves = double((tiles + slots - 1) / slots);
-            const int st = tail_split_of(c.tile_m, c.tile_n);
-            if (st >= 2)
-                waves = double(tiles / slots) + 1.0 / st + 0.1;
-            cost = waves * c.tile_n / c.eff;
+            const Tail tl = tail_of(c.tile_m, c.tile_n);
+            const double waves = tl.pieces ? double(tiles / slots) + tl.frac
+                                           : double((tiles + slots - 1) / slots);
+            cost = waves * double(k_blocks) * kb_us(c.tile_m, c.tile_n) +
+                   (c.tile_m == 2 * kTileM ? 8.0 : 0.0);
         }
         if (!best || cost < best_cost) {
             best = &c;
@@ -457,23 +490,26 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const ge
                        rows_per * bn * 4 * split <= int64_t(sb.stages) * sb.stage_bytes;
     pl->tail_tiles = 0;
     pl->tail_split = 0;
+    pl->tail_narrow = 0;
     if (split == 1) {
-        const int st = tail_split_of(tm, bn);
-        if (st >= 2) {
+        const Tail tl = tail_of(tm, bn);
+        if (tl.pieces >= 2) {
             pl->tail_tiles = int32_t(tiles % slots_of(tm));
-            pl->tail_split = st;
-            pl->units = tiles - pl->tail_tiles + int64_t(pl->tail_tiles) * st;
+            pl->tail_split = tl.pieces;
+            pl->tail_narrow = tl.narrow ? 1 : 0;
+            pl->units = tiles - pl->tail_tiles + int64_t(pl->tail_tiles) * tl.pieces;
             pl->grid = int(std::min<int64_t>(pl->units, slots_of(tm)) * ctas_per_unit);
-            pl->fused_reduce = 1;
+            pl->fused_reduce = tl.narrow ? 0 : 1;
         }
     }
     // Split partials: in-kernel sums use a compact [split unit][tile_m][tile_n]
     // workspace plus a counter per split tile and a 16-byte launch tag; the
     // reduce kernel reads
     // [batch * split][M][ldw].
-    const int64_t split_tiles = pl->tail_split ? pl->tail_tiles : (split > 1 ? tiles : 0);
-    const int64_t split_units = pl->tail_split ? split_tiles * pl->tail_split : split_tiles * split;
-    if (split == 1 && !pl->tail_split)
+    const bool ktail = pl->tail_split && !pl->tail_narrow;
+    const int64_t split_tiles = ktail ? pl->tail_tiles : (split > 1 ? tiles : 0);
+    const int64_t split_units = ktail ? split_tiles * pl->tail_split : split_tiles * split;
+    if (split == 1 && !ktail)
         pl->workspace_bytes = 0;
     else if (pl->fused_reduce)
         pl->workspace_bytes = split_units * tile_elems_of(tm, bn) * 4 + (split_tiles * 4 + 15) / 16 * 16 + 16;
@@ -718,6 +754,10 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
         const int64_t map_cols = kp.n_tma > 0 ? kp.n_tma : pr.N;  // an unused map still needs extent
         if ((st = encode_out(&map_out, map_cols)) != GEMM_OK)
             return st;
+        if (pl.tail_narrow) {
+            kp.narrow = pl.tail_split;
+            kp.dp_units = int64_t(pl.tiles_m) * pl.tiles_n * pr.batch - pl.tail_tiles;
+        }
         if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, use_epi, map_a, map_b, map_out, map_out, map_out, kp,
                                      pl.grid, stream)) != cudaSuccess)
             return fail_cuda(e, "GEMM kernel launch");
@@ -1332,6 +1372,10 @@ extern "C" gemm_status_t gemm_f16_f32acc_splitk_noalloc(const uint16_t *A, const
         if ((st = encode_3d(&map_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, map_cols, M, 1, ldc,
                             M * ldc, 32, 32, CU_TENSOR_MAP_L2_PROMOTION_NONE, "C")) != GEMM_OK)
             return st;
+        if (pl.tail_narrow) {
+            kp.narrow = pl.tail_split;
+            kp.dp_units = int64_t(pl.tiles_m) * pl.tiles_n - pl.tail_tiles;
+        }
         if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, false, map_a, map_b, map_out, map_out, map_out, kp, pl.grid, stream)) != cudaSuccess)
             return fail_cuda(e, "GEMM kernel launch");
         return GEMM_OK;

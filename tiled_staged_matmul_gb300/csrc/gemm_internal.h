@@ -83,6 +83,11 @@ struct KernelParams {
     // of tile dp_units + j / split_k, and its partial goes to the compact
     // workspace [j][tile_m][tile_n] (through the workspace map).
     int64_t dp_units;
+    // Narrow tail (not with `fused`): units [0, dp_units) are whole tiles,
+    // and each later tile is cut into `narrow` column slices of
+    // tile_n / narrow columns (2 or 4), each a unit of its own over all of K:
+    // the last wave keeps more slots busy without any partial sums.  0: none.
+    int32_t narrow;
     int32_t prefetch_l2;  // 1: the producer first asks L2 for its unit's whole K range
     uint32_t *counters;
     int32_t counter_words;

@@ -87,12 +87,13 @@ struct TileCfg {
 // Instruction descriptor of tcgen05.mma.kind::f16: D f32 (bits 4-5 = 1),
 // A and B f16 (bits 7-9, 10-12 = 0), A K-major (bit 15 = 0), B MN-major
 // (bit 16 = 1: B is row-major K x N, so N is contiguous), N >> 3 in bits
-// 17-22, M >> 4 in bits 24-28 (M = 256 for a CTA pair).
-template <int BN, bool PAIR>
+// 17-22, M >> 4 in bits 24-28 (M = 256 for a CTA pair).  N is the MMA's
+// width: the tile's, or a column slice of it.
+template <int N, bool PAIR>
 __device__ __forceinline__ constexpr uint32_t mma_idesc()
 {
-    return (1u << 4) | (1u << 16) | (uint32_t(BN >> 3) << 17) |
-           (uint32_t(TileCfg<BN, PAIR>::TILE_M >> 4) << 24);
+    static_assert(N % 16 == 0 && N >= 16 && N <= 256, "MMA width");
+    return (1u << 4) | (1u << 16) | (uint32_t(N >> 3) << 17) | (uint32_t(PAIR ? 256 : 128) >> 4 << 24);
 }
 
 // Shared-memory matrix descriptor fields common to both operands: 128-byte
@@ -260,6 +261,7 @@ struct Unit {
     int32_t s;         // fused split unit: its split index
     int64_t red_tile;  // fused split unit: index of its tile among the split tiles
     int32_t rows;      // rows of the matrix: M, or the group's count in a grouped launch
+    int32_t width;     // columns of the unit: the tile width, or a slice of it (narrow tail)
 };
 
 // Tile index (within one matrix) -> first row / column, in a grouped raster:
@@ -281,6 +283,9 @@ __device__ __forceinline__ void raster(int64_t t, const KernelParams &p, int32_t
 // Work unit -> tile and K range.
 //   fused plans: units below dp_units are whole tiles; the others are split
 //     units, tile-major (the splits of one tile sit on neighbouring clusters).
+//   narrow tails: units below dp_units are whole tiles; the others are column
+//     slices of the remaining tiles (`narrow` slices of bn / narrow columns
+//     each, full K), tile-major.
 //   grouped launches: the group whose tiles hold u (binary search of `gtab`,
 //     the inclusive tile counts per group), then its tiles as in one matrix.
 //   otherwise: (batch, split) outermost, then the tiles of one matrix; split
@@ -294,6 +299,7 @@ __device__ __forceinline__ Unit decode_unit(int64_t u, const KernelParams &p, co
     w.s = 0;
     w.red_tile = 0;
     w.rows = p.M;
+    w.width = bn;
     if (p.group_rows) {
         int32_t lo = 0, hi = p.groups - 1;
         while (lo < hi) {
@@ -313,23 +319,31 @@ __device__ __forceinline__ Unit decode_unit(int64_t u, const KernelParams &p, co
         w.rows = min(max(p.group_rows[lo], 0), p.M);
         return w;
     }
-    if (p.fused) {
-        int64_t tg;  // tile index over all matrices of the batch
-        if (u < p.dp_units) {
-            tg = u;
-            w.kb0 = 0;
-            w.kb1 = p.k_blocks;
-        } else {
+    if (p.fused || p.narrow) {
+        int64_t tg = u;  // tile index over all matrices of the batch
+        int32_t piece = 0;
+        w.kb0 = 0;
+        w.kb1 = p.k_blocks;
+        if (u >= p.dp_units) {
             const int64_t j = u - p.dp_units;
-            w.red_tile = j / p.split_k;
-            w.s = int32_t(j - w.red_tile * p.split_k);
-            tg = p.dp_units + w.red_tile;
-            w.split = 1;
-            w.kb0 = int32_t(int64_t(w.s) * p.k_blocks / p.split_k);
-            w.kb1 = int32_t(int64_t(w.s + 1) * p.k_blocks / p.split_k);
+            const int32_t per = p.narrow ? p.narrow : p.split_k;
+            const int64_t t = j / per;
+            const int32_t s = int32_t(j - t * per);
+            tg = p.dp_units + t;
+            if (p.narrow) {
+                piece = s;
+                w.width = bn / p.narrow;
+            } else {
+                w.red_tile = t;
+                w.s = s;
+                w.split = 1;
+                w.kb0 = int32_t(int64_t(s) * p.k_blocks / p.split_k);
+                w.kb1 = int32_t(int64_t(s + 1) * p.k_blocks / p.split_k);
+            }
         }
         const int64_t b = tg / tiles;
         raster(tg - b * tiles, p, p.tiles_m, tile_m, bn, w.m0, w.n0);
+        w.n0 += piece * w.width;
         w.z_in = int32_t(b);
         w.z_out = w.split ? int32_t(u - p.dp_units) : int32_t(b);
         return w;
@@ -571,8 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The leader's `full` and `tempty` barriers as shared::cluster addresses.
     const uint32_t full_lead0 = PAIR ? ptx::mapa_shared(full0, 0) : full0;
     const uint32_t tempty_lead0 = PAIR ? ptx::mapa_shared(tempty0, 0) : tempty0;
-    const int32_t row_off = PAIR ? int32_t(rank) * kTileM : 0;       // this CTA's rows
-    const int32_t col_off = PAIR ? int32_t(rank) * Cfg::B_COLS : 0;  // this CTA's B columns
+    const int32_t row_off = PAIR ? int32_t(rank) * kTileM : 0;  // this CTA's rows
 
     if (warp == 0) {
         if (lane == 0) {
@@ -582,6 +595,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int64_t u = cluster; ok && u < num_units; u += nclusters) {
                 const Unit w = decode_unit(u, p, gtab, Cfg::TILE_M, BN);
+                // This CTA's B columns: half of the unit's in a pair, in
+                // boxes of 64 columns.
+                const int nbox = w.width / (PAIR ? 128 : 64);
+                const int32_t col_off = PAIR ? int32_t(rank) * (w.width / 2) : 0;
+                const uint32_t tx = uint32_t(Cfg::A_BYTES + nbox * Cfg::B_BOX_BYTES);
                 if (p.prefetch_l2) {
                     // The unit's whole K range of A and B at once: DRAM sees the
                     // requests together (better page locality than the ring's
@@ -590,7 +608,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::tma_prefetch_l2_3d(&map_a, kb * kTileK, w.m0 + row_off, w.z_in);
 #pragma unroll
                         for (int j = 0; j < Cfg::B_BOXES; ++j)
-                            ptx::tma_prefetch_l2_3d(&map_b, w.n0 + col_off + 64 * j, kb * kTileK, w.z_in);
+                            if (j < nbox)
+                                ptx::tma_prefetch_l2_3d(&map_b, w.n0 + col_off + 64 * j, kb * kTileK, w.z_in);
                     }
                 }
                 for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
@@ -603,20 +622,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // Both CTAs' bytes are counted on the leader's barrier.
                         const uint32_t fb = full_lead0 + 8u * stage;
                         if (leader)
-                            ptx::mbar_arrive_expect_tx(full0 + 8u * stage, 2 * Cfg::STAGE_BYTES);
+                            ptx::mbar_arrive_expect_tx(full0 + 8u * stage, 2u * tx);
                         ptx::tma_load_3d_pair(sa, &map_a, fb, kb * kTileK, w.m0 + row_off, w.z_in);
 #pragma unroll
                         for (int j = 0; j < Cfg::B_BOXES; ++j)
-                            ptx::tma_load_3d_pair(sa + Cfg::A_BYTES + j * Cfg::B_BOX_BYTES, &map_b,
-                                                  fb, w.n0 + col_off + 64 * j, kb * kTileK, w.z_in);
+                            if (j < nbox)
+                                ptx::tma_load_3d_pair(sa + Cfg::A_BYTES + j * Cfg::B_BOX_BYTES, &map_b,
+                                                      fb, w.n0 + col_off + 64 * j, kb * kTileK, w.z_in);
                     } else {
                         const uint32_t fb = full0 + 8u * stage;
-                        ptx::mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES);
+                        ptx::mbar_arrive_expect_tx(fb, tx);
                         ptx::tma_load_3d(sa, &map_a, fb, kb * kTileK, w.m0, w.z_in);
 #pragma unroll
                         for (int j = 0; j < Cfg::B_BOXES; ++j)
-                            ptx::tma_load_3d(sa + Cfg::A_BYTES + j * Cfg::B_BOX_BYTES, &map_b, fb,
-                                             w.n0 + 64 * j, kb * kTileK, w.z_in);
+                            if (j < nbox)
+                                ptx::tma_load_3d(sa + Cfg::A_BYTES + j * Cfg::B_BOX_BYTES, &map_b, fb,
+                                                 w.n0 + 64 * j, kb * kTileK, w.z_in);
                     }
                     ++issued;
                     if (++stage == S) {
@@ -647,7 +668,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         if (lane == 0 && leader) {
             // ---------------- MMA issuer (one thread; the leader of a pair)
+            // Instruction descriptors of a whole tile and of the column
+            // slices a narrow tail cuts it into (halves and quarters).
             constexpr uint32_t idesc = mma_idesc<BN, PAIR>();
+            constexpr uint32_t idesc2 = mma_idesc<BN / 2, PAIR>();
+            constexpr uint32_t idesc4 = mma_idesc<BN / 4, PAIR>();
             constexpr uint16_t both = PAIR ? 3 : 1;
             uint32_t stage = 0, phase = 0, abuf = 0, aphase = 0;
             bool ok = true;
@@ -659,6 +684,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ptx::tc_fence_after_sync();
                 const uint32_t d = tmem_base + abuf * uint32_t(BN);
+                const uint32_t id = w.width == BN ? idesc : (w.width == BN / 2 ? idesc2 : idesc4);
                 for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!wait_bounded(full0 + 8u * stage, phase, af, kStatusMma, true)) {
                         ok = false;
@@ -674,7 +700,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // A: advance 16 f16 = 32 bytes along the swizzled row.
                         // B: advance 16 K rows = 2048 bytes.
                         ptx::mma_f16_ss<PAIR>(d, desc_a(sa + 32u * kk), desc_b(sb + 2048u * kk),
-                                              idesc, (kb > w.kb0 || kk > 0) ? 1u : 0u);
+                                              id, (kb > w.kb0 || kk > 0) ? 1u : 0u);
                     }
                     ptx::mma_commit<PAIR>(empty0 + 8u * stage, both);  // slot free in both CTAs
                     if (++stage == S) {
@@ -715,10 +741,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (warp == 2 && lane == 0)
                 trace_stamp(p, kTraceAccReady);
             const int32_t row0 = w.m0 + row_off + 32 * q;
+            // A column slice of the last tile column may start at or past N:
+            // then nothing is stored, and the accumulator is still released.
             int nch = 0;
-            if (row0 < w.rows) {
+            if (row0 < w.rows && w.n0 < p.N) {
                 const int live = (p.N - w.n0 + 31) / 32;
-                nch = live < BN / 32 ? live : BN / 32;
+                nch = live < w.width / 32 ? live : w.width / 32;
             }
             const uint32_t tm_row = tmem_base + (uint32_t(32 * q) << 16) + abuf * uint32_t(BN);
             const int32_t tail_row = row0 + lane;
