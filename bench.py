@@ -48,6 +48,8 @@ def parse_args(argv=None):
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--warm-seconds", type=float, default=0.5,
+                   help="after the warm-up steps, keep warming up until the GPU has been busy this long")
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD,
                    help="one of the named workloads in tiled_staged_matmul_gb300.synthetic "
@@ -182,10 +184,20 @@ class ClockSampler:
         if self.thread is not None:
             self.thread.join(timeout=5)
 
+    # nvidia-smi's readings refresh about every 0.1 s and describe the time
+    # before the reading: a state of the timed region shows up to LAG_S later.
+    LAG_S = 0.25
+
     def summary(self, t0: float, t1: float) -> dict:
-        rows = [s for (t, s) in self.samples if t0 <= t <= t1]
+        """SM clock (median) and throttle reasons of the timed region
+        [t0, t1]: the clock from readings taken in the region shifted by
+        0.1 s, the reasons from every reading up to LAG_S after it."""
+        def window(a, b):
+            return [s for (t, s) in self.samples if a <= t <= b]
+        rows = window(t0 + 0.1, t1 + 0.1)
         if not rows:  # region shorter than the sampling period: nearest samples
             rows = [s for (t, s) in sorted(self.samples, key=lambda ts: abs(ts[0] - (t0 + t1) / 2))[:3]]
+        reason_rows = window(t0, t1 + self.LAG_S) or rows
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows:
@@ -196,6 +208,10 @@ class ClockSampler:
                 sm.append(float(parts[0]))
                 smax.append(float(parts[1]))
             except ValueError:
+                continue
+        for r in reason_rows:
+            parts = [p.strip() for p in r.split(",")]
+            if len(parts) < 8:
                 continue
             for name, v in zip(names, parts[4:8]):
                 if v.lower().startswith("active"):
@@ -218,6 +234,17 @@ def timed_loop(args, call, flush, stream, world, local_rank):
         if flush:
             flush()
         call()
+    # ... and on until the GPU has been loaded for warm_seconds, so that the
+    # timed steps run in the clock and power state the workload settles in
+    # (on GB300 the power cap lowers the SM clock ~0.1 s into a dense GEMM).
+    torch.cuda.synchronize()
+    w0 = time.time()
+    while time.time() - w0 < args.warm_seconds:
+        for _ in range(8):
+            if flush:
+                flush()
+            call()
+        torch.cuda.synchronize()
     binding.check(binding.gemm_get_device_status(stream.cuda_stream))
     torch.cuda.synchronize()
 
@@ -238,30 +265,46 @@ def timed_loop(args, call, flush, stream, world, local_rank):
     torch.cuda.synchronize()
     barrier(world)
     t1 = time.time()
-    time.sleep(0.1)
+    time.sleep(ClockSampler.LAG_S + 0.1)  # readings trail the GPU's state
     sampler.stop()
     binding.check(binding.gemm_get_device_status(stream.cuda_stream))
     return [s.elapsed_time(e) for s, e in zip(starts, ends)], t0, t1, sampler
 
 
-def roofline_of(flops, algorithmic_bytes, ms, traffic, kernel):
+def power_capped(clocks) -> bool:
+    """The timed region ran under the power cap (or well below the maximum
+    SM clock): the sustained regime."""
+    if not clocks:
+        return False
+    if "sw_power_cap" in clocks.get("reasons", []):
+        return True
+    sm, smax = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
+    return bool(sm and smax and sm < 0.97 * smax)
+
+
+def roofline_of(flops, algorithmic_bytes, ms, traffic, kernel, clocks=None):
     """Achieved against the slower of the two roofs: dense tensor peak for
-    the flops, HBM bandwidth for the algorithmic bytes (both measured)."""
+    the flops, HBM bandwidth for the algorithmic bytes (both measured).  The
+    tensor peak is the burst one, or the sustained one (cuBLAS back to back
+    for seconds, under the power cap) when the timed region ran power-capped."""
     peaks = measured_peaks()
     tflops_launch = flops / (ms * 1e-3) / 1e12
     gbs_launch = algorithmic_bytes / (ms * 1e-3) / 1e9
     t_tensor = flops / (peaks["bf16_tflops"] * 1e12)
     t_hbm = algorithmic_bytes / (peaks["hbm_gbs"] * 1e9)
+    sustained = power_capped(clocks) and peaks.get("bf16_tflops_sustained")
+    tensor_peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
     if t_tensor >= t_hbm:
         roofline = {"bound": "tensor", "achieved": round(tflops_launch, 2),
-                    "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                    "frac": round(tflops_launch / peaks["bf16_tflops"], 4)}
+                    "peak": tensor_peak, "unit": "TFLOP/s",
+                    "frac": round(tflops_launch / tensor_peak, 4)}
     else:
         roofline = {"bound": "hbm", "achieved": round(gbs_launch, 1), "peak": peaks["hbm_gbs"],
                     "unit": "GB/s", "frac": round(gbs_launch / peaks["hbm_gbs"], 4)}
     roofline["traffic"] = traffic
-    roofline["peak_source"] = (f"{peaks['source']} (MEASURED_PEAKS.json bf16 burst; f16 dense "
-                               "rate taken equal to bf16, the nominal ratio)"
+    roofline["peak_source"] = (f"{peaks['source']} (MEASURED_PEAKS.json bf16 "
+                               f"{'sustained: the timed region ran power-capped' if sustained else 'burst'}"
+                               "; f16 dense rate taken equal to bf16, the nominal ratio)"
                                if roofline["bound"] == "tensor" else
                                f"{peaks['source']} (MEASURED_PEAKS.json copy bandwidth)")
     roofline["kernel"] = kernel
@@ -308,6 +351,7 @@ def run_grouped(args, rank, local_rank, world):
     per_step_ms, t0, t1, sampler = timed_loop(args, call, flush_l2 if flush else None, stream,
                                               world, local_rank)
     ms_local = sum(per_step_ms) / len(per_step_ms)
+    clocks = sampler.summary(t0, t1)
     value, ms = replica_throughput(flops, ms_local, world, dev)
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
@@ -324,9 +368,8 @@ def run_grouped(args, rank, local_rank, world):
                    "parallelism": f"replicas x{world}"},
         "gpu_launches": args.steps * launches_per_call,
         "roofline": roofline_of(flops, abytes, ms_local, recorded_traffic(w.name),
-                                "tsm_gemm_tcgen05_kernel (grouped)"),
+                                "tsm_gemm_tcgen05_kernel (grouped)", clocks),
     }
-    clocks = sampler.summary(t0, t1)
     result["clocks"] = {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = grouped_cpu_baseline(w, A_h, B_h, counts_h, target_s=15.0)
@@ -369,9 +412,10 @@ def run_rows(args, rank, local_rank, world):
     per_step_ms, t0, t1, sampler = timed_loop(args, call, flush_l2 if flush else None, stream,
                                               world, local_rank)
     ms_local = sum(per_step_ms) / len(per_step_ms)
+    clocks = sampler.summary(t0, t1)
     value, ms = replica_throughput(w.flops, ms_local, world, dev)
     roofline = roofline_of(w.flops, w.algorithmic_bytes, ms_local, recorded_traffic(w.name),
-                           "tsm_row_reduce_kernel")
+                           "tsm_row_reduce_kernel", clocks)
     result = {
         "metric": METRIC, "value": round(value, 4), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
@@ -386,7 +430,6 @@ def run_rows(args, rank, local_rank, world):
         "roofline": roofline,
         "hbm_gbs": round(w.algorithmic_bytes / (ms_local * 1e-3) / 1e9, 1),
     }
-    clocks = sampler.summary(t0, t1)
     result["clocks"] = {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")}
     return result
 
@@ -448,6 +491,7 @@ def run_ours(args, rank, local_rank, world):
     per_step_ms, t0, t1, sampler = timed_loop(args, call, flush_l2 if flush else None, stream,
                                               world, local_rank)
     ms_local = sum(per_step_ms) / len(per_step_ms)
+    clocks = sampler.summary(t0, t1)
     value, ms = replica_throughput(w.flops, ms_local, world, dev)
     abytes = 2 * w.M * w.K + 2 * w.K * w.N + out_bytes * w.M * w.N + (4 * w.N if args.bias else 0)
     roofline = roofline_of(w.flops, abytes, ms_local,
@@ -455,7 +499,7 @@ def run_ours(args, rank, local_rank, world):
                            "tsm_gemm_tcgen05_kernel" + (" + tsm_splitk_reduce_kernel"
                                                         if plan["split_k"] > 1
                                                         and not plan["fused_reduce"] else "")
-                           + (f" + {copies} x tsm_pitch_copy_kernel" if repacked else ""))
+                           + (f" + {copies} x tsm_repack_kernel" if repacked else ""), clocks)
 
     result = {
         "metric": METRIC,
@@ -492,7 +536,6 @@ def run_ours(args, rank, local_rank, world):
         "gpu_launches": args.steps * launches_per_call,
         "roofline": roofline,
     }
-    clocks = sampler.summary(t0, t1)
     result["clocks"] = {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")}
     if args.trace:
         result["trace"] = traced_step(args, binding, call, plan, flush_l2 if flush else None, dev)
@@ -721,6 +764,8 @@ def main(argv=None):
     else:
         result = run_ours(args, rank, local_rank, world)
     if rank == 0:
+        result["config"]["warm_up"] = (f"{max(args.warmup, 3)} steps, then steps until the GPU "
+                                       f"had been busy {args.warm_seconds:g} s")
         print(json.dumps(result), flush=True)
     if world > 1:
         import torch.distributed as dist
