@@ -19,6 +19,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from tiled_staged_matmul_gb300 import synthetic
 
 pytestmark = pytest.mark.gpu
@@ -108,3 +109,21 @@ def test_call_leaves_free_device_memory_unchanged(b):
     free_after, _ = torch.cuda.mem_get_info()
     b.check(b.gemm_get_device_status(s))
     assert free_after == free_before
+
+
+@pytest.mark.parametrize("M,N,K", [(4096, 4096, 1024), (2304, 2304, 320)])
+def test_column_slice_tail_without_split(b, M, N, K):
+    """Shapes whose no-allocation plan keeps whole K (no partials to hold) but
+    cuts the last wave's tiles into column slices: exact on small integers,
+    and no scratch involved."""
+    plan = b.gemm_plan(M, N, K, 1, b.GemmOptions(0, 0, 0, 0, 0, 1))
+    assert plan["split_k"] == 1 and plan["tail_narrow"] == 1 and plan["workspace_bytes"] == 0, plan
+    A, B = synthetic.operands(M, N, K, "int4", seed=M + K)
+    dA, dB = A.cuda().contiguous(), B.cuda().contiguous()
+    C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    b.check(b.gemm_f16_f32acc_splitk_noalloc(dA.data_ptr(), dB.data_ptr(), C.data_ptr(),
+                                             M, N, K, K, N, N, 0, s))
+    b.check(b.gemm_get_device_status(s))
+    ref = oracle.gemm_f64(A, B, M, N, K)
+    assert np.array_equal(C.cpu().double().numpy(), ref)
