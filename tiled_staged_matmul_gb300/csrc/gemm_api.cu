@@ -422,20 +422,22 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const ge
     for (const TileChoice &c : kChoices) {
         if (!allowed(c))
             continue;
-        // Long K: one CTA per tile measured faster than CTA pairs (the first
-        // k-block lands sooner and each reducer sums fewer rows), e.g. 26.9 us
-        // against 29.2 us on 256 x 256 x 65536.
-        if (long_k && req_m == 0 && c.tile_m != kTileM)
-            continue;
         const int64_t tiles = tiles_of(c.tile_m, c.tile_n);
         double cost;
         if (long_k) {
+            // Each unit's K range at the tile's time per k-block, in waves of
+            // units; split partials cost ~2 us plus ~20 us per MB each CTA
+            // stores (and its reducer rows read back); pairs their fixed
+            // ~8 us.  Fitted to every tile shape timed on 44 long-K shapes on
+            // GB300: within 0.1 % (geometric mean) of the fastest, against
+            // 4.2 % for a count of bytes moved; on 256 x 256 x 65536 it keeps
+            // 128 x 128 tiles in 38 splits (27.7 us; 128 x 256 in 76: 29.7).
             const int sk = split_for(c.tile_m, c.tile_n);
-            const double stage = 2.0 * c.tile_m * kTileK + 2.0 * kTileK * c.tile_n;
-            // Partial sums cost about four times their bytes (written, waited
-            // for, read back and summed), measured on the 256 x 256 x 65536 case.
-            cost = double(tiles) * sk * ceil_div(k_blocks, sk) * stage +
-                   (sk > 1 ? 4.0 * 2.0 * sk * double(M) * ldw * 4 * batch : 0.0);
+            const int64_t units = tiles * sk;
+            const int64_t waves = (units + slots_of(c.tile_m) - 1) / slots_of(c.tile_m);
+            const double partial_mb = 2.0 * kTileM * c.tile_n * 4 / 1e6;
+            cost = double(waves) * ceil_div(k_blocks, sk) * kb_us(c.tile_m, c.tile_n) +
+                   (sk > 1 ? 2.0 + 20.0 * partial_mb : 0.0) + (c.tile_m == 2 * kTileM ? 8.0 : 0.0);
         } else {
             // Full waves of persistent CTAs at the tile's time per k-block
             // (kb_us), and the last wave: whole, or spread over every slot by
