@@ -931,7 +931,10 @@ gemm_status_t row_reduce(const void *X, int elem, int64_t R, int64_t C, int64_t 
     const int64_t max_workers = resident * per_block;  // workers that run at once
     int64_t segs = 1;
     if (R < max_workers && C > 0)
-        segs = std::max<int64_t>(1, std::min<int64_t>((max_workers + R - 1) / R,
+        // Rounded down: R x segs items at most the workers that fit at once
+        // (one full pass; rounding up made two half-empty ones, measured 1.9x
+        // slower at 1024 x 131072 f32).
+        segs = std::max<int64_t>(1, std::min<int64_t>(max_workers / R,
                                                       std::min<int64_t>(units / (16 * tpr), 65536)));
     int64_t seg = C > 0 ? (C + segs - 1) / segs : 0;
     if (vec)

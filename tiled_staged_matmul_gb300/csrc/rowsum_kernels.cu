@@ -97,21 +97,45 @@ __global__ void __launch_bounds__(256) tsm_row_reduce_kernel(RowReduceParams p)
                 const int64_t nchunk = (c1 - c0) / V;
                 const uint4 *ap = reinterpret_cast<const uint4 *>(row);
                 const uint4 *xp = GEMV ? reinterpret_cast<const uint4 *>(p.xv + c0) : nullptr;
-                for (int64_t k = sub; k < nchunk; k += 8 * tpr) {
-                    uint4 a[8], xv[8];
+                if constexpr (ET == kOutF32) {
+                    // Whole groups of eight independent loads, then the last,
+                    // partial group (chunk k + j * tpr still to acc[j]).
+                    // For f32 this form keeps eight loads in flight (1.3-1.9x
+                    // faster on GB300, 55 registers instead of 74); for the
+                    // 16-bit types the guarded form below measured faster.
+                    int64_t k = sub;
+                    for (; k + 7 * int64_t(tpr) < nchunk; k += 8 * tpr) {
+                        uint4 a[8];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int64_t kk = k + int64_t(j) * tpr;
-                        if (kk < nchunk) {
-                            a[j] = __ldg(ap + kk);
-                            if constexpr (GEMV)
-                                xv[j] = __ldg(xp + kk);
-                        }
+                        for (int j = 0; j < 8; ++j)
+                            a[j] = __ldg(ap + k + int64_t(j) * tpr);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            acc[j] += chunk_sum<ET, false>(a[j], a[j]);
                     }
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        if (k + int64_t(j) * tpr < nchunk)
-                            acc[j] += chunk_sum<ET, GEMV>(a[j], GEMV ? xv[j] : a[j]);
+                    for (int j = 0; j < 7; ++j)
+                        if (k + int64_t(j) * tpr < nchunk) {
+                            const uint4 aj = __ldg(ap + k + int64_t(j) * tpr);
+                            acc[j] += chunk_sum<ET, false>(aj, aj);
+                        }
+                } else {
+                for (int64_t k = sub; k < nchunk; k += 8 * tpr) {
+                        uint4 a[8], xv[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const int64_t kk = k + int64_t(j) * tpr;
+                            if (kk < nchunk) {
+                                a[j] = __ldg(ap + kk);
+                                if constexpr (GEMV)
+                                    xv[j] = __ldg(xp + kk);
+                            }
+                        }
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            if (k + int64_t(j) * tpr < nchunk)
+                                acc[j] += chunk_sum<ET, GEMV>(a[j], GEMV ? xv[j] : a[j]);
+                    }
                 }
                 if (sub == 0) {
                     for (int64_t c = c0 + nchunk * V; c < c1; ++c) {
@@ -175,7 +199,18 @@ __global__ void __launch_bounds__(256) tsm_row_partials_kernel(const float *__re
     for (int64_t r = int64_t(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5); r < R; r += warps) {
         const float *pr = partial + r * segs;
         float v = 0.f;
-        for (int32_t s = lane; s < segs; s += 32)
+        int32_t s = lane;
+        // Eight loads in flight, added in the same ascending order.
+        for (; s + 7 * 32 < segs; s += 8 * 32) {
+            float t[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                t[j] = pr[s + 32 * j];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                v += t[j];
+        }
+        for (; s < segs; s += 32)
             v += pr[s];
         for (int o = 16; o >= 1; o >>= 1)
             v += __shfl_xor_sync(0xffffffffu, v, o);
