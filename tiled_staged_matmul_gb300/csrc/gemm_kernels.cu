@@ -175,11 +175,18 @@ __device__ __forceinline__ uint32_t epi_out16(float v, int32_t out_type)
                                 : uint32_t(__half_as_ushort(__float2half_rn(v)));
 }
 
+// An activation as a compile-time constant (template argument of a lambda).
+template <int A>
+struct ActTag {
+    static constexpr int value = A;
+};
+
 // The fused epilogue on four consecutive values of one row (columns col ...
-// col + 3): v = act(alpha * v + bias[col]); the activation is chosen once,
-// outside the four.
-__device__ __forceinline__ void epi_apply4(float4 &v, int32_t col, int32_t N, const float *bias,
-                                           const Epilogue &e)
+// col + 3), the activation fixed at compile time so that the four overlap:
+// v = act(alpha * v + bias[col]).
+template <int ACT>
+__device__ __forceinline__ void epi_apply4_as(float4 &v, int32_t col, int32_t N, const float *bias,
+                                              const Epilogue &e)
 {
     float b[4] = {0.f, 0.f, 0.f, 0.f};
     if (bias) {
@@ -187,31 +194,10 @@ __device__ __forceinline__ void epi_apply4(float4 &v, int32_t col, int32_t N, co
         for (int k = 0; k < 4; ++k)
             b[k] = col + k < N ? __ldg(bias + col + k) : 0.f;
     }
-    v.x = e.alpha * v.x + b[0];
-    v.y = e.alpha * v.y + b[1];
-    v.z = e.alpha * v.z + b[2];
-    v.w = e.alpha * v.w + b[3];
-    switch (e.act) {
-    case kActNone: break;
-    case kActRelu:
-        v.x = v.x > 0.f ? v.x : 0.f;
-        v.y = v.y > 0.f ? v.y : 0.f;
-        v.z = v.z > 0.f ? v.z : 0.f;
-        v.w = v.w > 0.f ? v.w : 0.f;
-        break;
-    case kActLeakyRelu:
-        v.x = v.x > 0.f ? v.x : e.slope * v.x;
-        v.y = v.y > 0.f ? v.y : e.slope * v.y;
-        v.z = v.z > 0.f ? v.z : e.slope * v.z;
-        v.w = v.w > 0.f ? v.w : e.slope * v.w;
-        break;
-    default:
-        v.x = epi_act(v.x, e.act, e.slope);
-        v.y = epi_act(v.y, e.act, e.slope);
-        v.z = epi_act(v.z, e.act, e.slope);
-        v.w = epi_act(v.w, e.act, e.slope);
-        break;
-    }
+    v.x = epi_act(fmaf(e.alpha, v.x, b[0]), ACT, e.slope);
+    v.y = epi_act(fmaf(e.alpha, v.y, b[1]), ACT, e.slope);
+    v.z = epi_act(fmaf(e.alpha, v.z, b[2]), ACT, e.slope);
+    v.w = epi_act(fmaf(e.alpha, v.w, b[3]), ACT, e.slope);
 }
 
 // One row of a staged 32 x 32 f32 box (this lane's, 128-byte swizzled) through
@@ -985,7 +971,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float4 *stg = reinterpret_cast<const float4 *>(base_ptr);
                     const int32_t per_split = p.rows_per * (BN / 4);  // float4s of one split
                     const int32_t nsplit = p.split_k;
-                    auto put = [&](int32_t f, const float4 &acc) {
+                    auto put = [&](auto act, int32_t f, const float4 &acc) {
                         const int32_t row = f / (BN / 4);
                         const int32_t gr = w.m0 + r0 + row;
                         const int32_t gc = w.n0 + (f - row * (BN / 4)) * 4;
@@ -995,7 +981,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 const float *bias =
                                     p.epi.bias ? p.epi.bias + bz * p.epi.bias_stride : nullptr;
                                 float4 v = acc;
-                                epi_apply4(v, gc, p.N, bias, p.epi);
+                                epi_apply4_as<decltype(act)::value>(v, gc, p.N, bias, p.epi);
                                 if (gc + 3 < p.N && p.epi.out_type == kOutF32) {
                                     *reinterpret_cast<float4 *>(static_cast<float *>(p.c_direct) + at) = v;
                                 } else if (gc + 3 < p.N) {
@@ -1027,28 +1013,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                     };
                     // Two float4s per thread per pass, splits unrolled: the
                     // shared-memory loads overlap, while each sum still adds
-                    // the splits one at a time in ascending order.
-                    for (int32_t f0 = et; f0 < per_split; f0 += 256) {
-                        const int32_t f1 = f0 + 128;
-                        const bool two = f1 < per_split;
-                        float4 a0 = stg[f0];
-                        float4 a1 = two ? stg[f1] : make_float4(0.f, 0.f, 0.f, 0.f);
+                    // the splits one at a time in ascending order.  The
+                    // activation is a compile-time constant of the loop (one
+                    // dispatch per CTA), so the values' activations overlap.
+                    auto sum_all = [&](auto act) {
+                        for (int32_t f0 = et; f0 < per_split; f0 += 256) {
+                            const int32_t f1 = f0 + 128;
+                            const bool two = f1 < per_split;
+                            float4 a0 = stg[f0];
+                            float4 a1 = two ? stg[f1] : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
-                        for (int32_t s2 = 1; s2 < nsplit; ++s2) {
-                            const float4 v0 = stg[s2 * per_split + f0];
-                            const float4 v1 = two ? stg[s2 * per_split + f1] : v0;
-                            a0.x += v0.x;
-                            a0.y += v0.y;
-                            a0.z += v0.z;
-                            a0.w += v0.w;
-                            a1.x += v1.x;
-                            a1.y += v1.y;
-                            a1.z += v1.z;
-                            a1.w += v1.w;
+                            for (int32_t s2 = 1; s2 < nsplit; ++s2) {
+                                const float4 v0 = stg[s2 * per_split + f0];
+                                const float4 v1 = two ? stg[s2 * per_split + f1] : v0;
+                                a0.x += v0.x;
+                                a0.y += v0.y;
+                                a0.z += v0.z;
+                                a0.w += v0.w;
+                                a1.x += v1.x;
+                                a1.y += v1.y;
+                                a1.z += v1.z;
+                                a1.w += v1.w;
+                            }
+                            put(act, f0, a0);
+                            if (two)
+                                put(act, f1, a1);
                         }
-                        put(f0, a0);
-                        if (two)
-                            put(f1, a1);
+                    };
+                    if constexpr (EPI) {
+                        switch (p.epi.act) {
+                        case kActRelu: sum_all(ActTag<kActRelu>{}); break;
+                        case kActLeakyRelu: sum_all(ActTag<kActLeakyRelu>{}); break;
+                        case kActGelu: sum_all(ActTag<kActGelu>{}); break;
+                        case kActGeluTanh: sum_all(ActTag<kActGeluTanh>{}); break;
+                        case kActSilu: sum_all(ActTag<kActSilu>{}); break;
+                        default: sum_all(ActTag<kActNone>{}); break;
+                        }
+                    } else {
+                        sum_all(ActTag<kActNone>{});
                     }
                 }
             }
