@@ -275,6 +275,25 @@ def test_subnormal_inputs_are_not_flushed(b):
     assert torch.equal(C, A[:, :N].float())
 
 
+def test_nan_and_inf_propagate_as_ieee(b):
+    """One NaN row and one +Inf entry in A: the CUDA path makes the same cells
+    NaN, +Inf and -Inf as the oracle (IEEE: Inf x 0 = NaN, one infinite term
+    per cell so the order of the sum does not matter) and the rest exact."""
+    from test_oracle_pins import special_values_case
+    A, B, nan_cells, pos_inf, neg_inf = special_values_case()
+    M, K = A.shape
+    N = B.shape[1]
+    C, dC = run_gemm(b, torch.from_numpy(A), torch.from_numpy(B))
+    C = C.numpy().astype(np.float64)
+    ref = oracle.gemm_f64(A, B, M, N, K)
+    assert np.array_equal(np.isnan(C), nan_cells)
+    assert np.array_equal(np.isposinf(C), pos_inf)
+    assert np.array_equal(np.isneginf(C), neg_inf)
+    finite = ~(nan_cells | pos_inf | neg_inf)
+    assert np.array_equal(C[finite], ref[finite])
+    assert dC.outside_untouched()
+
+
 def test_batched(b):
     for (M, N, K) in [(64, 128, 128), (1000, 1000, 1000)]:
         batch = 3

@@ -223,6 +223,41 @@ def test_thread_count_does_not_change_results():
     assert np.array_equal(C1, C3)
 
 
+def special_values_case():
+    """A small case with one NaN row and one +Inf entry in A (seeded, int4
+    elsewhere, so the finite cells are exact), and what IEEE arithmetic
+    makes of it: row 3 of C is all NaN; cell (5, j) is +Inf, -Inf or NaN as
+    B[7, j] is positive, negative or zero (one infinite term per cell, so
+    the summation order does not matter); every other cell is finite."""
+    rng = np.random.default_rng(77)
+    M, N, K = 16, 40, 24
+    A = rng.integers(-4, 5, size=(M, K)).astype(np.float16)
+    B = rng.integers(-4, 5, size=(K, N)).astype(np.float16)
+    A[3, 10] = np.float16(np.nan)
+    A[5, 7] = np.float16(np.inf)
+    nan_cells = np.zeros((M, N), dtype=bool)
+    nan_cells[3, :] = True
+    nan_cells[5, :] = B[7, :] == 0
+    pos_inf = np.zeros((M, N), dtype=bool)
+    neg_inf = np.zeros((M, N), dtype=bool)
+    pos_inf[5, :] = B[7, :] > 0
+    neg_inf[5, :] = B[7, :] < 0
+    return A, B, nan_cells, pos_inf, neg_inf
+
+
+def test_nan_and_inf_propagate_as_ieee():
+    A, B, nan_cells, pos_inf, neg_inf = special_values_case()
+    M, K = A.shape
+    N = B.shape[1]
+    C = oracle.gemm_f64(A, B, M, N, K)
+    assert np.array_equal(np.isnan(C), nan_cells)
+    assert np.array_equal(np.isposinf(C), pos_inf)
+    assert np.array_equal(np.isneginf(C), neg_inf)
+    finite = ~(nan_cells | pos_inf | neg_inf)
+    exact = np.where(np.isfinite(A), A, 0).astype(np.int64) @ B.astype(np.int64)
+    assert np.array_equal(C[finite], exact[finite].astype(np.float64))
+
+
 def test_rejects_bad_arguments():
     with pytest.raises(RuntimeError):
         oracle.gemm_cells(np.ones(4, np.float16), np.ones(4, np.float16), 2, 2, 2,
