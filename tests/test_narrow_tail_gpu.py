@@ -124,3 +124,21 @@ def test_planner_default_column_slices(b, M, N, K, batch):
         for i in range(batch):
             check_exact(C[i].numpy(), ref_of(A[i], B[i]))
     assert dC.outside_untouched()
+
+
+@pytest.mark.parametrize("tile_m,tile_n,pieces", [(256, 256, 2), (0, 0, 4)])
+def test_narrow_tail_batched_with_a_bias_per_batch(b, tile_m, tile_n, pieces):
+    """A batch of two whose last wave's tiles (all in the second matrix) are
+    cut into column slices, with a bias per batch and GELU into bf16: each
+    slice takes the bias row of its own batch."""
+    M, N, K, batch = 2048, 1280, 192, 2
+    opts = b.GemmOptions(0, tile_n, 0, 0, tile_m, 0, 0, NARROW)
+    plan = b.gemm_plan(M, N, K, batch, opts)
+    assert plan["tail_narrow"] == 1 and plan["tail_split"] == pieces, plan
+    A, B = synthetic.operands(M, N, K, "uniform", seed=93, batch=batch)
+    bias = np.random.default_rng(94).uniform(-1, 1, size=(batch, N)).astype(np.float32)
+    C, pad_ok = run_fused(b, A, B, alpha=0.5, bias=bias, act="gelu", out="bf16", batch=batch,
+                          opts=opts)
+    acc = np.stack([oracle.gemm_f64(A[i], B[i], M, N, K) for i in range(batch)])
+    check_epilogue(C, acc, 0.5, bias.astype(np.float64), "gelu", "bf16", K)
+    assert pad_ok
