@@ -142,3 +142,15 @@ def test_narrow_tail_batched_with_a_bias_per_batch(b, tile_m, tile_n, pieces):
     acc = np.stack([oracle.gemm_f64(A[i], B[i], M, N, K) for i in range(batch)])
     check_epilogue(C, acc, 0.5, bias.astype(np.float64), "gelu", "bf16", K)
     assert pad_ok
+
+
+def test_narrow_tail_through_repacked_operands(b):
+    """Odd row pitches (A and B not addressable by the TMA): the operands are
+    repacked and the repacked call plans its own column-slice tail."""
+    M, N, K = 2304, 2304, 320
+    plan = b.gemm_plan(M, N, K, 1)
+    assert plan["tail_narrow"] == 1, plan
+    A, B = synthetic.operands(M, N, K, "int4", seed=97)
+    C, dC = run_gemm(b, A, B, lda=K + 1, ldb=N + 3, ldc=N + 1)
+    check_exact(C.numpy(), ref_of(A, B))
+    assert dC.outside_untouched()
