@@ -73,7 +73,8 @@ def parse_args(argv=None):
                    help="add a per-CTA phase timeline (one extra traced step) to the JSON line")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--e2e-steps", type=int, default=30,
+                   help="end-to-end steps timed (the three-deep pipeline fills and drains once)")
     return p.parse_args(argv)
 
 
@@ -615,7 +616,7 @@ def run_e2e(args, w, A_h, B_h, dev, world):
     ms = start.elapsed_time(end) / args.e2e_steps
     ms = max_over_ranks(ms, world, dev)
     return {"value": round(world * w.flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-            "ms_per_step": round(ms, 4), "pipeline_depth": depth,
+            "ms_per_step": round(ms, 4), "pipeline_depth": depth, "steps": args.e2e_steps,
             "h2d_bytes_per_step": A_p.numel() * 2 + B_p.numel() * 2,
             "d2h_bytes_per_step": C_p[0].numel() * 4}
 
