@@ -235,6 +235,19 @@ def timed_loop(args, call, flush, stream, world, local_rank):
         if flush:
             flush()
         call()
+    # The burst regime: 30 steps before the power cap can engage (~0.1 s of
+    # load on GB300), reported beside the line, not as it.
+    torch.cuda.synchronize()
+    b_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(30)]
+    for e0, e1 in b_ev:
+        if flush:
+            flush()
+        e0.record(stream)
+        call()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    burst_ms = sum(e0.elapsed_time(e1) for e0, e1 in b_ev) / len(b_ev)
     # ... and on until the GPU has been loaded for warm_seconds, so that the
     # timed steps run in the clock and power state the workload settles in
     # (on GB300 the power cap lowers the SM clock ~0.1 s into a dense GEMM).
@@ -269,7 +282,16 @@ def timed_loop(args, call, flush, stream, world, local_rank):
     time.sleep(ClockSampler.LAG_S + 0.1)  # readings trail the GPU's state
     sampler.stop()
     binding.check(binding.gemm_get_device_status(stream.cuda_stream))
-    return [s.elapsed_time(e) for s, e in zip(starts, ends)], t0, t1, sampler
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)], t0, t1, sampler, burst_ms
+
+
+def burst_of(flops, algorithmic_bytes, ms):
+    """The first 30 steps after the minimum warm-up, before the power cap can
+    engage, against the burst peaks (reported beside the line)."""
+    r = roofline_of(flops, algorithmic_bytes, ms, None, "",
+                    {"sm_mhz": None, "sm_max_mhz": None, "reasons": []})
+    return {"steps": 30, "ms_per_step": round(ms, 5), "value": round(flops / (ms * 1e-3) / 1e12, 2),
+            "unit": "TFLOP/s", "roofline_frac": r["frac"], "bound": r["bound"], "peak": r["peak"]}
 
 
 def power_capped(clocks) -> bool:
@@ -349,8 +371,8 @@ def run_grouped(args, rank, local_rank, world):
             A.data_ptr(), B.data_ptr(), C.data_ptr(), counts.data_ptr(), w.groups, w.M, w.N, w.K,
             w.K, w.N, w.N, w.M * w.K, w.K * w.N, w.M * w.N, opts, stream.cuda_stream))
 
-    per_step_ms, t0, t1, sampler = timed_loop(args, call, flush_l2 if flush else None, stream,
-                                              world, local_rank)
+    per_step_ms, t0, t1, sampler, burst_ms = timed_loop(args, call, flush_l2 if flush else None,
+                                                        stream, world, local_rank)
     ms_local = sum(per_step_ms) / len(per_step_ms)
     clocks = sampler.summary(t0, t1)
     value, ms = replica_throughput(flops, ms_local, world, dev)
@@ -370,6 +392,7 @@ def run_grouped(args, rank, local_rank, world):
         "gpu_launches": args.steps * launches_per_call,
         "roofline": roofline_of(flops, abytes, ms_local, recorded_traffic(w.name),
                                 "tsm_gemm_tcgen05_kernel (grouped)", clocks),
+        "burst": burst_of(flops, abytes, burst_ms),
     }
     result["clocks"] = {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -410,8 +433,8 @@ def run_rows(args, rank, local_rank, world):
             binding.check(binding.rowsum_f32acc(X.data_ptr(), w.elem, out.data_ptr(), w.R, w.C, w.C,
                                                 1, stream.cuda_stream))
 
-    per_step_ms, t0, t1, sampler = timed_loop(args, call, flush_l2 if flush else None, stream,
-                                              world, local_rank)
+    per_step_ms, t0, t1, sampler, burst_ms = timed_loop(args, call, flush_l2 if flush else None,
+                                                        stream, world, local_rank)
     ms_local = sum(per_step_ms) / len(per_step_ms)
     clocks = sampler.summary(t0, t1)
     value, ms = replica_throughput(w.flops, ms_local, world, dev)
@@ -489,8 +512,8 @@ def run_ours(args, rank, local_rank, world):
                                                        w.M, w.N, w.K, lda, ldb, ldc, 0, 0, 0, 1,
                                                        o, stream.cuda_stream))
 
-    per_step_ms, t0, t1, sampler = timed_loop(args, call, flush_l2 if flush else None, stream,
-                                              world, local_rank)
+    per_step_ms, t0, t1, sampler, burst_ms = timed_loop(args, call, flush_l2 if flush else None,
+                                                        stream, world, local_rank)
     ms_local = sum(per_step_ms) / len(per_step_ms)
     clocks = sampler.summary(t0, t1)
     value, ms = replica_throughput(w.flops, ms_local, world, dev)
@@ -536,6 +559,7 @@ def run_ours(args, rank, local_rank, world):
                    "parallelism": f"replicas x{world}"},
         "gpu_launches": args.steps * launches_per_call,
         "roofline": roofline,
+        "burst": burst_of(w.flops, abytes, burst_ms),
     }
     result["clocks"] = {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")}
     if args.trace:
