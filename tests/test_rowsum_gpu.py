@@ -4,7 +4,8 @@ Row sums run on f32, f16 and bf16 views with every layout the call takes:
 contiguous rows (the 16-byte vector path), padded and odd row strides, a
 column stride (a transposed view sums columns), an unaligned base (the
 element path), few long rows (cut into segments summed in a second pass)
-and many short ones.  Bound: max |out - ref| <= 1e-3 sqrt(C) and relative
+and many short ones; the four benchmarked row workloads run at full size,
+checked on sampled rows.  Bound: max |out - ref| <= 1e-3 sqrt(C) and relative
 error <= 1e-4 (the GEMM's, with K = C); small-integer inputs must match
 bit for bit, and repeated calls must agree bit for bit."""
 import json
@@ -152,3 +153,30 @@ def test_gemv_integer_exact_and_wrapper(b):
     check(y, ref, 3000, exact=True)
     y2 = b.gemv(A[:, ::1], x[::1])
     assert np.array_equal(y2.cpu().double().numpy(), y)
+
+
+@pytest.mark.parametrize("name", ["rowsum_8192x32768_f16", "rowsum_262144x1024_bf16",
+                                  "rowsum_4x33554432_f32", "gemv_16384x16384_f16"])
+def test_row_workloads_full_size_sampled(b, name):
+    """The benchmarked row workloads at full size through the C ABI, checked
+    against the oracle on sampled rows (all four of the long-row case)."""
+    from tiled_staged_matmul_gb300 import synthetic
+    w = synthetic.ROW_WORKLOADS[name]
+    X, x = w.operands()
+    dX = X.cuda()
+    out = torch.full((w.R + 4,), float("nan"), dtype=torch.float32, device="cuda")
+    if w.kind == "gemv":
+        dx = x.cuda()
+        b.check(b.gemv_f16_f32acc(dX.data_ptr(), dx.data_ptr(), out.data_ptr(), w.R, w.C, w.C, 1, 0))
+    else:
+        b.check(b.rowsum_f32acc(dX.data_ptr(), w.elem, out.data_ptr(), w.R, w.C, w.C, 1, 0))
+    b.check(b.gemm_get_device_status(0))
+    assert bool(torch.isnan(out[w.R:]).all()), "wrote past out"
+    got = out[:w.R].cpu().double().numpy()
+    rows = np.arange(w.R) if w.R <= 4 else np.unique(np.random.default_rng(5).integers(0, w.R, 64))
+    Xs = X[torch.from_numpy(rows)].contiguous()
+    if w.kind == "gemv":
+        ref = oracle.gemv_f64(bits_of(Xs).view(np.float16), bits_of(x).view(np.float16), len(rows), w.C)
+    else:
+        ref = oracle.rowsum_f64(bits_of(Xs), len(rows), w.C, w.C, 1, w.elem)
+    check(got[rows], ref, w.C)
