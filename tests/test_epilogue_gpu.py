@@ -220,3 +220,23 @@ def test_activation_accuracy_on_its_own(b, act):
     bound = 2e-6 * np.maximum(1.0, np.abs(xs.astype(np.float64)))
     worst = int(np.argmax(err - bound))
     assert np.all(err <= bound), (act, float(xs[worst]), float(got[worst]), float(want[worst]))
+
+
+@pytest.mark.parametrize("name", ["gemm_4096x4096x4096_normal_invsqrtk", "gemm_256x256x65536_uniform",
+                                  "gemm_8192x8192x8192_normal_invsqrtk"])
+def test_benchmarked_epilogue_full_size_sampled(b, name):
+    """The fused epilogue the bench times (bias + GELU into bf16) at the
+    workloads' full sizes and in their default plans, on sampled cells and
+    the corners."""
+    w = synthetic.WORKLOADS[name]
+    A, B = synthetic.workload_operands(w)
+    bias = np.linspace(-1, 1, w.N).astype(np.float32)
+    C, pad_ok = run_fused(b, A, B, alpha=1.0, bias=bias, act="gelu", out="bf16")
+    rng = np.random.default_rng(11)
+    rows = rng.integers(0, w.M, 4096)
+    cols = rng.integers(0, w.N, 4096)
+    rows[:4] = [0, 0, w.M - 1, w.M - 1]
+    cols[:4] = [0, w.N - 1, 0, w.N - 1]
+    acc = oracle.gemm_cells(A, B, w.M, w.N, w.K, rows, cols)
+    check_epilogue(C[rows, cols], acc, 1.0, bias.astype(np.float64)[cols], "gelu", "bf16", w.K)
+    assert pad_ok
