@@ -80,6 +80,17 @@ def test_4096_cube(b):
     assert dC.outside_untouched()
 
 
+def test_4096_cube_integer_bit_exact(b):
+    """The integer twin at full size in the default plan (the last wave's
+    tiles split along K and summed in the kernel): exact in f32."""
+    w = integer_twin(WORKLOADS["gemm_4096x4096x4096_normal_invsqrtk"])
+    assert b.gemm_plan(w.M, w.N, w.K)["tail_split"] >= 2
+    A, B = synthetic.workload_operands(w)
+    C, dC = run_gemm(b, A, B)
+    check_exact(C.numpy(), ref_of(A, B))
+    assert dC.outside_untouched()
+
+
 def test_long_K_split(b):
     w = WORKLOADS["gemm_256x256x65536_uniform"]
     plan = b.gemm_plan(w.M, w.N, w.K)
