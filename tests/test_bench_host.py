@@ -68,3 +68,16 @@ def test_peak_follows_the_regime():
     hbm = bench.roofline_of(2 * 256 * 256 * 65536, 67 * 2 ** 20, 0.027, None, "k",
                             {"sm_mhz": 1525.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]})
     assert hbm["bound"] == "hbm" and hbm["peak"] == peaks["hbm_gbs"]
+
+
+def test_burst_object_uses_the_burst_peak():
+    with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+        peaks = json.load(f)
+    flops = 2 * 8192 ** 3
+    bo = bench.burst_of(flops, 8192 * 8192 * 8, 0.655)
+    assert bo["steps"] == 30 and bo["bound"] == "tensor" and bo["peak"] == peaks["bf16_tflops"]
+    assert bo["value"] == pytest.approx(flops / 0.655e-3 / 1e12, rel=1e-4)
+    assert bo["roofline_frac"] == pytest.approx(bo["value"] / peaks["bf16_tflops"], abs=1e-4)
+    # a bandwidth-bound shape against the copy bandwidth
+    lk = bench.burst_of(2 * 256 * 256 * 65536, 67 * 2 ** 20, 0.027)
+    assert lk["bound"] == "hbm" and lk["peak"] == peaks["hbm_gbs"]
