@@ -389,7 +389,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const ge
             if (st >= 2 && st <= 256 && rows_per * tn * 4 * st <= int64_t(b.stages) * b.stage_bytes)
                 ks = Tail{int(st), false, 1.0 / double(st) + 6.0 / tile_us};
         }
-        Tail ns;  // column slices of at least 64 B columns per CTA
+        Tail ns;  // column slices of at least 64 columns of B per CTA
         if (mode != 1) {
             const int b_cols = tm == 2 * kTileM ? tn / 2 : tn;
             int n = 1;
@@ -413,8 +413,8 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const ge
             best = ns;
         return best;
     };
-    // Long K on a small output: the split-K regime.  Pick the tile that moves
-    // the fewest bytes from L2 into shared memory, partials included.
+    // Long K on a small output: the split-K regime (costed below by per-SM
+    // time, partial sums included).
     const bool long_k = req_s == 0 && K > 0 && k_blocks >= 16 &&
                         tiles_of(2 * kTileM, 256) * 2 <= slots_of(2 * kTileM);
     const TileChoice *best = nullptr;
