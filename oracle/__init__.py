@@ -205,6 +205,16 @@ ACTIVATIONS = ("none", "relu", "leaky_relu", "gelu", "gelu_tanh", "silu")
 OUT_TYPES = ("f32", "f16", "bf16")
 
 
+def _erf(x: np.ndarray) -> np.ndarray:
+    """erf elementwise in fp64: scipy's vectorised routine where scipy is
+    installed, else the standard library's, one element at a time."""
+    try:
+        from scipy.special import erf
+    except ImportError:
+        return np.vectorize(math.erf, otypes=[np.float64])(x)
+    return erf(x)
+
+
 def activation_f64(x: np.ndarray, name: str, slope: float = 0.01) -> np.ndarray:
     """The activations a fused epilogue may apply, in fp64, each written from
     its mathematical definition (the pages name an ``ACTIVATION`` meta-
@@ -224,8 +234,7 @@ def activation_f64(x: np.ndarray, name: str, slope: float = 0.01) -> np.ndarray:
     if name == "leaky_relu":
         return np.where(x > 0, x, slope * x)
     if name == "gelu":
-        erf = np.vectorize(math.erf, otypes=[np.float64])
-        return 0.5 * x * (1.0 + erf(x / math.sqrt(2.0)))
+        return 0.5 * x * (1.0 + _erf(x / math.sqrt(2.0)))
     if name == "gelu_tanh":
         return 0.5 * x * (1.0 + np.tanh(math.sqrt(2.0 / math.pi) * (x + 0.044715 * x ** 3)))
     if name == "silu":
