@@ -131,6 +131,17 @@ typedef struct gemm_options {
                            stage does not apply to the CTA's role).  For profiling only:
                            the timer ticks in steps of about a quarter microsecond and
                            stamps of different warps are not ordered within a step. */
+    int32_t red_cluster; /* split-K summed inside the kernel with one CTA per tile: 0 or 1:
+                            off (measured slower on GB300, so never the planner's choice); 2
+                            or 4, when the plan allows it: the grid runs in clusters of that
+                            many CTAs holding consecutive K ranges of one tile, which add their
+                            partials on chip (distributed shared memory) before one partial
+                            per cluster goes through the workspace.  The sum is then taken in
+                            a fixed two-level order -- the cluster's ranges in ascending
+                            order, then the clusters in ascending order -- so a given plan is
+                            bitwise reproducible and integer-valued inputs are exact, but
+                            random inputs may differ in the last bits from a plan that sums
+                            the ranges one by one. */
 } gemm_options_t;
 
 /* What the planner chose for a problem (see gemm_plan). */
@@ -157,6 +168,8 @@ typedef struct gemm_plan_info {
     int32_t tail_split;
     int32_t tail_narrow;  /* 1: the pieces are column slices of tile_n / tail_split columns over
                              all of K; 0: K ranges summed in the kernel */
+    int32_t red_cluster;  /* > 1: split-K partials are first added on chip in clusters of this
+                             many CTAs (see gemm_options_t.red_cluster); 1: not */
 } gemm_plan_info_t;
 
 /* C = A . B for one matrix.
@@ -322,8 +335,7 @@ gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int64_t batch,
                         gemm_plan_info_t *plan);
 
 /* C = A . B like gemm_f16_f32acc, for callers that cannot allocate device
- * memory while they run: code being captured into a CUDA graph that must not
- * gain allocation nodes, allocators or memory managers that call into this
+ * memory while they run: allocators or memory managers that call into this
  * library and may not re-enter themselves, and hosts that reserved all of
  * the GPU's memory in advance.  The paper has no counterpart to this entry
  * point; it exists for those callers only.

@@ -58,7 +58,7 @@ class DeviceMatrix:
 
 def run_gemm(b, A: torch.Tensor, B: torch.Tensor, *, lda=None, ldb=None, ldc=None, batch=1,
              sA=None, sB=None, sC=None, split_k=0, tile_n=0, tile_m=0, splitk_reduce=0,
-             split_tail=0, stream=None):
+             split_tail=0, red_cluster=0, stream=None):
     """A: (batch,) M x K f16 CPU, B: (batch,) K x N f16 CPU.  Runs the GEMM
     through the C ABI on padded device buffers and returns (C as a CPU f32
     tensor of shape (batch,) M x N, the output DeviceMatrix)."""
@@ -72,6 +72,7 @@ def run_gemm(b, A: torch.Tensor, B: torch.Tensor, *, lda=None, ldb=None, ldc=Non
     dC = DeviceMatrix(None, M, N, ldc, torch.float32, SENTINEL, batch, sC,
                       inner_fill=float("nan"))
     opts = b.GemmOptions(split_k, tile_n, 0, 0, tile_m, splitk_reduce, 0, split_tail)
+    opts.red_cluster = red_cluster
     s = torch.cuda.current_stream() if stream is None else stream
     st = b.gemm_f16_f32acc_opts(dA.ptr(), dB.ptr(), dC.ptr(), M, N, K, lda, ldb, ldc,
                                 dA.stride if batch > 1 else 0, dB.stride if batch > 1 else 0,

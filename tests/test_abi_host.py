@@ -177,6 +177,7 @@ def test_plan_invariants(b, M, N, K):
         assert p["units"] == tiles * p["split_k"]
     if p["tile_m"] == 128:
         assert p["grid"] == min(p["units"], SMS)
+        assert p["red_cluster"] in (1, 2, 4)
     else:
         assert p["grid"] == 2 * min(p["units"], SMS // 2)
     ldw = -(-N // 4) * 4
@@ -188,6 +189,15 @@ def test_plan_invariants(b, M, N, K):
         assert p["workspace_bytes"] == p["tail_tiles"] * p["tail_split"] * tile_bytes + counters
     elif p["split_k"] == 1:
         assert p["workspace_bytes"] == 0 and not p["fused_reduce"]
+    elif p["fused_reduce"] and p["red_cluster"] > 1:
+        # cluster sum: one compact partial tile per cluster (none with one
+        # cluster per tile), one arrival counter per tile and cluster rank
+        cl = p["red_cluster"]
+        assert p["tile_m"] == 128 and p["split_k"] % cl == 0 and p["grid"] % cl == 0
+        groups = p["split_k"] // cl
+        counters = -(-(tiles * cl * 4) // 16) * 16 + 16  # + launch tag
+        assert p["workspace_bytes"] == tiles * (groups if groups > 1 else 0) * tile_bytes + counters
+        assert p["units"] == p["grid"] and p["grid"] // cl <= (SMS // 4 * 18 // 19 if cl == 4 else SMS // 2)
     elif p["fused_reduce"]:
         # one compact partial tile per split unit, one arrival counter per tile;
         # every cluster owns exactly one unit
@@ -208,6 +218,66 @@ def test_long_K_small_output_splits_K(b):
 def test_large_square_uses_wide_tiles_without_split(b):
     p = b.gemm_plan(8192, 8192, 8192, 1, None, SMS)
     assert (p["tile_m"], p["tile_n"], p["split_k"]) == (256, 256, 1)  # CTA pairs
+
+
+def cluster_opts(b, red_cluster, split_k=0, tile_n=0):
+    o = b.GemmOptions()
+    o.split_k = split_k
+    o.red_cluster = red_cluster
+    if tile_n:
+        o.tile_m, o.tile_n = 128, tile_n
+    return o
+
+
+def test_long_K_small_output_sums_in_clusters_on_request(b):
+    # off unless asked for (measured slower than the split-by-split sum)
+    p = b.gemm_plan(256, 256, 65536, 1, None, SMS)
+    assert (p["tile_m"], p["tile_n"], p["red_cluster"], p["split_k"], p["grid"]) == (128, 128, 1, 38, 152)
+    # four 128 x 128 tiles; 36 four-CTA clusters fit on 152 SMs (the GPCs'
+    # SMs past a multiple of four stay idle): 9 clusters per tile, 36 K ranges
+    p = b.gemm_plan(256, 256, 65536, 1, cluster_opts(b, 4), SMS)
+    assert (p["tile_m"], p["tile_n"], p["red_cluster"], p["split_k"], p["grid"]) == (128, 128, 4, 36, 144)
+    # pairs: 76 clusters, 19 per tile
+    p = b.gemm_plan(256, 256, 65536, 1, cluster_opts(b, 2), SMS)
+    assert (p["red_cluster"], p["split_k"], p["grid"]) == (2, 38, 152)
+    # off: one partial per K range, as before
+    p = b.gemm_plan(256, 256, 65536, 1, cluster_opts(b, 1), SMS)
+    assert (p["red_cluster"], p["split_k"], p["grid"]) == (1, 38, 152) and p["fused_reduce"]
+
+
+def test_cluster_sum_with_a_requested_split(b):
+    # a split that is a multiple of the cluster and fits: kept
+    p = b.gemm_plan(256, 256, 65536, 1, cluster_opts(b, 4, 16, 128), SMS)
+    assert (p["red_cluster"], p["split_k"], p["grid"]) == (4, 16, 64)
+    # not a multiple of the cluster: summed split by split
+    p = b.gemm_plan(256, 256, 65536, 1, cluster_opts(b, 4, 38, 128), SMS)
+    assert (p["red_cluster"], p["split_k"]) == (1, 38)
+    # more clusters than fit at once: never (the CTAs wait for one another)
+    p = b.gemm_plan(256, 256, 65536, 1, cluster_opts(b, 4, 37 + 3, 128), SMS)
+    assert p["red_cluster"] == 1
+    # 128 x 256 tiles (two of them): 18 clusters each, 72 K ranges
+    p = b.gemm_plan(256, 256, 65536, 1, cluster_opts(b, 4, 0, 256), SMS)
+    assert (p["red_cluster"], p["split_k"], p["grid"]) == (4, 72, 144)
+    with pytest.raises(b.GemmError):
+        b.gemm_plan(256, 256, 65536, 1, cluster_opts(b, 3), SMS)
+
+
+def test_cluster_sum_of_one_cluster_per_tile(b):
+    # 16 k-blocks: one four-CTA cluster per tile holds the whole K (4 ranges
+    # of 4 k-blocks) and writes C itself -- no partials in the workspace
+    p = b.gemm_plan(128, 128, 1024, 1, cluster_opts(b, 4, 0, 128), SMS)
+    assert (p["red_cluster"], p["split_k"]) == (4, 4)
+    assert p["workspace_bytes"] == 16 + 16
+
+
+def test_no_cluster_sum_for_pairs_tails_or_the_separate_reduce(b):
+    assert b.gemm_plan(8192, 8192, 8192, 1, cluster_opts(b, 4), SMS)["red_cluster"] == 1
+    o = cluster_opts(b, 4)
+    o.splitk_reduce = 1
+    assert b.gemm_plan(256, 256, 65536, 1, o, SMS)["red_cluster"] == 1
+    o = cluster_opts(b, 4)
+    o.tile_m, o.tile_n = 256, 256
+    assert b.gemm_plan(512, 512, 65536, 1, o, SMS)["red_cluster"] == 1
 
 
 def test_forced_split_is_clamped_to_k_blocks(b):

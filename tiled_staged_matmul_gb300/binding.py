@@ -31,7 +31,7 @@ class GemmOptions(ctypes.Structure):
                 ("timeout_ms", ctypes.c_int32), ("inject_stall", ctypes.c_int32),
                 ("tile_m", ctypes.c_int32), ("splitk_reduce", ctypes.c_int32),
                 ("l2_prefetch", ctypes.c_int32), ("split_tail", ctypes.c_int32),
-                ("trace", ctypes.c_void_p)]
+                ("trace", ctypes.c_void_p), ("red_cluster", ctypes.c_int32)]
 
 
 ACTIVATIONS = {"none": 0, "relu": 1, "leaky_relu": 2, "gelu": 3, "gelu_tanh": 4, "silu": 5}
@@ -62,7 +62,8 @@ class GemmPlanInfo(ctypes.Structure):
                 ("group_m", ctypes.c_int32), ("stage_bytes", ctypes.c_int64),
                 ("smem_bytes", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
                 ("fused_reduce", ctypes.c_int32), ("tail_tiles", ctypes.c_int32),
-                ("tail_split", ctypes.c_int32), ("tail_narrow", ctypes.c_int32)]
+                ("tail_split", ctypes.c_int32), ("tail_narrow", ctypes.c_int32),
+                ("red_cluster", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}

@@ -65,6 +65,9 @@ gemm_status_t fail_cuda(cudaError_t e, const char *what)
 }
 
 constexpr int kMaxDevices = 64;
+// Dynamic shared memory of a GEMM CTA outside its operand ring and epilogue
+// buffers: the alignment slack and the control block (TileCfg).
+constexpr int64_t kSmemSlackAndControl = 1024 + 2048;
 constexpr int64_t kInt32Max = 2147483647;
 
 // ------------------------------------------------------------- driver entry points
@@ -107,9 +110,11 @@ struct DeviceState {
     int sms = 0;
     int cc_major = 0, cc_minor = 0;
     int smem_optin = 0;
-    bool attrs_set[10] = {};  // see config_index; +5 for the kernels with the fused epilogue
+    bool attrs_set[14] = {};  // see attr_index
     cudaMemPool_t pool = nullptr;
     uint32_t *status = nullptr;
+    // Clusters of 2 and of 4 CTAs of the cluster-sum kernel that fit at once.
+    int caps2 = 0, caps4 = 0;
 };
 
 DeviceState g_devices[kMaxDevices];
@@ -143,6 +148,12 @@ gemm_status_t device_state(int dev, DeviceState **out)
             return fail_cuda(e, "cudaMemPoolCreate(split-K workspace pool)");
         uint64_t keep = UINT64_MAX;  // keep freed workspace for the next call
         cudaMemPoolSetAttribute(s.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+        // Every CTA of an in-kernel split-K sum must be resident at once (they
+        // wait for one another), so the cluster sum is planned only within
+        // what the occupancy API says fits.
+        if ((e = cluster_capacity(128, 2, &s.caps2)) != cudaSuccess ||
+            (e = cluster_capacity(128, 4, &s.caps4)) != cudaSuccess)
+            return fail_cuda(e, "cudaOccupancyMaxActiveClusters(cluster split-K sum)");
         s.ready = true;
     }
     *out = &s;
@@ -155,6 +166,24 @@ int config_index(int tile_m, int tile_n)
     if (tile_m == 2 * kTileM)
         return tile_n == 128 ? 3 : 4;
     return tile_n == 64 ? 0 : tile_n == 128 ? 1 : 2;
+}
+
+// Slot of DeviceState::attrs_set: the plain kernels 0-4, with the fused
+// epilogue 5-9, the cluster-sum kernels (tile_n 128 / 256, plain or fused) 10-13.
+int attr_index(int tile_m, int tile_n, bool epi, int red_cluster)
+{
+    if (red_cluster > 1)
+        return 10 + (tile_n == 256 ? 1 : 0) + (epi ? 2 : 0);
+    return config_index(tile_m, tile_n) + (epi ? 5 : 0);
+}
+
+// Estimated clusters of `n` CTAs (one per SM) that fit at once on a GB300 of
+// `sms` SMs, for planning without a device: pairs fit everywhere; four-CTA
+// clusters leave the SMs of each GPC past a multiple of four idle (36 of 38
+// on the 152-SM part, as the occupancy API reports there).
+int estimated_cluster_capacity(int sms, int n)
+{
+    return n == 2 ? sms / 2 : sms / 4 * 18 / 19;
 }
 
 // ------------------------------------------------------------- argument checks
@@ -307,7 +336,7 @@ struct TileChoice {
 constexpr TileChoice kChoices[] = {{256, 256}, {256, 128}, {128, 256}, {128, 128}, {128, 64}};
 
 gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const gemm_options_t *o,
-                        int sms, gemm_plan_info_t *pl)
+                        int sms, int caps2, int caps4, gemm_plan_info_t *pl)
 {
     if (sms <= 0)
         return fail(GEMM_ERR_INVALID_VALUE, "SM count must be positive");
@@ -329,6 +358,9 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const ge
         return fail(GEMM_ERR_INVALID_VALUE, "splitk_reduce must be 0, 1 or 2");
     if (o && (o->split_tail < 0 || o->split_tail > 3))
         return fail(GEMM_ERR_INVALID_VALUE, "split_tail must be 0, 1, 2 or 3");
+    const int req_c = o ? o->red_cluster : 0;
+    if (req_c != 0 && req_c != 1 && req_c != 2 && req_c != 4)
+        return fail(GEMM_ERR_INVALID_VALUE, "red_cluster must be 0, 1, 2 or 4 (got %d)", req_c);
     const int k_blocks = ceil_div(std::max<int64_t>(K, 1), kTileK);
     const int64_t Mx = std::max<int64_t>(M, 1), Nx = std::max<int64_t>(N, 1);
     const int64_t ldw = (N + 3) / 4 * 4;
@@ -462,7 +494,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const ge
     if (!best)
         return fail(GEMM_ERR_INVALID_VALUE, "no tile shape matches tile_m=%d tile_n=%d", req_m, req_n);
     const int tm = best->tile_m, bn = best->tile_n;
-    const int split = K == 0 ? 1 : split_for(tm, bn);
+    int split = K == 0 ? 1 : split_for(tm, bn);
     const int64_t tiles = tiles_of(tm, bn);
     const SmemBudget sb = smem_budget(tm, bn);
     pl->tile_m = tm;
@@ -504,15 +536,56 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const ge
             pl->fused_reduce = tl.narrow ? 0 : 1;
         }
     }
+    // Cluster split-K sum (one CTA per tile, every unit a K range summed in
+    // the kernel): clusters of CL CTAs hold CL consecutive K ranges of a tile
+    // and add them on chip, so only split / CL partials per tile go through
+    // the workspace.  The split becomes a multiple of CL that keeps every
+    // cluster resident at once (the occupancy API's count), at least 4
+    // k-blocks per range.  The idle ring and the epilogue buffers must hold
+    // CL receive slots of tile_m / CL rows and the CL - 1 slots a CTA sends,
+    // and the slots one reducer's rows of the tile's cluster partials.
+    pl->red_cluster = 1;
+    // Opt-in: on GB300 the exchange through distributed shared memory costs
+    // more than the smaller workspace traffic saves (256 x 256 x 65536:
+    // 28.7 us in pairs and 29.8 us in 4-CTA clusters against 27.7 us summed
+    // split by split, interleaved on one box), so the planner leaves it off.
+    if (pl->fused_reduce && split > 1 && pl->tail_split == 0 && tm == kTileM &&
+        (bn == 128 || bn == 256) && (req_c == 2 || req_c == 4)) {
+        const int cl = req_c;
+        const int64_t cap = cl == 4 ? caps4 : caps2;
+        int s2 = 0;
+        if (req_s > 0)
+            s2 = (split % cl == 0 && tiles * split <= cap * cl) ? split : 0;
+        else
+            s2 = int(std::min<int64_t>(cap / tiles, k_blocks / (4 * cl))) * cl;
+        if (s2 >= cl) {
+            const int64_t G = s2 / cl;
+            const int64_t rows_own = kTileM / cl;
+            const int64_t rp = (rows_own + G - 1) / G;
+            const int64_t slot = rows_own * bn * 4;
+            const int64_t room = sb.smem_bytes - kSmemSlackAndControl;  // ring + epilogue buffers
+            if (G <= 256 && (2 * cl - 1) * slot <= room && rp * G <= kTileM) {
+                split = s2;
+                pl->split_k = s2;
+                pl->units = tiles * s2;
+                pl->grid = int(pl->units);
+                pl->red_cluster = cl;
+            }
+        }
+    }
     // Split partials: in-kernel sums use a compact [split unit][tile_m][tile_n]
-    // workspace plus a counter per split tile and a 16-byte launch tag; the
-    // reduce kernel reads
-    // [batch * split][M][ldw].
+    // workspace (with a cluster sum: [tile * clusters per tile + g]) plus a
+    // counter per split tile (per tile and cluster rank) and a 16-byte launch
+    // tag; the reduce kernel reads [batch * split][M][ldw].
     const bool ktail = pl->tail_split && !pl->tail_narrow;
     const int64_t split_tiles = ktail ? pl->tail_tiles : (split > 1 ? tiles : 0);
     const int64_t split_units = ktail ? split_tiles * pl->tail_split : split_tiles * split;
     if (split == 1 && !ktail)
         pl->workspace_bytes = 0;
+    else if (pl->red_cluster > 1)
+        pl->workspace_bytes = split_tiles * (split / pl->red_cluster > 1 ? split / pl->red_cluster : 0) *
+                                  tile_elems_of(tm, bn) * 4 +
+                              (split_tiles * pl->red_cluster * 4 + 15) / 16 * 16 + 16;
     else if (pl->fused_reduce)
         pl->workspace_bytes = split_units * tile_elems_of(tm, bn) * 4 + (split_tiles * 4 + 15) / 16 * 16 + 16;
     else
@@ -522,12 +595,46 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const ge
 
 // ------------------------------------------------------------- tensor maps
 
+// Encoding a tensor map is a pure function of its arguments, so each host
+// thread keeps its last few maps and hands back the same 128 bytes when a
+// call repeats a layout (the usual case: the same operands, or the same
+// shapes at the same addresses from a caching allocator).  Nothing about the
+// memory behind the address is remembered -- only what the encoder was told.
+struct MapKey {
+    uint64_t base;
+    int64_t cols, rows, mats, ld, stride;
+    uint32_t box_cols, box_rows, box_mats;
+    int32_t dt, elem, promo, swizzle;
+    bool operator==(const MapKey &o) const
+    {
+        return base == o.base && cols == o.cols && rows == o.rows && mats == o.mats && ld == o.ld &&
+               stride == o.stride && box_cols == o.box_cols && box_rows == o.box_rows &&
+               box_mats == o.box_mats && dt == o.dt && elem == o.elem && promo == o.promo &&
+               swizzle == o.swizzle;
+    }
+};
+struct MapCacheEntry {
+    MapKey key;
+    alignas(64) CUtensorMap map;
+};
+constexpr int kMapCacheEntries = 16;
+thread_local MapCacheEntry t_map_cache[kMapCacheEntries];
+thread_local int t_map_cache_used = 0, t_map_cache_next = 0;
+
 gemm_status_t encode_3d(CUtensorMap *map, CUtensorMapDataType dt, int elem, const void *base,
                         int64_t cols, int64_t rows, int64_t mats, int64_t ld, int64_t stride,
                         uint32_t box_cols, uint32_t box_rows, CUtensorMapL2promotion promo,
                         const char *name, uint32_t box_mats = 1,
                         CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B)
 {
+    const MapKey key{uint64_t(reinterpret_cast<uintptr_t>(base)), cols, rows, mats, ld, stride,
+                     box_cols, box_rows, box_mats, int32_t(dt), elem, int32_t(promo), int32_t(swizzle)};
+    for (int i = 0; i < t_map_cache_used; ++i) {
+        if (t_map_cache[i].key == key) {
+            *map = t_map_cache[i].map;
+            return GEMM_OK;
+        }
+    }
     Driver &d = driver();
     if (!d.loaded)
         return fail(GEMM_ERR_CUDA, "%s", d.error.c_str());
@@ -540,6 +647,12 @@ gemm_status_t encode_3d(CUtensorMap *map, CUtensorMapDataType dt, int elem, cons
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(GEMM_ERR_INVALID_VALUE, "tensor map for %s rejected (CUresult %d)", name, int(r));
+    MapCacheEntry &slot = t_map_cache[t_map_cache_next];
+    slot.key = key;
+    slot.map = *map;
+    t_map_cache_next = (t_map_cache_next + 1) % kMapCacheEntries;
+    if (t_map_cache_used < kMapCacheEntries)
+        ++t_map_cache_used;
     return GEMM_OK;
 }
 
@@ -681,14 +794,14 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
     }
     gemm_plan_info_t pl;
     if ((st = make_plan(pr.M, pr.N, pr.K, pr.batch, (o || pr.group_rows) ? &og : nullptr, ds->sms,
-                        &pl)) != GEMM_OK)
+                        ds->caps2, ds->caps4, &pl)) != GEMM_OK)
         return st;
     if (ds->smem_optin < pl.smem_bytes)
         return fail(GEMM_ERR_UNSUPPORTED_DEVICE, "device allows %d bytes of shared memory per block, the kernel needs %lld",
                     ds->smem_optin, (long long)pl.smem_bytes);
-    const int ti = config_index(pl.tile_m, pl.tile_n) + (use_epi ? 5 : 0);
+    const int ti = attr_index(pl.tile_m, pl.tile_n, use_epi, pl.red_cluster);
     if (!ds->attrs_set[ti]) {
-        if ((e = set_kernel_attributes(pl.tile_m, pl.tile_n, use_epi)) != cudaSuccess)
+        if ((e = set_kernel_attributes(pl.tile_m, pl.tile_n, use_epi, pl.red_cluster)) != cudaSuccess)
             return fail_cuda(e, "cudaFuncSetAttribute(max dynamic shared memory)");
         ds->attrs_set[ti] = true;
     }
@@ -760,8 +873,8 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
             kp.narrow = pl.tail_split;
             kp.dp_units = int64_t(pl.tiles_m) * pl.tiles_n * pr.batch - pl.tail_tiles;
         }
-        if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, use_epi, map_a, map_b, map_out, map_out, map_out, kp,
-                                     pl.grid, stream)) != cudaSuccess)
+        if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, use_epi, 1, map_a, map_b, map_out, map_out,
+                                     map_out, kp, pl.grid, stream)) != cudaSuccess)
             return fail_cuda(e, "GEMM kernel launch");
         return GEMM_OK;
     }
@@ -775,8 +888,12 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
         const int32_t S = tail ? pl.tail_split : pl.split_k;
         const int64_t tiles = int64_t(pl.tiles_m) * pl.tiles_n * pr.batch;
         const int64_t split_tiles = tail ? pl.tail_tiles : tiles;
-        const int64_t split_units = split_tiles * S;
+        const int32_t CL = pl.red_cluster;
+        const int32_t G = S / CL;  // partials per tile in the workspace (clusters per tile)
+        // With a cluster sum and one cluster per tile nothing goes through the workspace.
+        const int64_t split_units = split_tiles * (CL > 1 && G == 1 ? 0 : G);
         const int64_t tile_elems = int64_t(pl.tile_m) * pl.tile_n;
+        const int64_t counter_words = split_tiles * CL;
         void *ws = nullptr;
         if ((e = cudaMallocFromPoolAsync(&ws, size_t(pl.workspace_bytes), ds->pool, stream)) != cudaSuccess)
             return fail_cuda(e, "split-K workspace allocation");
@@ -784,12 +901,19 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
         kp.fused = 1;
         kp.split_k = S;
         kp.dp_units = tail ? tiles - split_tiles : 0;
-        kp.reducers = int32_t(S * cpu);
-        kp.rows_per = int32_t((pl.tile_m + kp.reducers - 1) / kp.reducers);
+        kp.red_cluster = CL;
+        kp.red_groups = G;
+        if (CL > 1) {
+            kp.reducers = G;
+            kp.rows_per = (kTileM / CL + G - 1) / G;
+        } else {
+            kp.reducers = int32_t(S * cpu);
+            kp.rows_per = int32_t((pl.tile_m + kp.reducers - 1) / kp.reducers);
+        }
         kp.counters = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + split_units * tile_elems * 4);
-        kp.counter_words = int32_t(split_tiles);
+        kp.counter_words = int32_t(counter_words);
         kp.epoch_tag = reinterpret_cast<unsigned long long *>(
-            static_cast<char *>(ws) + split_units * tile_elems * 4 + (split_tiles * 4 + 15) / 16 * 16);
+            static_cast<char *>(ws) + split_units * tile_elems * 4 + (counter_words * 4 + 15) / 16 * 16);
         kp.epoch = next_launch_epoch();
         kp.timeout_ns = uint64_t(timeout_ns_for(o, pl));
         alignas(64) CUtensorMap map_ws, map_red;
@@ -800,18 +924,21 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
         }
         const int64_t map_cols = kp.n_tma > 0 ? kp.n_tma : pr.N;
         st = encode_out(&map_out, map_cols);
+        // (A cluster sum with one cluster per tile uses neither workspace
+        // map; they still need a valid extent to be prefetched.)
+        const int64_t ws_mats = std::max<int64_t>(split_units, 1);
         if (st == GEMM_OK)
             st = encode_3d(&map_ws, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ws, pl.tile_n, pl.tile_m,
-                           split_units, pl.tile_n, tile_elems, 32, 32,
+                           ws_mats, pl.tile_n, tile_elems, 32, 32,
                            CU_TENSOR_MAP_L2_PROMOTION_NONE, "split-K workspace");
         if (st == GEMM_OK)
             st = encode_3d(&map_red, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ws, pl.tile_n, pl.tile_m,
-                           split_units, pl.tile_n, tile_elems, uint32_t(pl.tile_n),
+                           ws_mats, pl.tile_n, tile_elems, uint32_t(pl.tile_n),
                            uint32_t(kp.rows_per), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                           "split-K workspace (reduce)", uint32_t(S), CU_TENSOR_MAP_SWIZZLE_NONE);
+                           "split-K workspace (reduce)", uint32_t(G), CU_TENSOR_MAP_SWIZZLE_NONE);
         if (st == GEMM_OK &&
-            (e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, use_epi, map_a, map_b, map_out, map_ws, map_red, kp,
-                                     pl.grid, stream)) != cudaSuccess)
+            (e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, use_epi, CL, map_a, map_b, map_out, map_ws,
+                                     map_red, kp, pl.grid, stream)) != cudaSuccess)
             st = fail_cuda(e, "GEMM kernel launch");
         cudaFreeAsync(ws, stream);
         return st;
@@ -828,15 +955,15 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
     // The GEMM writes raw partials (the plain kernel); the reduce applies
     // the epilogue to the sums.
     kp.epi = Epilogue{};
-    if (st == GEMM_OK && !ds->attrs_set[config_index(pl.tile_m, pl.tile_n)]) {
+    if (st == GEMM_OK && !ds->attrs_set[attr_index(pl.tile_m, pl.tile_n, false, 1)]) {
         if ((e = set_kernel_attributes(pl.tile_m, pl.tile_n, false)) != cudaSuccess)
             st = fail_cuda(e, "cudaFuncSetAttribute(max dynamic shared memory)");
         else
-            ds->attrs_set[config_index(pl.tile_m, pl.tile_n)] = true;
+            ds->attrs_set[attr_index(pl.tile_m, pl.tile_n, false, 1)] = true;
     }
     if (st == GEMM_OK) {
-        if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, false, map_a, map_b, map_out, map_out, map_out, kp,
-                                     pl.grid, stream)) != cudaSuccess)
+        if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, false, 1, map_a, map_b, map_out, map_out,
+                                     map_out, kp, pl.grid, stream)) != cudaSuccess)
             st = fail_cuda(e, "GEMM kernel launch");
     }
     if (st == GEMM_OK) {
@@ -1155,7 +1282,19 @@ gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const ge
         if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
             return fail_cuda(e, "cudaDeviceGetAttribute(SM count)");
     }
-    return make_plan(M, N, K, std::max<int64_t>(batch, 1), opts, sms, plan);
+    // Cluster capacities of the current device when planning for it, else
+    // the GB300 estimate for the given SM count.
+    int caps2 = estimated_cluster_capacity(sms, 2), caps4 = estimated_cluster_capacity(sms, 4);
+    if (num_sms <= 0) {
+        int dev = 0;
+        DeviceState *ds = nullptr;
+        if (cudaGetDevice(&dev) == cudaSuccess && device_state(dev, &ds) == GEMM_OK) {
+            caps2 = ds->caps2;
+            caps4 = ds->caps4;
+        }
+        g_last_error.clear();
+    }
+    return make_plan(M, N, K, std::max<int64_t>(batch, 1), opts, sms, caps2, caps4, plan);
 }
 
 gemm_status_t gemm_get_device_status(gemm_stream_t stream)
@@ -1270,6 +1409,22 @@ gemm_status_t noalloc_setup(int dev, NoAllocDevice **out)
     return GEMM_OK;
 }
 
+// The kernel's shared-memory limit, set once per device and tile shape
+// (under the same lock as the set-up, so two host threads making their first
+// calls at once do not both write the flag).
+gemm_status_t noalloc_kernel_attributes(NoAllocDevice *nd, int tile_m, int tile_n)
+{
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    const int ti = config_index(tile_m, tile_n);
+    if (!nd->attrs_set[ti]) {
+        const cudaError_t e = set_kernel_attributes(tile_m, tile_n, false);
+        if (e != cudaSuccess)
+            return fail_cuda(e, "cudaFuncSetAttribute(max dynamic shared memory)");
+        nd->attrs_set[ti] = true;
+    }
+    return GEMM_OK;
+}
+
 }  // namespace
 }  // namespace tsm
 
@@ -1314,13 +1469,13 @@ extern "C" gemm_status_t gemm_f16_f32acc_splitk_noalloc(const uint16_t *A, const
     o.split_k = split_k;
     o.splitk_reduce = 1;  // partials in the scratch, summed by the separate reduce kernel
     gemm_plan_info_t pl;
-    if ((st = make_plan(M, N, K, 1, &o, nd->sms, &pl)) != GEMM_OK)
+    if ((st = make_plan(M, N, K, 1, &o, nd->sms, 0, 0, &pl)) != GEMM_OK)
         return st;
     if (split_k == 0 && uint64_t(pl.workspace_bytes) > kNoAllocScratchBytes) {
         // The planner's split does not fit: take the largest split that does.
         const int64_t per_split = M * ((N + 3) / 4 * 4) * 4;
         o.split_k = int32_t(std::max<int64_t>(1, int64_t(kNoAllocScratchBytes) / per_split));
-        if ((st = make_plan(M, N, K, 1, &o, nd->sms, &pl)) != GEMM_OK)
+        if ((st = make_plan(M, N, K, 1, &o, nd->sms, 0, 0, &pl)) != GEMM_OK)
             return st;
     }
     if (uint64_t(pl.workspace_bytes) > kNoAllocScratchBytes)
@@ -1332,12 +1487,8 @@ extern "C" gemm_status_t gemm_f16_f32acc_splitk_noalloc(const uint16_t *A, const
     if (nd->smem_optin < pl.smem_bytes)
         return fail(GEMM_ERR_UNSUPPORTED_DEVICE, "device allows %d bytes of shared memory per block, the kernel needs %lld",
                     nd->smem_optin, (long long)pl.smem_bytes);
-    const int ti = config_index(pl.tile_m, pl.tile_n);
-    if (!nd->attrs_set[ti]) {
-        if ((e = set_kernel_attributes(pl.tile_m, pl.tile_n, false)) != cudaSuccess)
-            return fail_cuda(e, "cudaFuncSetAttribute(max dynamic shared memory)");
-        nd->attrs_set[ti] = true;
-    }
+    if ((st = noalloc_kernel_attributes(nd, pl.tile_m, pl.tile_n)) != GEMM_OK)
+        return st;
 
     alignas(64) CUtensorMap map_a, map_b, map_out;
     if ((st = encode_3d(&map_a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, A, K, M, 1, lda, M * lda, kTileK,
@@ -1381,7 +1532,8 @@ extern "C" gemm_status_t gemm_f16_f32acc_splitk_noalloc(const uint16_t *A, const
             kp.narrow = pl.tail_split;
             kp.dp_units = int64_t(pl.tiles_m) * pl.tiles_n - pl.tail_tiles;
         }
-        if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, false, map_a, map_b, map_out, map_out, map_out, kp, pl.grid, stream)) != cudaSuccess)
+        if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, false, 1, map_a, map_b, map_out, map_out,
+                                     map_out, kp, pl.grid, stream)) != cudaSuccess)
             return fail_cuda(e, "GEMM kernel launch");
         return GEMM_OK;
     }
@@ -1393,7 +1545,8 @@ extern "C" gemm_status_t gemm_f16_f32acc_splitk_noalloc(const uint16_t *A, const
                         ldw, M * ldw, 32, 32, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                         "static split-K scratch")) != GEMM_OK)
         return st;
-    if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, false, map_a, map_b, map_out, map_out, map_out, kp, pl.grid, stream)) != cudaSuccess)
+    if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, false, 1, map_a, map_b, map_out, map_out,
+                                 map_out, kp, pl.grid, stream)) != cudaSuccess)
         return fail_cuda(e, "GEMM kernel launch");
     const int64_t threads = M * ((N + 3) / 4);
     const int grid = int(std::min<int64_t>((threads + 255) / 256, int64_t(nd->sms) * 8));

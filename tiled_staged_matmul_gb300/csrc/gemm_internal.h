@@ -77,6 +77,19 @@ struct KernelParams {
     int32_t fused;
     int32_t reducers;
     int32_t rows_per;
+    // Cluster split-K sum (with `fused`, every unit a split unit): the grid
+    // runs in clusters of red_cluster CTAs (2 or 4) holding red_cluster
+    // consecutive K ranges of one tile; CTA rank r of a cluster owns tile rows
+    // [r * tile_m / red_cluster, (r + 1) * tile_m / red_cluster), receives
+    // those rows of the other CTAs' partials through distributed shared
+    // memory and adds them in ascending rank.  The tile's red_groups =
+    // split_k / red_cluster cluster partials then go through the compact
+    // workspace ([tile * red_groups + g][tile_m][tile_n]) and are summed as
+    // above in ascending g, rows_per rows per reducer; counters then hold one
+    // word per (tile, rank).  With red_groups == 1 the cluster writes C.
+    // 1: off.
+    int32_t red_cluster;
+    int32_t red_groups;
     // With `fused`, units [0, dp_units) are whole tiles written straight to C
     // (the full waves of a "split tail" plan) and units from dp_units on are
     // split units, tile-major: unit dp_units + j computes split j % split_k
@@ -132,8 +145,14 @@ SmemBudget smem_budget(int tile_m, int tile_n);
 // Kernel-side entry points (defined in gemm_kernels.cu).
 // `epi`: the kernel built with the fused epilogue (any Epilogue), else the
 // plain one (identity Epilogue only).
-cudaError_t set_kernel_attributes(int tile_m, int tile_n, bool epi);
-cudaError_t launch_tcgen05_gemm(int tile_m, int tile_n, bool epi, const CUtensorMap &map_a,
+// `red_cluster` > 1: the kernel built for the cluster split-K sum, launched in
+// clusters of that many CTAs (one CTA per tile only).
+cudaError_t set_kernel_attributes(int tile_m, int tile_n, bool epi, int red_cluster = 1);
+// Clusters of `red_cluster` CTAs of the cluster-sum kernel (tile_n columns)
+// that fit on the device at once (cudaOccupancyMaxActiveClusters).
+cudaError_t cluster_capacity(int tile_n, int red_cluster, int *clusters);
+cudaError_t launch_tcgen05_gemm(int tile_m, int tile_n, bool epi, int red_cluster,
+                                const CUtensorMap &map_a,
                                 const CUtensorMap &map_b, const CUtensorMap &map_out,
                                 const CUtensorMap &map_ws, const CUtensorMap &map_red,
                                 const KernelParams &p, int grid, cudaStream_t stream);

@@ -71,7 +71,7 @@ struct TileCfg {
         (SMEM_LIMIT - ALIGN_SLACK - EPI_BYTES - CTRL_BYTES) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
     static_assert(STAGES >= 2, "the ring needs at least two stages");
-    static_assert(16 * STAGES + 80 <= GROUP_TABLE_OFF &&
+    static_assert(16 * STAGES + 88 <= GROUP_TABLE_OFF &&
                       GROUP_TABLE_OFF + 4 * kMaxGroupsPerLaunch <= CTRL_BYTES,
                   "control block layout");
     static constexpr int SMEM_BYTES = ALIGN_SLACK + STAGES * STAGE_BYTES + EPI_BYTES + CTRL_BYTES;
@@ -357,15 +357,20 @@ struct AbortFlags {
 
 // Bounded mbarrier wait.  Returns false if the CTA's abort flag is raised
 // (when `honor_abort`) or if `timeout_ns` passes; a timeout raises the flags
-// and ORs `who` into the device status word.
+// and ORs `who` into the device status word.  CLUSTER_ACQ: the wait acquires
+// at cluster scope (for data other CTAs of the cluster counted on `bar`).
+template <bool CLUSTER_ACQ = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const AbortFlags &af,
                                              uint32_t who, bool honor_abort)
 {
-    if (ptx::mbar_try_wait(bar, parity))
+    auto try_wait = [&]() {
+        return CLUSTER_ACQ ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
+    };
+    if (try_wait())
         return true;
     const uint64_t t0 = ptx::globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (ptx::mbar_try_wait(bar, parity))
+        if (try_wait())
             return true;
         if ((it & 31u) == 0) {
             if (honor_abort && *af.local)
@@ -477,9 +482,265 @@ __device__ __forceinline__ void trace_stamp(const KernelParams &p, int slot)
         p.trace[int64_t(blockIdx.x) * kTraceSlots + slot] = ptx::globaltimer_ns();
 }
 
+// ------------------------------------------------------------- cluster split-K sum
+
+// The epilogue of the cluster split-K sum (warps 2..5; one split unit per
+// CTA, clusters of CL = p.red_cluster CTAs holding CL consecutive K ranges
+// of one 128-row tile, every CTA of the launch resident at once).
+//
+//  1. Once its accumulator is complete, every MMA that read the CTA's operand
+//     ring has finished, so the ring is idle: the CTA tells its peers so.
+//  2. CTA rank r owns tile rows [r * 128 / CL, (r + 1) * 128 / CL).  Each
+//     epilogue warp reads its 32 TMEM rows box by box (32 x 32 f32, in the
+//     128-byte swizzled layout of the C boxes): an owner's own rows go into
+//     its slot for its own rank; other rows are staged in the idle ring past
+//     the slots and sent to the owner's slot for this rank with one bulk copy
+//     per box (cp.async.bulk into distributed shared memory), counted on the
+//     owner's recv_full.
+//  3. The owner adds its CL slots in ascending rank (= split) order.  With one
+//     cluster per tile that is C (through the epilogue); otherwise the sum is
+//     TMA-stored to the workspace as cluster partial g and the tile's G
+//     cluster partials of the owner's rows are summed in ascending g, rows_per
+//     rows per CTA, after every CTA holding those rows has arrived -- the
+//     same arrival, load and sum as the plain in-kernel split-K sum.
+// Shared memory: [0, CL x slot) the receive slots (later the target of the
+// load of the cluster partials), then (CL - 1) x slot of outgoing staging;
+// the planner checks that both fit the ring and the epilogue buffers.
+template <int BN, bool EPI>
+__device__ __forceinline__ void cluster_sum_epilogue(
+    const KernelParams &p, const CUtensorMap &map_ws, const CUtensorMap &map_red, uint32_t base,
+    uint8_t *base_ptr, uint32_t tmem_base, uint32_t tfull0, uint32_t stall_bar, uint32_t red_bar,
+    uint32_t peers_free, uint32_t recv_full, volatile uint32_t *red_ok, volatile uint32_t *clu_bad,
+    volatile uint32_t *abort_flag, const AbortFlags &af, int64_t num_units, int warp, int lane)
+{
+    using Cfg = TileCfg<BN, false>;
+    constexpr uint32_t BOX = Cfg::EPI_BUF_BYTES;  // one 32 x 32 f32 box
+    const int q = warp & 3;                       // TMEM lanes 32q ... 32q + 31 = tile rows
+    const int et = int(threadIdx.x) - 64;         // 0..127
+    if (blockIdx.x == 0 && threadIdx.x == 64)
+        publish_counters(p.counters, p.counter_words, p.epoch_tag, p.epoch);
+    const int CL = p.red_cluster;
+    const int G = p.red_groups;
+    const uint32_t crank = ptx::cluster_ctarank();
+    const int per = 4 / CL;                       // epilogue warps whose rows one CTA owns
+    const int rows_own = Cfg::ROWS / CL;
+    const int32_t own0 = int32_t(crank) * rows_own;
+    const uint32_t slot_bytes = uint32_t(rows_own) * BN * 4u;
+    const bool has_unit = int64_t(blockIdx.x) < num_units;
+    const Unit w = has_unit ? decode_unit(blockIdx.x, p, nullptr, Cfg::TILE_M, BN) : Unit{};
+    const int g = w.s / CL;
+
+    bool ok = has_unit && uint32_t(w.s % CL) == crank;
+    ok = ok && wait_bounded(tfull0, 0, af, kStatusEpilogue, true);
+    if (p.inject_stall && ok)
+        ok = wait_bounded(stall_bar, 0, af, kStatusEpilogue, true);
+    ok = __all_sync(0xffffffffu, ok);
+    ptx::tc_fence_after_sync();
+    if (warp == 2 && lane == 0)
+        trace_stamp(p, kTraceAccReady);
+    // 1.  (The wait on the setup arrive makes sure the peers' barriers exist.)
+    ptx::cluster_wait();
+    if (ok && warp == 2 && lane == 0) {
+        for (int r = 0; r < CL; ++r)
+            if (r != int(crank))
+                ptx::mbar_arrive_cluster(ptx::mapa_shared(peers_free, uint32_t(r)));
+    }
+    // 2.
+    const int owner = q / per;
+    const bool local = owner == int(crank);
+    const uint32_t slot = base + crank * slot_bytes + uint32_t(q - owner * per) * uint32_t(BN / 32) * BOX;
+    const int sidx = q < int(crank) * per ? q : q - per;  // index among this CTA's sending warps
+    const uint32_t stage = base + uint32_t(CL) * slot_bytes + uint32_t(sidx) * uint32_t(BN / 32) * BOX;
+    if (ok && !local)
+        ok = wait_bounded(peers_free, 0, af, kStatusReduce, true);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+        const uint32_t bar = ptx::mapa_shared(recv_full, uint32_t(owner));
+        const uint32_t tm_row = tmem_base + (uint32_t(32 * q) << 16);
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+            uint32_t r[32];
+            ptx::tmem_ld_32x32b_x32(tm_row + 32u * uint32_t(c), r);
+            ptx::tmem_wait_ld();
+            const uint32_t buf = (local ? slot : stage) + uint32_t(c) * BOX;
+            const uint32_t row_addr = buf + uint32_t(lane) * 128u;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                ptx::st_shared_v4(row_addr + (uint32_t(j ^ (lane & 7)) << 4), r[4 * j], r[4 * j + 1],
+                                  r[4 * j + 2], r[4 * j + 3]);
+            if (!local) {
+                ptx::fence_proxy_async_smem();  // the box before the bulk copy reads it
+                __syncwarp();
+                if (lane == 0)
+                    ptx::bulk_copy_to_cluster(ptx::mapa_shared(slot + uint32_t(c) * BOX, uint32_t(owner)),
+                                              buf, BOX, bar);
+            }
+        }
+    }
+    // The owned rows: the peers' (counted on recv_full, acquired at cluster
+    // scope) and this CTA's own warps' (the named barrier).
+    if (ok)
+        ok = wait_bounded<true>(recv_full, 0, af, kStatusReduce, true);
+    if (!ok)
+        *clu_bad = 1u;
+    ptx::named_bar_sync(1, 128);
+    const bool go = *clu_bad == 0u;
+
+    // Four sums of one row of the tile (tile row tr, columns tc ... tc + 3)
+    // through the epilogue into C, clipped at M and N.
+    auto put4 = [&](auto act, int32_t tr, int32_t tc, const float4 &acc) {
+        const int32_t gr = w.m0 + tr;
+        const int32_t gc = w.n0 + tc;
+        if (gr >= p.M || gc >= p.N)
+            return;
+        const int64_t bz = w.z_in;
+        const int64_t at = bz * p.stride_c + int64_t(gr) * p.ldc + gc;
+        if constexpr (EPI) {
+            const float *bias = p.epi.bias ? p.epi.bias + bz * p.epi.bias_stride : nullptr;
+            float4 v = acc;
+            epi_apply4_as<decltype(act)::value>(v, gc, p.N, bias, p.epi);
+            if (gc + 3 < p.N && p.epi.out_type == kOutF32) {
+                *reinterpret_cast<float4 *>(static_cast<float *>(p.c_direct) + at) = v;
+            } else if (gc + 3 < p.N) {
+                *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(p.c_direct) + at) =
+                    make_uint2(epi_out16(v.x, p.epi.out_type) | (epi_out16(v.y, p.epi.out_type) << 16),
+                               epi_out16(v.z, p.epi.out_type) | (epi_out16(v.w, p.epi.out_type) << 16));
+            } else {
+                const float vv[3] = {v.x, v.y, v.z};
+#pragma unroll
+                for (int k = 0; k < 3; ++k)
+                    if (gc + k < p.N)
+                        epi_store(p.c_direct, at + k, vv[k], p.epi.out_type);
+            }
+        } else {
+            float *dst = static_cast<float *>(p.c_direct) + at;
+            if (gc + 3 < p.N) {
+                *reinterpret_cast<float4 *>(dst) = acc;
+            } else {
+                dst[0] = acc.x;
+                if (gc + 1 < p.N)
+                    dst[1] = acc.y;
+                if (gc + 2 < p.N)
+                    dst[2] = acc.z;
+            }
+        }
+    };
+    auto with_act = [&](auto &&fn) {
+        if constexpr (EPI) {
+            switch (p.epi.act) {
+            case kActRelu: fn(ActTag<kActRelu>{}); break;
+            case kActLeakyRelu: fn(ActTag<kActLeakyRelu>{}); break;
+            case kActGelu: fn(ActTag<kActGelu>{}); break;
+            case kActGeluTanh: fn(ActTag<kActGeluTanh>{}); break;
+            case kActSilu: fn(ActTag<kActSilu>{}); break;
+            default: fn(ActTag<kActNone>{}); break;
+            }
+        } else {
+            fn(ActTag<kActNone>{});
+        }
+    };
+
+    // 3.  Chunk f (16 bytes) of a slot: box f / 256 (row block, then column
+    // box), row (f / 8) % 32, column chunk (f % 8) ^ row % 8.
+    const int nf = rows_own * BN / 4;
+    float4 *const slots = reinterpret_cast<float4 *>(base_ptr);
+    if (go) {
+        with_act([&](auto act) {
+            for (int f = et; f < nf; f += 128) {
+                float4 a = slots[f];
+                for (int r = 1; r < CL; ++r) {
+                    const float4 v = slots[r * nf + f];
+                    a.x += v.x;
+                    a.y += v.y;
+                    a.z += v.z;
+                    a.w += v.w;
+                }
+                if (G == 1) {
+                    const int bx = f >> 8, i = (f >> 3) & 31, j = (f & 7) ^ (i & 7);
+                    put4(act, own0 + 32 * (bx / (BN / 32)) + i, 32 * (bx % (BN / 32)) + 4 * j, a);
+                } else {
+                    slots[f] = a;
+                }
+            }
+        });
+    }
+    if (G == 1) {
+        ptx::named_bar_sync(1, 128);
+        if (et == 0)
+            trace_stamp(p, kTraceReduced);
+        return;
+    }
+    // The cluster partial of the owned rows to the workspace.
+    ptx::fence_proxy_async_smem();  // the sums above before the TMA store reads them
+    ptx::named_bar_sync(1, 128);
+    uint64_t epoch_now = 0;
+    if (et == 0) {
+        epoch_now = ptx::ld_relaxed_gpu(p.epoch_tag);
+        if (go) {
+            for (int rb = 0; rb < rows_own / 32; ++rb)
+                for (int cb = 0; cb < BN / 32; ++cb)
+                    ptx::tma_store_3d(&map_ws, base + uint32_t(rb * (BN / 32) + cb) * BOX, 32 * cb,
+                                      own0 + 32 * rb, int32_t(w.red_tile * G + g));
+            ptx::bulk_commit_group();
+            ptx::bulk_wait_group_all();
+            ptx::fence_proxy_async_global();
+        }
+        trace_stamp(p, kTraceStored);
+    }
+    // Arrive on the (tile, rank) counter once the partial is in the
+    // workspace, wait (bounded) for the tile's G clusters, fetch rows
+    // [r0, r0 + rows_per) of the G partials with one TMA load into the slots
+    // (summed and stored above: free again), add them in ascending g.
+    const int32_t r0 = own0 + g * p.rows_per;
+    const bool active = g * p.rows_per < rows_own && w.m0 + r0 < p.M;
+    if (et == 0) {
+        uint32_t okv = 0;
+        if (go) {
+            const bool epoch_ok = epoch_now == p.epoch ||
+                poll_bounded<unsigned long long>(p.epoch_tag, p.epoch, af, kStatusReduce);
+            if (!*abort_flag && epoch_ok) {
+                uint32_t *count = p.counters + w.red_tile * CL + crank;
+                __threadfence();
+                atomicAdd(count, 1u);  // arrive
+                okv = poll_bounded<uint32_t>(count, uint32_t(G), af, kStatusReduce);
+                if (okv && active) {
+                    ptx::fence_proxy_async_global();
+                    ptx::mbar_arrive_expect_tx(red_bar, uint32_t(p.rows_per) * BN * 4u * uint32_t(G));
+                    ptx::tma_load_3d(base, &map_red, red_bar, 0, r0, int32_t(w.red_tile * G));
+                }
+            }
+        }
+        *red_ok = okv;
+    }
+    ptx::named_bar_sync(1, 128);
+    if (*red_ok && active && wait_bounded(red_bar, 0, af, kStatusReduce, false)) {
+        const int32_t per_split = p.rows_per * (BN / 4);  // float4s of one cluster partial
+        const int32_t row_end = own0 + rows_own;
+        with_act([&](auto act) {
+            for (int32_t f = et; f < per_split; f += 128) {
+                float4 a = slots[f];
+#pragma unroll 4
+                for (int32_t s2 = 1; s2 < G; ++s2) {
+                    const float4 v = slots[s2 * per_split + f];
+                    a.x += v.x;
+                    a.y += v.y;
+                    a.z += v.z;
+                    a.w += v.w;
+                }
+                const int32_t row = f / (BN / 4);
+                if (r0 + row < row_end)
+                    put4(act, r0 + row, (f - row * (BN / 4)) * 4, a);
+            }
+        });
+    }
+    ptx::named_bar_sync(1, 128);
+    if (et == 0)
+        trace_stamp(p, kTraceReduced);
+}
+
 // ------------------------------------------------------------- the GEMM
 
-template <int BN, bool PAIR, bool EPI>
+template <int BN, bool PAIR, bool EPI, bool CLU>
 __global__ void __launch_bounds__(kThreads, 1)
     tsm_gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a,
                             const __grid_constant__ CUtensorMap map_b,
@@ -489,6 +750,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 {
     using Cfg = TileCfg<BN, PAIR>;
     constexpr int S = Cfg::STAGES;
+    static_assert(!(CLU && PAIR), "the cluster split-K sum is built for one CTA per tile");
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -513,6 +775,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile uint32_t *const abort_flag = tmem_slot + 1;
     volatile uint32_t *const red_ok = tmem_slot + 2;  // in-kernel split-K: go / no-go
     const uint32_t red_bar = ctrl + 16u * S + 64u;    // in-kernel split-K: partial chunks landed
+    volatile uint32_t *const clu_bad = tmem_slot + 3; // cluster sum: some epilogue warp gave up
+    const uint32_t peers_free = ctrl + 16u * S + 72u; // cluster sum: every peer's ring is idle
+    const uint32_t recv_full = ctrl + 16u * S + 80u;  // cluster sum: the peers' rows have landed
 
     const int warp = int(threadIdx.x >> 5);
     const int lane = int(threadIdx.x & 31);
@@ -535,7 +800,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(stall_bar, 1);
         ptx::mbar_init(red_bar, 1);
         *abort_flag = 0u;
+        if constexpr (CLU) {
+            ptx::mbar_init(peers_free, uint32_t(p.red_cluster - 1));
+            ptx::mbar_init(recv_full, 1);
+            *clu_bad = 0u;
+        }
         ptx::fence_mbar_init();
+        if constexpr (CLU) {
+            // The phase completes once the other CTAs' rows (one slot each)
+            // have landed.
+            ptx::mbar_arrive_expect_tx(recv_full, uint32_t(p.red_cluster - 1) *
+                                                      uint32_t(Cfg::ROWS / p.red_cluster) * BN * 4u);
+        }
         ptx::prefetch_tensormap(&map_a);
         ptx::prefetch_tensormap(&map_b);
         ptx::prefetch_tensormap(&map_out);
@@ -545,6 +821,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     __syncwarp();
+    if constexpr (CLU)
+        ptx::cluster_arrive_relaxed();  // barriers published; waited on before the first remote access
     if constexpr (PAIR)
         ptx::cluster_sync();  // the peer's barriers exist before anything signals them
     if (warp == 1) {
@@ -651,6 +929,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();  // lanes 1..31 wait for lane 0 before the CTA barrier
+        if constexpr (CLU)
+            ptx::cluster_wait();  // the setup arrive's phase, before the exit's
     } else if (warp == 1) {
         if (lane == 0 && leader) {
             // ---------------- MMA issuer (one thread; the leader of a pair)
@@ -708,6 +988,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             wait_bounded(done_bar, 0, af, kStatusDrain, false);
         }
         __syncwarp();  // lanes 1..31 wait for lane 0 before the CTA barrier
+        if constexpr (CLU)
+            ptx::cluster_wait();  // the setup arrive's phase, before the exit's
+    } else if constexpr (CLU) {
+        // ---------------- epilogue of a cluster split-K sum: warps 2..5
+        cluster_sum_epilogue<BN, EPI>(p, map_ws, map_red, base, base_ptr, tmem_base, tfull0, stall_bar,
+                                      red_bar, peers_free, recv_full, red_ok, clu_bad, abort_flag, af,
+                                      num_units, warp, lane);
     } else {
         // ---------------- epilogue: warps 2..5, TMEM lane quarter = warp % 4
         const int e = warp - 2;
@@ -1062,9 +1349,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     ptx::tc_fence_before_sync();
     ptx::cta_sync();
-    if constexpr (PAIR)
-        ptx::cluster_sync();  // neither CTA leaves while the other may still signal it
-    if (threadIdx.x == 0)
+    if constexpr (PAIR || CLU)
+        ptx::cluster_sync();  // no CTA leaves while another of its cluster may still signal it
+    if (threadIdx.x == 64)    // an epilogue thread: the last role to finish
         trace_stamp(p, kTraceExit);
     if (warp == 1) {
         __syncwarp();
@@ -1233,17 +1520,26 @@ SmemBudget smem_budget(int tile_m, int tile_n)
     }
 }
 
-template <int BN, bool PAIR, bool EPI>
+template <int BN, bool PAIR, bool EPI, bool CLU = false>
 static cudaError_t set_attr()
 {
-    return cudaFuncSetAttribute(tsm_gemm_tcgen05_kernel<BN, PAIR, EPI>,
+    return cudaFuncSetAttribute(tsm_gemm_tcgen05_kernel<BN, PAIR, EPI, CLU>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 TileCfg<BN, PAIR>::SMEM_BYTES);
 }
 
 template <bool EPI>
-static cudaError_t set_attrs_of(int tile_m, int tile_n)
+static cudaError_t set_attrs_of(int tile_m, int tile_n, int red_cluster)
 {
+    if (red_cluster > 1) {
+        if (tile_m != kTileM)
+            return cudaErrorInvalidValue;
+        switch (tile_n) {
+        case 128: return set_attr<128, false, EPI, true>();
+        case 256: return set_attr<256, false, EPI, true>();
+        default: return cudaErrorInvalidValue;
+        }
+    }
     if (tile_m == 2 * kTileM) {
         switch (tile_n) {
         case 128: return set_attr<128, true, EPI>();
@@ -1259,12 +1555,13 @@ static cudaError_t set_attrs_of(int tile_m, int tile_n)
     }
 }
 
-cudaError_t set_kernel_attributes(int tile_m, int tile_n, bool epi)
+cudaError_t set_kernel_attributes(int tile_m, int tile_n, bool epi, int red_cluster)
 {
-    return epi ? set_attrs_of<true>(tile_m, tile_n) : set_attrs_of<false>(tile_m, tile_n);
+    return epi ? set_attrs_of<true>(tile_m, tile_n, red_cluster)
+               : set_attrs_of<false>(tile_m, tile_n, red_cluster);
 }
 
-template <int BN, bool PAIR, bool EPI>
+template <int BN, bool PAIR, bool EPI, bool CLU>
 static cudaError_t launch_bn(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o,
                              const CUtensorMap &ws, const CUtensorMap &r, const KernelParams &p,
                              int grid, cudaStream_t stream)
@@ -1275,9 +1572,9 @@ static cudaError_t launch_bn(const CUtensorMap &a, const CUtensorMap &b, const C
     cfg.dynamicSmemBytes = TileCfg<BN, PAIR>::SMEM_BYTES;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
-    if (PAIR) {
+    if (PAIR || CLU) {
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.x = PAIR ? 2u : unsigned(p.red_cluster);
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
@@ -1286,39 +1583,77 @@ static cudaError_t launch_bn(const CUtensorMap &a, const CUtensorMap &b, const C
         cfg.attrs = nullptr;
         cfg.numAttrs = 0;
     }
-    return cudaLaunchKernelEx(&cfg, tsm_gemm_tcgen05_kernel<BN, PAIR, EPI>, a, b, o, ws, r, p);
+    return cudaLaunchKernelEx(&cfg, tsm_gemm_tcgen05_kernel<BN, PAIR, EPI, CLU>, a, b, o, ws, r, p);
 }
 
 template <bool EPI>
-static cudaError_t launch_of(int tile_m, int tile_n, const CUtensorMap &map_a,
+static cudaError_t launch_of(int tile_m, int tile_n, int red_cluster, const CUtensorMap &map_a,
                              const CUtensorMap &map_b, const CUtensorMap &map_out,
                              const CUtensorMap &map_ws, const CUtensorMap &map_red,
                              const KernelParams &p, int grid, cudaStream_t stream)
 {
+    if (red_cluster > 1) {
+        if (tile_m != kTileM || grid % red_cluster || p.red_cluster != red_cluster)
+            return cudaErrorInvalidValue;
+        switch (tile_n) {
+        case 128: return launch_bn<128, false, EPI, true>(map_a, map_b, map_out, map_ws, map_red, p, grid, stream);
+        case 256: return launch_bn<256, false, EPI, true>(map_a, map_b, map_out, map_ws, map_red, p, grid, stream);
+        default: return cudaErrorInvalidValue;
+        }
+    }
     if (tile_m == 2 * kTileM) {
         if (grid % 2)
             return cudaErrorInvalidValue;
         switch (tile_n) {
-        case 128: return launch_bn<128, true, EPI>(map_a, map_b, map_out, map_ws, map_red, p, grid, stream);
-        case 256: return launch_bn<256, true, EPI>(map_a, map_b, map_out, map_ws, map_red, p, grid, stream);
+        case 128: return launch_bn<128, true, EPI, false>(map_a, map_b, map_out, map_ws, map_red, p, grid, stream);
+        case 256: return launch_bn<256, true, EPI, false>(map_a, map_b, map_out, map_ws, map_red, p, grid, stream);
         default: return cudaErrorInvalidValue;
         }
     }
     switch (tile_n) {
-    case 64: return launch_bn<64, false, EPI>(map_a, map_b, map_out, map_ws, map_red, p, grid, stream);
-    case 128: return launch_bn<128, false, EPI>(map_a, map_b, map_out, map_ws, map_red, p, grid, stream);
-    case 256: return launch_bn<256, false, EPI>(map_a, map_b, map_out, map_ws, map_red, p, grid, stream);
+    case 64: return launch_bn<64, false, EPI, false>(map_a, map_b, map_out, map_ws, map_red, p, grid, stream);
+    case 128: return launch_bn<128, false, EPI, false>(map_a, map_b, map_out, map_ws, map_red, p, grid, stream);
+    case 256: return launch_bn<256, false, EPI, false>(map_a, map_b, map_out, map_ws, map_red, p, grid, stream);
     default: return cudaErrorInvalidValue;
     }
 }
 
-cudaError_t launch_tcgen05_gemm(int tile_m, int tile_n, bool epi, const CUtensorMap &map_a,
-                                const CUtensorMap &map_b, const CUtensorMap &map_out,
-                                const CUtensorMap &map_ws, const CUtensorMap &map_red,
-                                const KernelParams &p, int grid, cudaStream_t stream)
+cudaError_t launch_tcgen05_gemm(int tile_m, int tile_n, bool epi, int red_cluster,
+                                const CUtensorMap &map_a, const CUtensorMap &map_b,
+                                const CUtensorMap &map_out, const CUtensorMap &map_ws,
+                                const CUtensorMap &map_red, const KernelParams &p, int grid,
+                                cudaStream_t stream)
 {
-    return epi ? launch_of<true>(tile_m, tile_n, map_a, map_b, map_out, map_ws, map_red, p, grid, stream)
-               : launch_of<false>(tile_m, tile_n, map_a, map_b, map_out, map_ws, map_red, p, grid, stream);
+    return epi ? launch_of<true>(tile_m, tile_n, red_cluster, map_a, map_b, map_out, map_ws, map_red, p, grid, stream)
+               : launch_of<false>(tile_m, tile_n, red_cluster, map_a, map_b, map_out, map_ws, map_red, p, grid, stream);
+}
+
+template <int BN>
+static cudaError_t capacity_of(int red_cluster, int *clusters)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(red_cluster), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = TileCfg<BN, false>::SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = unsigned(red_cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaOccupancyMaxActiveClusters(clusters, tsm_gemm_tcgen05_kernel<BN, false, false, true>, &cfg);
+}
+
+cudaError_t cluster_capacity(int tile_n, int red_cluster, int *clusters)
+{
+    *clusters = 0;
+    cudaError_t e = set_attr<128, false, false, true>();
+    if (e == cudaSuccess)
+        e = set_attr<256, false, false, true>();
+    if (e != cudaSuccess)
+        return e;
+    return tile_n == 256 ? capacity_of<256>(red_cluster, clusters) : capacity_of<128>(red_cluster, clusters);
 }
 
 cudaError_t launch_splitk_reduce(const float *W, void *C, int32_t M, int32_t N, int32_t S,

@@ -229,6 +229,46 @@ __device__ __forceinline__ void cluster_sync()
                  "barrier.cluster.wait.acquire;" ::: "memory");
 }
 
+// The two halves of cluster_sync apart: arrive early (relaxed, after the
+// mbarrier-init fence has published the barriers), wait later, so that the
+// cluster-wide handshake costs nothing on the critical path.
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait()
+{
+    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to
+// another CTA's in the cluster; `dst` and `bar` are shared::cluster addresses
+// in that CTA, whose mbarrier counts the bytes when they have landed.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, uint32_t src, uint32_t bytes,
+                                                     uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(dst), "r"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// try_wait with cluster-scope acquire: the phase's completion also makes the
+// writes other CTAs of the cluster counted on it visible to this thread.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
 // The shared::cluster address of the same shared-memory location in CTA `rank`.
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank)
 {
