@@ -1,17 +1,17 @@
 """The GEMM entry point that allocates nothing, checked against the ordinary one.
 
-Some callers cannot allocate device memory while they run: code being
-captured into a CUDA graph that must not gain allocation nodes, allocators
-or memory managers that call this library and may not re-enter themselves,
-and hosts that reserved all of the GPU's memory up front.  For them
+Some callers cannot allocate device memory while they run: allocators or
+memory managers that call this library and may not re-enter themselves, and
+hosts that reserved all of the GPU's memory up front.  For them
 ``gemm_f16_f32acc_splitk_noalloc`` keeps its split-K partial sums in a fixed
 16 MiB array compiled into the library instead of taking workspace from a
 memory pool.  These tests call it through the C ABI twice in a row, with
 different inputs so that the second call cannot pass on the first call's
 leftover partials, and compare each result with ``gemm_f16_f32acc`` within
-the tolerance the other tests use.  They also check that a plan needing
-more than the array holds is refused, and that a call leaves the device's
-free memory unchanged.
+the tolerance the other tests use, and -- on small-integer inputs, whose
+sums are exact in f32 -- with the oracle bit for bit.  They also check that
+a plan needing more than the array holds is refused, and that a call leaves
+the device's free memory unchanged.
 """
 import math
 
@@ -39,9 +39,10 @@ def _pad(n, m):
     return -(-n // m) * m
 
 
-def _both(b, M, N, K, seed, split_k):
-    """The no-allocation result and the ordinary one, for one seeded input."""
-    A, B = synthetic.operands(M, N, K, "uniform", seed=seed)
+def _both(b, M, N, K, seed, split_k, dist="uniform", with_operands=False):
+    """The no-allocation result and the ordinary one, for one seeded input
+    (and the CPU operands, with ``with_operands``)."""
+    A, B = synthetic.operands(M, N, K, dist, seed=seed)
     lda, ldb, ldc = _pad(K, 8), _pad(N, 8), _pad(N, 4)
     dA = torch.zeros((M, lda), dtype=torch.float16, device="cuda")
     dB = torch.zeros((K, ldb), dtype=torch.float16, device="cuda")
@@ -56,7 +57,8 @@ def _both(b, M, N, K, seed, split_k):
     b.check(b.gemm_f16_f32acc_opts(dA.data_ptr(), dB.data_ptr(), c_regular.data_ptr(), M, N, K,
                                    lda, ldb, ldc, 0, 0, 0, 1, opts, s))
     b.check(b.gemm_get_device_status(s))
-    return c_noalloc[:, :N].cpu().double().numpy(), c_regular[:, :N].cpu().double().numpy()
+    out = c_noalloc[:, :N].cpu().double().numpy(), c_regular[:, :N].cpu().double().numpy()
+    return out + (A, B) if with_operands else out
 
 
 def _within_tolerance(got, ref, K):
@@ -79,6 +81,17 @@ def test_two_calls_in_a_row_match_the_ordinary_entry_point(b, M, N, K, split_k):
     for seed in (101, 202):
         got, ref = _both(b, M, N, K, seed, split_k)
         _within_tolerance(got, ref, K)
+
+
+@pytest.mark.parametrize("M,N,K,split_k", [(256, 256, 65536, 0), (300, 250, 5000, 4)])
+def test_small_integer_splits_exact_against_the_oracle(b, M, N, K, split_k):
+    """Split plans on small-integer inputs: both entry points bit for bit
+    equal to the oracle, on two calls in a row with different inputs."""
+    for seed in (303, 404):
+        got, regular, A, B = _both(b, M, N, K, seed, split_k, dist="int4", with_operands=True)
+        ref = oracle.gemm_f64(A, B, M, N, K)
+        assert np.array_equal(got, ref)
+        assert np.array_equal(regular, ref)
 
 
 def test_plan_larger_than_the_scratch_is_refused(b):
