@@ -61,6 +61,8 @@ def parse_args(argv=None):
     p.add_argument("--split-k", type=int, default=0, help="K ranges; 0: planner")
     p.add_argument("--splitk-reduce", type=int, default=0,
                    help="0/2: in-kernel split-K sum when possible, 1: separate reduce kernel")
+    p.add_argument("--red-cluster", type=int, default=0,
+                   help="in-kernel split-K sum taken in clusters of 2 or 4 CTAs; 1: off; 0: planner")
     p.add_argument("--ld-pad", type=int, default=0,
                    help="lay A, B and C out with lda = K + p, ldb = ldc = N + p elements; an odd p "
                         "makes every operand unaddressable by the TMA (the repacking path)")
@@ -73,6 +75,10 @@ def parse_args(argv=None):
                    help="add a per-CTA phase timeline (one extra traced step) to the JSON line")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-workloads", action="store_true",
+                   help="skip timing the other four GEMM shapes beside the default line")
+    p.add_argument("--workload-rounds", type=int, default=100,
+                   help="interleaved rounds (one step of each shape) timed for the workloads table")
     p.add_argument("--e2e-steps", type=int, default=30,
                    help="end-to-end steps timed (the three-deep pipeline fills and drains once)")
     return p.parse_args(argv)
@@ -231,6 +237,11 @@ def timed_loop(args, call, flush, stream, world, local_rank):
     sampled throughout.  Returns (ms per step, wall start, wall end, sampler)."""
     import torch
     from tiled_staged_matmul_gb300 import binding
+    # The sampler runs from the first warm-up step on: the timed steps follow
+    # the warm-up with no idle gap, in the clock and power state the workload
+    # has settled in, whatever the number of steps.
+    sampler = ClockSampler(local_rank)
+    sampler.start()
     for _ in range(max(args.warmup, 3)):
         if flush:
             flush()
@@ -264,9 +275,6 @@ def timed_loop(args, call, flush, stream, world, local_rank):
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    sampler = ClockSampler(local_rank)
-    sampler.start()
-    time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.time()
@@ -283,6 +291,13 @@ def timed_loop(args, call, flush, stream, world, local_rank):
     sampler.stop()
     binding.check(binding.gemm_get_device_status(stream.cuda_stream))
     return [s.elapsed_time(e) for s, e in zip(starts, ends)], t0, t1, sampler, burst_ms
+
+
+def step_stats(per_step_ms):
+    """Mean, median and minimum of the per-step event times (ms)."""
+    return {"mean": round(statistics.fmean(per_step_ms), 5),
+            "median": round(statistics.median(per_step_ms), 5),
+            "min": round(min(per_step_ms), 5)}
 
 
 def burst_of(flops, algorithmic_bytes, ms):
@@ -481,6 +496,7 @@ def run_ours(args, rank, local_rank, world):
                            args.out) if fused else None
     stream = torch.cuda.current_stream()
     opts = binding.GemmOptions(args.split_k, args.tile_n, 0, 0, args.tile_m, args.splitk_reduce)
+    opts.red_cluster = args.red_cluster
     plan = binding.gemm_plan(w.M, w.N, w.K, 1, opts)
     launches_per_call = 2 if plan["split_k"] > 1 and not plan["fused_reduce"] else 1
     # Row pitches that are not multiples of 16 bytes: that operand is copied
@@ -545,6 +561,7 @@ def run_ours(args, rank, local_rank, world):
                                   f"{plan['tail_split']} ways "
                                   + ("in column slices" if plan["tail_narrow"] else "along K")
                                   if plan["tail_split"] else "none"),
+                   "red_cluster": plan["red_cluster"],
                    "splitk_sum": ("in-kernel" if plan["fused_reduce"] else "separate kernel")
                    if plan["split_k"] > 1 or (plan["tail_split"] and not plan["tail_narrow"])
                    else "none",
@@ -561,15 +578,190 @@ def run_ours(args, rank, local_rank, world):
         "roofline": roofline,
         "burst": burst_of(w.flops, abytes, burst_ms),
     }
+    result["ms_per_step_stats"] = step_stats(per_step_ms)
     result["clocks"] = {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")}
     if args.trace:
         result["trace"] = traced_step(args, binding, call, plan, flush_l2 if flush else None, dev)
+    plain_default = (args.workload == DEFAULT_WORKLOAD and not args.shape and not fused
+                     and not pad and not (args.tile_m or args.tile_n or args.split_k
+                                          or args.splitk_reduce or args.red_cluster))
+    if plain_default and not args.no_workloads:
+        # The other four shapes, interleaved, in the same run.
+        table, _ = time_workloads(args, SIDE_WORKLOADS, dev, world, local_rank,
+                                  max(args.workload_rounds, 10),
+                                  headline=(w.name, per_step_ms, result["clocks"]))
+        result["workloads"] = table
+        result["binding_us_per_call"] = ctypes_us_per_call()
+        result["gpu_launches"] += len(SIDE_WORKLOADS) * max(args.workload_rounds, 10)
 
     if not args.no_e2e and not fused:
         result["e2e"] = run_e2e(args, w, A_h, B_h, dev, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(w, A_h, B_h, target_s=15.0)
+        result["cpu_baseline"] = cpu_baseline(w, A_h, B_h, target_s=15.0,
+                                              C_gpu=C if plain_default else None)
     return result
+
+
+# The other four GEMM shapes timed beside the headline in the same run
+# (the small-integer twin of 64 x 128 x 128 is a parity case only).
+SIDE_WORKLOADS = ("gemm_64x128x128_uniform", "gemm_1000x1000x1000_normal",
+                  "gemm_4096x4096x4096_normal_invsqrtk", "gemm_256x256x65536_uniform")
+
+
+def time_workloads(args, names, dev, world, local_rank, rounds: int, headline=None):
+    """Time several GEMM workloads in one interleaved loop: every round runs
+    one step of each (L2 flushed before each step whose inputs fit in it),
+    each step bracketed by CUDA events on the launching stream, clocks
+    sampled throughout.  Per workload: mean, median and minimum time per
+    step, the roofline of the mean, median and best step, the in-kernel span
+    of one traced step (first CTA entry to last CTA exit, %globaltimer: the
+    kernel alone, without the launch) and the clocks of the loop.
+    ``headline`` (name, per-step ms list, clocks) adds the headline
+    workload's own timed steps to the table."""
+    import torch
+    from tiled_staged_matmul_gb300 import binding, synthetic
+
+    stream = torch.cuda.current_stream()
+    scrub = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    sweep = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    sink = torch.empty(1, dtype=torch.float32, device=dev)
+
+    def flush_l2():
+        scrub.zero_()
+        torch.sum(sweep, dim=0, keepdim=True, out=sink)
+
+    runs = []
+    for name in names:
+        w = synthetic.WORKLOADS[name]
+        A_h, B_h = synthetic.workload_operands(w)
+        A, B = A_h.to(dev), B_h.to(dev)
+        C = torch.empty((w.M, w.N), dtype=torch.float32, device=dev)
+        working_set = 2 * w.M * w.K + 2 * w.K * w.N + 4 * w.M * w.N
+
+        def call(w=w, A=A, B=B, C=C, o=None):
+            if o is None:
+                binding.check(binding.gemm_f16_f32acc(A.data_ptr(), B.data_ptr(), C.data_ptr(),
+                                                      w.M, w.N, w.K, w.K, w.N, w.N,
+                                                      stream.cuda_stream))
+            else:
+                binding.check(binding.gemm_f16_f32acc_opts(A.data_ptr(), B.data_ptr(),
+                                                           C.data_ptr(), w.M, w.N, w.K, w.K, w.N,
+                                                           w.N, 0, 0, 0, 1, o, stream.cuda_stream))
+        runs.append((w, call, working_set < 2 * L2_BYTES, [], (A, B, C)))
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    for _ in range(max(args.warmup, 3)):
+        for w, call, flush, _, _ in runs:
+            if flush:
+                flush_l2()
+            call()
+    torch.cuda.synchronize()
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(rounds)] for _ in runs]
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for r in range(rounds):
+        for i, (w, call, flush, _, _) in enumerate(runs):
+            if flush:
+                flush_l2()
+            ev[i][r][0].record(stream)
+            call()
+            ev[i][r][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t1 = time.time()
+    time.sleep(ClockSampler.LAG_S + 0.1)
+    sampler.stop()
+    binding.check(binding.gemm_get_device_status(stream.cuda_stream))
+    clocks = sampler.summary(t0, t1)
+    clocks = {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")}
+
+    out = {}
+    table = [(w, [e0.elapsed_time(e1) for e0, e1 in ev[i]], call, flush)
+             for i, (w, call, flush, _, _) in enumerate(runs)]
+    head_clocks = None
+    if headline is not None:
+        table.append((synthetic.WORKLOADS[headline[0]], headline[1], None, False))
+        head_clocks = headline[2]
+    for w, ms_list, call, flush in table:
+        st = step_stats(ms_list)
+        plan = binding.gemm_plan(w.M, w.N, w.K, 1, None)
+        entry = {
+            "M": w.M, "N": w.N, "K": w.K, "dist": w.dist, "seed": w.seed,
+            "plan": {k: plan[k] for k in ("tile_m", "tile_n", "split_k", "fused_reduce",
+                                          "red_cluster", "tail_split", "tail_narrow", "grid")},
+            "steps": len(ms_list), "ms_per_step": st,
+            "value": round(w.flops / (st["mean"] * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+            "l2": ("flushed before every step (write 2xL2, then read 2xL2)" if flush else
+                   "inputs+output > L2, no flush"),
+        }
+        roof = roofline_of(w.flops, w.algorithmic_bytes, st["mean"],
+                           recorded_traffic(w.name), "tsm_gemm_tcgen05_kernel",
+                           clocks if call is not None else head_clocks)
+        roof["frac_median"] = round(roof["frac"] * st["mean"] / st["median"], 4)
+        roof["frac_best"] = round(roof["frac"] * st["mean"] / st["min"], 4)
+        entry["roofline"] = roof
+        entry["clocks"] = clocks if call is not None else head_clocks
+        if call is not None:
+            entry["host_us_per_call"] = host_us_per_call(call)
+            span = kernel_span_us(binding, call, plan, flush_l2 if flush else None, dev)
+            if span:
+                entry["kernel_span_us"] = span
+                entry["kernel_span_roofline_frac"] = round(
+                    roof["frac"] * st["mean"] * 1e3 / span, 4)
+        out[w.name] = entry
+    return out, clocks
+
+
+def host_us_per_call(call, calls: int = 200) -> float:
+    """Host time of one call through the C ABI (argument checks, planning,
+    tensor maps, the launch), the GPU idle before each: median over
+    ``calls`` calls, each timed on its own with the device synchronised
+    outside the timing.  It includes the Python binding's ctypes call."""
+    import torch
+    times = []
+    for _ in range(calls):
+        torch.cuda.synchronize()
+        t = time.perf_counter()
+        call()
+        times.append(time.perf_counter() - t)
+    torch.cuda.synchronize()
+    return round(statistics.median(times) * 1e6, 2)
+
+
+def ctypes_us_per_call(calls: int = 2000) -> float:
+    """The binding's own cost: median host time of a C ABI call that does
+    nothing (gemm_version) through the same ctypes path."""
+    from tiled_staged_matmul_gb300 import binding
+    times = []
+    for _ in range(calls):
+        t = time.perf_counter()
+        binding.gemm_version()
+        times.append(time.perf_counter() - t)
+    return round(statistics.median(times) * 1e6, 3)
+
+
+def kernel_span_us(binding, call, plan, flush, dev, repeats: int = 5):
+    """The GEMM kernel alone: first CTA entry to last CTA exit of one step,
+    read from the kernel's own %globaltimer trace (median of a few flushed
+    steps).  Launch latency and the events' own cost are outside it."""
+    import torch
+    spans = []
+    for _ in range(repeats):
+        tr = torch.zeros((plan["grid"], 8), dtype=torch.int64, device=dev)
+        o = binding.GemmOptions(0, 0, 0, 0, 0, 0, 0, 0, tr.data_ptr())
+        if flush:
+            flush()
+        call(o=o)
+        torch.cuda.synchronize()
+        t = tr.cpu()
+        entry, exit_ = t[:, 0], t[:, 7]
+        if (entry > 0).sum() == 0 or (exit_ > 0).sum() == 0:
+            return None
+        spans.append(float(exit_[exit_ > 0].max() - entry[entry > 0].min()) / 1000.0)
+    return round(statistics.median(spans), 2)
 
 
 TRACE_PHASES = ("entry", "setup", "first_data", "last_mma", "acc_ready", "stored", "reduced",
@@ -584,6 +776,7 @@ def traced_step(args, binding, call, plan, flush, dev):
     tr = torch.zeros((plan["grid"], 8), dtype=torch.int64, device=dev)
     o = binding.GemmOptions(args.split_k, args.tile_n, 0, 0, args.tile_m, args.splitk_reduce,
                             0, 0, tr.data_ptr())
+    o.red_cluster = args.red_cluster
     if flush:
         flush()
     call(o)
@@ -647,29 +840,45 @@ def run_e2e(args, w, A_h, B_h, dev, world):
 
 # ------------------------------------------------------------------ the oracle, timed
 
-def oracle_sample_rows(w, A_h, B_h, rows: int, seed: int = 0):
+def oracle_sample_rows(w, A_h, B_h, rows: int, seed: int = 0, keep: bool = False):
     """Time the oracle on `rows` consecutive rows of C (a contiguous row
-    panel of A times all of B): flops = 2 * rows * N * K."""
+    panel of A times all of B): flops = 2 * rows * N * K.  With ``keep``,
+    also return (first row, the fp64 rows)."""
     import oracle
     r0 = (seed * 7919) % max(1, w.M - rows + 1)
     A_rows = A_h[r0:r0 + rows].contiguous()
     t = time.perf_counter()
-    oracle.gemm_f64(A_rows, B_h, rows, w.N, w.K)
-    return time.perf_counter() - t
+    ref = oracle.gemm_f64(A_rows, B_h, rows, w.N, w.K)
+    dt = time.perf_counter() - t
+    return (dt, r0, ref) if keep else dt
 
 
-def cpu_baseline(w, A_h, B_h, target_s: float):
+def cpu_baseline(w, A_h, B_h, target_s: float, C_gpu=None):
+    """The oracle timed on a bounded row sample of the workload.  With
+    ``C_gpu`` (the GPU's C of that workload) the rows it computed are also
+    compared with the GPU's, at the tolerances the parity tests use."""
+    import numpy as np
     import oracle
     probe_rows = max(1, min(w.M, int(2e9 // (2 * w.N * w.K)) or 1))
     dt = oracle_sample_rows(w, A_h, B_h, probe_rows)
     rate = 2 * probe_rows * w.N * w.K / max(dt, 1e-9)
     rows = max(1, min(w.M, int(rate * target_s / (2 * w.N * w.K))))
-    dt = oracle_sample_rows(w, A_h, B_h, rows, seed=1)
+    dt, r0, ref = oracle_sample_rows(w, A_h, B_h, rows, seed=1, keep=True)
     flops = 2 * rows * w.N * w.K
-    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.threads(),
-            "kind": "oracle", "seconds": round(dt, 2),
-            "sample": f"{rows} of {w.M} rows of C ({rows} x {w.N} x {w.K}), fp64 triple loop, "
-                      f"OpenMP over rows"}
+    out = {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.threads(),
+           "kind": "oracle", "seconds": round(dt, 2),
+           "sample": f"{rows} of {w.M} rows of C ({rows} x {w.N} x {w.K}), fp64 triple loop, "
+                     f"OpenMP over rows"}
+    if C_gpu is not None:
+        got = C_gpu[r0:r0 + rows].cpu().numpy().astype(np.float64)
+        err = float(np.abs(got - ref).max())
+        rel = float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300))
+        tol = 1e-3 * math.sqrt(w.K)
+        out["parity"] = {"rows": [r0, r0 + rows], "max_abs_err": err, "rel_fro_err": rel,
+                         "tol_max_abs": tol, "tol_rel_fro": 1e-4,
+                         "finite": bool(np.isfinite(got).all()),
+                         "pass": bool(err <= tol and rel <= 1e-4 and np.isfinite(got).all())}
+    return out
 
 
 def grouped_cpu_baseline(w, A_h, B_h, counts_h, target_s: float):
