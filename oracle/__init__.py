@@ -246,25 +246,22 @@ def activation_f64(x: np.ndarray, name: str, slope: float = 0.01) -> np.ndarray:
 def round_to_bf16(x: np.ndarray) -> np.ndarray:
     """fp64 values rounded once, to nearest with ties to even, to bfloat16
     (8 significant bits, the exponent range of binary32; subnormal spacing
-    2^-133; overflow to infinity), returned as fp64."""
+    2^-133; overflow to infinity), returned as fp64.
+
+    For |v| = m 2^e (m in [0.5, 1)) the quantum is 2^q, q = max(e - 8, -133):
+    |v| / 2^q is exact in fp64 (a power-of-two scaling that stays in range),
+    so rounding it to the nearest integer, ties to even, and scaling back is
+    the exact round-to-nearest-even of v."""
     x = np.asarray(x, dtype=np.float64)
-    out = np.empty_like(x)
-    flat, res = x.reshape(-1), out.reshape(-1)
+    a = np.abs(x)
+    _, e = np.frexp(a)
+    q = np.maximum(e - 8, -133)
+    y = np.ldexp(np.rint(np.ldexp(a, -q)), q)
     max_finite = (2.0 - 2.0 ** -7) * 2.0 ** 127
-    for i, v in enumerate(flat):
-        v = float(v)
-        if v == 0.0 or math.isnan(v) or math.isinf(v):
-            res[i] = v
-            continue
-        m, e = math.frexp(abs(v))           # abs(v) = m * 2^e, m in [0.5, 1)
-        q = max(e - 8, -133)                 # the quantum: 8 significant bits, or the subnormal step
-        scaled = Fraction(abs(v)) / Fraction(2) ** q
-        r = round(scaled)                    # Python rounds exact halves to even
-        y = float(r * Fraction(2) ** q)
-        if y > max_finite:
-            y = math.inf
-        res[i] = math.copysign(y, v)
-    return out
+    y = np.where(y > max_finite, np.inf, y)
+    y = np.copysign(y, x)
+    special = (x == 0) | np.isnan(x) | np.isinf(x)
+    return np.where(special, x, y)
 
 
 def round_to_out(x: np.ndarray, out_type: str) -> np.ndarray:

@@ -94,6 +94,42 @@ def test_bf16_rounding_against_brute_force():
     assert math.isinf(oracle.round_to_bf16(np.array([3.4e38 * 1.01]))[0])
 
 
+def _bf16_exact_rational(v: float) -> float:
+    """The same rounding element by element in exact rational arithmetic:
+    |v| / 2^q rounded to the nearest integer (Python rounds exact halves to
+    even), times 2^q, with q = max(e - 8, -133) for |v| = m 2^e."""
+    from fractions import Fraction
+    if v == 0.0 or math.isnan(v) or math.isinf(v):
+        return v
+    _, e = math.frexp(abs(v))
+    q = max(e - 8, -133)
+    y = float(round(Fraction(abs(v)) / Fraction(2) ** q) * Fraction(2) ** q)
+    if y > (2.0 - 2.0 ** -7) * 2.0 ** 127:
+        y = math.inf
+    return math.copysign(y, v)
+
+
+def test_bf16_rounding_vectorised_equals_exact_rational():
+    """Ties and near-ties at every binade from the subnormal range to the
+    overflow boundary, both signs, plus random values: the vectorised
+    rounding must equal the element-by-element exact-rational one."""
+    rng = np.random.default_rng(5)
+    vals = [0.0, -0.0, math.inf, -math.inf]
+    for e in range(-140, 129, 3):
+        base = 2.0 ** e
+        for k in (1, 2, 3, 255, 256, 257, 511):
+            for d in (-1, 0, 1):
+                vals.append((k + 0.5) * 2.0 ** (e - 8) + d * 2.0 ** (e - 40) if e - 40 > -1074 else (k + 0.5) * 2.0 ** (e - 8))
+        vals.append(base * 1.5)
+    vals += list(rng.normal(size=2000) * 10.0 ** rng.integers(-40, 38, size=2000))
+    vals += [(2.0 - 2.0 ** -8) * 2.0 ** 127, (2.0 - 2.0 ** -9) * 2.0 ** 127, 3.4e38, 1.5 * 2.0 ** -133,
+             2.5 * 2.0 ** -133, 0.5 * 2.0 ** -133, 0.75 * 2.0 ** -133]
+    v = np.array(vals + [-x for x in vals], dtype=np.float64)
+    got = oracle.round_to_bf16(v)
+    want = np.array([_bf16_exact_rational(float(x)) for x in v])
+    np.testing.assert_array_equal(got, want)
+
+
 def test_f16_and_f32_rounding_tie_cases():
     r = oracle.round_to_out
     assert r(np.array([1 + 2.0 ** -11]), "f16")[0] == 1.0
