@@ -910,6 +910,11 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
             kp.reducers = int32_t(S * cpu);
             kp.rows_per = int32_t((pl.tile_m + kp.reducers - 1) / kp.reducers);
         }
+        // CTA pairs with a K-range tail: the split units go first, so that
+        // their sums overlap the later tiles (they all fit the first wave).
+        kp.split_first = (tail && pl.tile_m == 2 * kTileM) ? 1 : 0;
+        kp.n_first = split_units;
+        kp.ws = static_cast<const float *>(ws);
         kp.counters = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + split_units * tile_elems * 4);
         kp.counter_words = int32_t(counter_words);
         kp.epoch_tag = reinterpret_cast<unsigned long long *>(

@@ -96,6 +96,15 @@ struct KernelParams {
     // of tile dp_units + j / split_k, and its partial goes to the compact
     // workspace [j][tile_m][tile_n] (through the workspace map).
     int64_t dp_units;
+    // Split units first (CTA pairs, "split tail" plans whose split units all
+    // fit the first wave): units [0, n_first) are the split units j = u and
+    // the whole tiles follow (unit n_first + t is tile t).  Each split unit is
+    // the first unit of its cluster, its partners run at the same time, and
+    // its epilogue warps sum the tile from the workspace (`ws`, read through
+    // L2) while the MMA warp already works on the cluster's next tile.
+    int32_t split_first;
+    int64_t n_first;
+    const float *ws;
     // Narrow tail (not with `fused`): units [0, dp_units) are whole tiles,
     // and each later tile is cut into `narrow` column slices of
     // tile_n / narrow columns (2 or 4), each a unit of its own over all of K:

@@ -268,7 +268,8 @@ __device__ __forceinline__ void raster(int64_t t, const KernelParams &p, int32_t
 
 // Work unit -> tile and K range.
 //   fused plans: units below dp_units are whole tiles; the others are split
-//     units, tile-major (the splits of one tile sit on neighbouring clusters).
+//     units, tile-major (the splits of one tile sit on neighbouring clusters);
+//     with split_first the split units come first and the whole tiles after.
 //   narrow tails: units below dp_units are whole tiles; the others are column
 //     slices of the remaining tiles (`narrow` slices of bn / narrow columns
 //     each, full K), tile-major.
@@ -310,8 +311,10 @@ __device__ __forceinline__ Unit decode_unit(int64_t u, const KernelParams &p, co
         int32_t piece = 0;
         w.kb0 = 0;
         w.kb1 = p.k_blocks;
-        if (u >= p.dp_units) {
-            const int64_t j = u - p.dp_units;
+        if (p.split_first && u >= p.n_first) {
+            tg = u - p.n_first;
+        } else if (p.split_first || u >= p.dp_units) {
+            const int64_t j = p.split_first ? u : u - p.dp_units;
             const int32_t per = p.narrow ? p.narrow : p.split_k;
             const int64_t t = j / per;
             const int32_t s = int32_t(j - t * per);
@@ -331,7 +334,7 @@ __device__ __forceinline__ Unit decode_unit(int64_t u, const KernelParams &p, co
         raster(tg - b * tiles, p, p.tiles_m, tile_m, bn, w.m0, w.n0);
         w.n0 += piece * w.width;
         w.z_in = int32_t(b);
-        w.z_out = w.split ? int32_t(u - p.dp_units) : int32_t(b);
+        w.z_out = w.split ? int32_t(p.split_first ? u : u - p.dp_units) : int32_t(b);
         return w;
     }
     const int64_t z = u / tiles;
@@ -1003,6 +1006,111 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t abuf = 0, aphase = 0, sbuf = 0;
         if (p.fused && blockIdx.x == 0 && threadIdx.x == 64)
             publish_counters(p.counters, p.counter_words, p.epoch_tag, p.epoch);
+        // Split units first (CTA pairs): as soon as the cluster's split unit
+        // has stored its partial, its epilogue warps take their share of the
+        // tile's sum -- arrive on the tile's counter, wait (bounded) for the
+        // tile's split_k x 2 reducers, read rows_per rows of every split from
+        // the workspace through L2 and add them in ascending split order into
+        // C -- while the MMA warp already works on the cluster's next tile in
+        // the other accumulator.  All four epilogue warps pass the three named
+        // barriers on every path.
+        auto split_sum_from_l2 = [&](const Unit &w) {
+            if (lane == 0) {
+                ptx::bulk_wait_group_all();  // this warp's partial boxes are written
+                ptx::fence_proxy_async_global();
+            }
+            const int et = int(threadIdx.x) - 64;
+            uint64_t epoch_now = 0;
+            if (et == 0)
+                epoch_now = ptx::ld_relaxed_gpu(p.epoch_tag);
+            ptx::named_bar_sync(1, 128);
+            const int32_t r0 = (w.s * 2 + int32_t(rank)) * p.rows_per;
+            const bool active = r0 < Cfg::TILE_M && w.m0 + r0 < p.M;
+            if (et == 0) {
+                uint32_t okv = 0;
+                const bool epoch_ok = epoch_now == p.epoch ||
+                    poll_bounded<unsigned long long>(p.epoch_tag, p.epoch, af, kStatusReduce);
+                if (!*abort_flag && epoch_ok) {
+                    uint32_t *count = p.counters + w.red_tile;
+                    __threadfence();
+                    atomicAdd(count, 1u);  // arrive
+                    okv = poll_bounded<uint32_t>(count, uint32_t(p.reducers), af, kStatusReduce);
+                }
+                *red_ok = okv;
+            }
+            ptx::named_bar_sync(1, 128);  // the acquire above orders the reads below
+            if (*red_ok && active) {
+                constexpr int U = 4;                                  // chunks in flight per thread
+                const int32_t per_row = BN / 4;                       // float4s of a row
+                const int32_t nf = p.rows_per * per_row;
+                const int64_t part = int64_t(Cfg::TILE_M) * per_row;  // float4s of one partial
+                const float4 *src = reinterpret_cast<const float4 *>(p.ws) +
+                                    int64_t(w.red_tile) * p.split_k * part + int64_t(r0) * per_row;
+                const float *bias = EPI && p.epi.bias ? p.epi.bias + int64_t(w.z_in) * p.epi.bias_stride : nullptr;
+                auto run = [&](auto act) {
+                    for (int32_t f0 = et; f0 < nf; f0 += 128 * U) {
+                        float4 a[U];
+#pragma unroll
+                        for (int k = 0; k < U; ++k)
+                            a[k] = f0 + 128 * k < nf ? __ldcg(src + f0 + 128 * k) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        for (int32_t s2 = 1; s2 < p.split_k; ++s2) {
+                            float4 v[U];
+#pragma unroll
+                            for (int k = 0; k < U; ++k)
+                                v[k] = f0 + 128 * k < nf ? __ldcg(src + s2 * part + f0 + 128 * k) : a[k];
+#pragma unroll
+                            for (int k = 0; k < U; ++k) {
+                                a[k].x += v[k].x;
+                                a[k].y += v[k].y;
+                                a[k].z += v[k].z;
+                                a[k].w += v[k].w;
+                            }
+                        }
+#pragma unroll
+                        for (int k = 0; k < U; ++k) {
+                            const int32_t f = f0 + 128 * k;
+                            const int32_t row = f / per_row;
+                            const int32_t gr = w.m0 + r0 + row;
+                            const int32_t gc = w.n0 + (f - row * per_row) * 4;
+                            if (f >= nf || r0 + row >= Cfg::TILE_M || gr >= p.M || gc >= p.N)
+                                continue;
+                            const int64_t at = int64_t(w.z_in) * p.stride_c + int64_t(gr) * p.ldc + gc;
+                            float4 v = a[k];
+                            if constexpr (EPI)
+                                epi_apply4_as<decltype(act)::value>(v, gc, p.N, bias, p.epi);
+                            if (gc + 3 < p.N && (!EPI || p.epi.out_type == kOutF32)) {
+                                *reinterpret_cast<float4 *>(static_cast<float *>(p.c_direct) + at) = v;
+                            } else if (EPI && gc + 3 < p.N) {
+                                *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(p.c_direct) + at) =
+                                    make_uint2(epi_out16(v.x, p.epi.out_type) | (epi_out16(v.y, p.epi.out_type) << 16),
+                                               epi_out16(v.z, p.epi.out_type) | (epi_out16(v.w, p.epi.out_type) << 16));
+                            } else {
+                                const float vv[3] = {v.x, v.y, v.z};
+#pragma unroll
+                                for (int t = 0; t < 3; ++t)
+                                    if (gc + t < p.N)
+                                        epi_store(p.c_direct, at + t, vv[t], EPI ? p.epi.out_type : kOutF32);
+                            }
+                        }
+                    }
+                };
+                if constexpr (EPI) {
+                    switch (p.epi.act) {
+                    case kActRelu: run(ActTag<kActRelu>{}); break;
+                    case kActLeakyRelu: run(ActTag<kActLeakyRelu>{}); break;
+                    case kActGelu: run(ActTag<kActGelu>{}); break;
+                    case kActGeluTanh: run(ActTag<kActGeluTanh>{}); break;
+                    case kActSilu: run(ActTag<kActSilu>{}); break;
+                    default: run(ActTag<kActNone>{}); break;
+                    }
+                } else {
+                    run(ActTag<kActNone>{});
+                }
+            }
+            ptx::named_bar_sync(1, 128);
+            if (et == 0)
+                trace_stamp(p, kTraceReduced);
+        };
         for (int64_t u = cluster; u < num_units; u += nclusters) {
             const Unit w = decode_unit(u, p, gtab, Cfg::TILE_M, BN);
             bool got = wait_bounded(tfull0 + 8u * abuf, aphase, af, kStatusEpilogue, true);
@@ -1185,6 +1293,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 abuf = 0;
                 aphase ^= 1u;
             }
+            if constexpr (PAIR) {
+                if (p.split_first && w.split)
+                    split_sum_from_l2(w);
+            }
         }
         if (lane == 0)
             ptx::bulk_wait_group_all();  // stores complete before the CTA exits
@@ -1199,7 +1311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (cluster < num_units)
             last_u = cluster + (num_units - 1 - cluster) / nclusters * nclusters;
         const Unit w = last_u >= 0 ? decode_unit(last_u, p, gtab, Cfg::TILE_M, BN) : Unit{};
-        if (p.fused && last_u >= 0 && w.split) {
+        if (p.fused && !p.split_first && last_u >= 0 && w.split) {
             // ---------------- in-kernel split-K sum
             // The CTA's partial is in the workspace (its TMA stores completed
             // above); the CTA arrives on its tile's counter, waits (bounded)
