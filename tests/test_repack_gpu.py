@@ -2,11 +2,11 @@
 
 Bases that are not 16-byte aligned and row or batch pitches that are not
 multiples of 16 bytes go through a packed, aligned copy (C is computed there
-and copied out).  Each case lays its operands out at such offsets and
-pitches in NaN-filled buffers, surrounds C with a sentinel, and compares
-with the oracle: bit for bit on small-integer inputs, within the tolerance
-on random ones; everything outside C's logical blocks (and, in a grouped
-call, C's rows past each count) must keep its value."""
+and copied out).  Each case lays its operands out at such
+offsets and pitches in NaN-filled buffers, surrounds C with a sentinel, and
+compares with the oracle: bit for bit on small-integer inputs, within the
+tolerance on random ones; everything outside C's logical blocks (and, in a
+grouped call, C's rows past each count) must keep its value."""
 import numpy as np
 import pytest
 import torch
@@ -186,3 +186,85 @@ def test_benchmarked_odd_pitches_full_size(b, full_8192):
     C, dC = run_gemm(b, A, B, lda=w.K + 1, ldb=w.N + 1, ldc=w.N + 1)
     check_tolerance(C.numpy(), ref, w.K)
     assert dC.outside_untouched()
+
+
+def _opts(b, **kw):
+    o = b.GemmOptions()
+    for k, v in kw.items():
+        setattr(o, k, v)
+    return o
+
+
+# A C the TMA cannot store to (odd ldc, C one element past a 16-byte
+# boundary) under every plan that writes C: whole tiles, the separate reduce
+# kernel, the end-of-launch in-kernel split-K sum, the CTA-pair split tail
+# summed first (split units first), and the cluster sums.
+ODD_C_PLANS = {
+    "whole tiles": ((600, 330, 520), dict(split_k=1, split_tail=2), (1, 0)),
+    "separate reduce": ((256, 130, 8192), dict(split_k=4, splitk_reduce=1), (1, 0)),
+    "in-kernel sum": ((256, 130, 8192), dict(split_k=8, tile_m=128, tile_n=128), (1, 1)),
+    "pair split tail": ((2304, 2304, 1024), dict(split_tail=1, tile_m=256, tile_n=256), (1, 1)),
+    "cluster of 4": ((256, 256, 16384), dict(split_k=8, tile_m=128, tile_n=128, red_cluster=4), (4, 1)),
+    "cluster of 2": ((200, 300, 20000), dict(split_k=12, tile_m=128, tile_n=128, red_cluster=2), (2, 1)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(ODD_C_PLANS))
+def test_odd_C_through_every_store_path(b, name):
+    (M, N, K), fields, (want_cluster, want_fused) = ODD_C_PLANS[name]
+    o = _opts(b, **fields)
+    p = b.gemm_plan(M, N, K, 1, o)
+    assert p["red_cluster"] == want_cluster and p["fused_reduce"] == want_fused, p
+    if name == "pair split tail":
+        assert p["tile_m"] == 256 and p["tail_split"] >= 2 and not p["tail_narrow"], p
+    A, B = synthetic.operands(M, N, K, "int4", seed=M + N + K)
+    L = layout(M, N, K, 1, K, N, N + 1, offs=(0, 0, 1))
+    C, outside_ok = run_case(b, A[None], B[None], L, o)
+    check_exact(C, refs(A[None], B[None]))
+    assert outside_ok
+
+
+@pytest.mark.parametrize("out", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("fields", [dict(split_tail=1, tile_m=256, tile_n=256),
+                                    dict(split_k=8, tile_m=128, tile_n=128)])
+def test_odd_C_with_the_fused_epilogue(b, out, fields):
+    """16-bit and f32 outputs with an odd pitch through the split-K sums."""
+    from test_epilogue_gpu import check_epilogue
+    M, N, K = (2304, 2304, 1024) if "split_tail" in fields else (256, 130, 8192)
+    A, B = synthetic.operands(M, N, K, "uniform", seed=K + 7)
+    dA, dB = A.cuda().contiguous(), B.cuda().contiguous()
+    dt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[out]
+    ldc = N + 1
+    fill = SENTINEL if out == "f32" else 1000.0
+    buf = torch.full((1 + M * ldc + GUARD,), fill, dtype=dt, device="cuda")
+    bias = torch.linspace(-1, 1, N, dtype=torch.float32, device="cuda")
+    epi = b.epilogue(0.5, bias.data_ptr(), 0, "gelu", 0.01, out)
+    s = torch.cuda.current_stream().cuda_stream
+    b.check(b.gemm_f16_fused(dA.data_ptr(), dB.data_ptr(), buf.data_ptr() + buf.element_size(), M, N, K,
+                             K, N, ldc, 0, 0, 0, 1, epi, _opts(b, **fields), s))
+    b.check(b.gemm_get_device_status(s))
+    C = buf[1:1 + M * ldc].view(M, ldc)
+    check_epilogue(C[:, :N].float().cpu().double().numpy(), oracle.gemm_f64(A, B, M, N, K), 0.5,
+                   bias.cpu().double().numpy(), "gelu", out, K)
+    assert bool((C[:, N:] == fill).all()) and bool((buf[0] == fill).all())
+    assert bool((buf[1 + M * ldc:] == fill).all())
+
+
+def test_odd_C_grouped(b):
+    G, M, N, K = 4, 300, 256, 512
+    rows = [300, 0, 129, 17]
+    A, B = synthetic.operands(M, N, K, "int4", seed=47, batch=G)
+    ldc = N + 3
+    dC = Strided(None, M, N, ldc, M * ldc + 1, 1, torch.float32, SENTINEL, inner=G)
+    counts = torch.tensor(rows, dtype=torch.int32, device="cuda")
+    dA, dB = A.cuda().contiguous(), B.cuda().contiguous()
+    s = torch.cuda.current_stream().cuda_stream
+    b.check(b.gemm_f16_f32acc_grouped(dA.data_ptr(), dB.data_ptr(), dC.ptr(), counts.data_ptr(), G, M, N,
+                                      K, K, N, ldc, M * K, K * N, M * ldc + 1, s))
+    b.check(b.gemm_get_device_status(s))
+    C = dC.logical().double().numpy()
+    for g in range(G):
+        r = rows[g]
+        ref = oracle.gemm_f64(A[g, :r].contiguous(), B[g], r, N, K) if r else np.zeros((0, N))
+        assert np.array_equal(C[g, :r], ref)
+        assert np.all(C[g, r:] == np.float32(SENTINEL))

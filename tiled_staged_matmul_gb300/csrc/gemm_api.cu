@@ -74,7 +74,7 @@ constexpr int64_t kInt32Max = 2147483647;
 
 struct Driver {
     PFN_cuTensorMapEncodeTiled_v12000 encode_tiled = nullptr;
-    PFN_cuMemGetAddressRange_v3020 get_address_range = nullptr;
+    PFN_cuPointerGetAttributes_v7000 pointer_attributes = nullptr;
     bool loaded = false;
     std::string error;
 };
@@ -90,14 +90,17 @@ Driver &driver()
         cudaError_t e1 =
             cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f1, 12000, cudaEnableDefault, &q1);
         cudaError_t e2 =
-            cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &f2, 12000, cudaEnableDefault, &q2);
+            cudaGetDriverEntryPointByVersion("cuPointerGetAttributes", &f2, 12000, cudaEnableDefault, &q2);
         if (e1 != cudaSuccess || q1 != cudaDriverEntryPointSuccess || !f1) {
             d.error = "cuTensorMapEncodeTiled is not available from the driver";
             return;
         }
         d.encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f1);
-        if (e2 == cudaSuccess && q2 == cudaDriverEntryPointSuccess && f2)
-            d.get_address_range = reinterpret_cast<PFN_cuMemGetAddressRange_v3020>(f2);
+        if (e2 != cudaSuccess || q2 != cudaDriverEntryPointSuccess || !f2) {
+            d.error = "cuPointerGetAttributes is not available from the driver";
+            return;
+        }
+        d.pointer_attributes = reinterpret_cast<PFN_cuPointerGetAttributes_v7000>(f2);
         d.loaded = true;
     });
     return d;
@@ -295,31 +298,35 @@ TmaLayout tma_layout(const Problem &pr)
     return t;
 }
 
-// The pointer is device memory of `dev` and its allocation covers `bytes`.
+// The pointer is device memory of `dev` and its allocation covers `bytes`:
+// one driver query for the memory type, the managed flag, the device and the
+// allocation's range (a pointer the driver does not know comes back as type 0).
 gemm_status_t check_device_pointer(const void *p, int64_t bytes, int dev, const char *name)
 {
-    cudaPointerAttributes at = {};
-    cudaError_t e = cudaPointerGetAttributes(&at, p);
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return fail(GEMM_ERR_INVALID_VALUE, "%s is not a CUDA pointer (%s)", name, cudaGetErrorName(e));
-    }
-    if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged)
-        return fail(GEMM_ERR_INVALID_VALUE, "%s is not device memory", name);
-    if (at.device != dev)
-        return fail(GEMM_ERR_INVALID_VALUE, "%s lives on device %d, the current device is %d", name,
-                    at.device, dev);
     Driver &d = driver();
-    if (d.get_address_range) {
-        CUdeviceptr base = 0;
-        size_t size = 0;
-        if (d.get_address_range(&base, &size, CUdeviceptr(reinterpret_cast<uintptr_t>(p))) == CUDA_SUCCESS) {
-            const uint64_t end = uint64_t(reinterpret_cast<uintptr_t>(p)) + uint64_t(bytes);
-            if (end > uint64_t(base) + uint64_t(size))
-                return fail(GEMM_ERR_INVALID_VALUE,
-                            "%s: the allocation ends %llu bytes before the last element", name,
-                            (unsigned long long)(end - (uint64_t(base) + uint64_t(size))));
-        }
+    if (!d.loaded)
+        return fail(GEMM_ERR_CUDA, "%s", d.error.c_str());
+    unsigned int type = 0, managed = 0;
+    int ordinal = -1;
+    CUdeviceptr start = 0;
+    size_t size = 0;
+    CUpointer_attribute attrs[5] = {CU_POINTER_ATTRIBUTE_MEMORY_TYPE, CU_POINTER_ATTRIBUTE_IS_MANAGED,
+                                    CU_POINTER_ATTRIBUTE_DEVICE_ORDINAL, CU_POINTER_ATTRIBUTE_RANGE_START_ADDR,
+                                    CU_POINTER_ATTRIBUTE_RANGE_SIZE};
+    void *data[5] = {&type, &managed, &ordinal, &start, &size};
+    const CUresult r = d.pointer_attributes(5, attrs, data, CUdeviceptr(reinterpret_cast<uintptr_t>(p)));
+    if (r != CUDA_SUCCESS)
+        return fail(GEMM_ERR_INVALID_VALUE, "%s: the driver cannot query the pointer (CUresult %d)", name, int(r));
+    if (type != CU_MEMORYTYPE_DEVICE && !managed)
+        return fail(GEMM_ERR_INVALID_VALUE, type == 0 ? "%s is not a CUDA pointer" : "%s is not device memory", name);
+    if (ordinal != dev)
+        return fail(GEMM_ERR_INVALID_VALUE, "%s lives on device %d, the current device is %d", name, ordinal, dev);
+    if (size > 0) {
+        const uint64_t end = uint64_t(reinterpret_cast<uintptr_t>(p)) + uint64_t(bytes);
+        if (end > uint64_t(start) + uint64_t(size))
+            return fail(GEMM_ERR_INVALID_VALUE,
+                        "%s: the allocation ends %llu bytes before the last element", name,
+                        (unsigned long long)(end - (uint64_t(start) + uint64_t(size))));
     }
     return GEMM_OK;
 }

@@ -1116,8 +1116,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool got = wait_bounded(tfull0 + 8u * abuf, aphase, af, kStatusEpilogue, true);
             if (p.inject_stall && got)
                 got = wait_bounded(stall_bar, 0, af, kStatusEpilogue, true);
-            if (!__all_sync(0xffffffffu, got))
+            if (!__all_sync(0xffffffffu, got)) {
+                if constexpr (PAIR) {
+                    // A wait ran out and raised the abort flag, so every later
+                    // wait returns at once.  With split units first the warps
+                    // still walk the remaining units, so that all four pass
+                    // the same named barriers in each split sum (which, seeing
+                    // the flag, neither arrives nor waits).
+                    if (p.split_first) {
+                        if (w.split)
+                            split_sum_from_l2(w);
+                        continue;
+                    }
+                }
                 break;
+            }
             ptx::tc_fence_after_sync();
             if (warp == 2 && lane == 0)
                 trace_stamp(p, kTraceAccReady);
