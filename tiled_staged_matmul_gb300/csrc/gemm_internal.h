@@ -12,6 +12,12 @@ constexpr int kTileM = 128;  // rows of C per tile = TMEM lanes of one accumulat
 constexpr int kTileK = 64;   // K depth of one k-block: one 128-byte swizzle row of f16
 constexpr int kThreads = 192;  // warp 0 TMA producer, warp 1 MMA issuer, warps 2..5 epilogue
 
+// Epilogue warps of a GEMM kernel: two per TMEM lane quarter with a fused
+// epilogue (not in the cluster split-K sum), else one.
+__host__ __device__ constexpr int epilogue_warps(bool epi, bool clu) { return epi && !clu ? 8 : 4; }
+// Threads of a GEMM kernel: the producer and MMA warps, then the epilogue's.
+__host__ __device__ constexpr int gemm_threads(bool epi, bool clu) { return 64 + 32 * epilogue_warps(epi, clu); }
+
 // Fused epilogue: what the kernels do to an output value before storing it,
 // C = act(alpha * acc + bias[j]), stored as `out_type`.  The identity (alpha
 // 1, no bias, no activation, f32) is the plain GEMM.

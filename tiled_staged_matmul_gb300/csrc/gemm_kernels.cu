@@ -60,7 +60,7 @@ struct TileCfg {
     static constexpr int B_BOXES = B_COLS / 64;
     static constexpr int B_BYTES = B_BOXES * B_BOX_BYTES;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // per CTA
-    static constexpr int EPI_WARPS = 4;
+    static constexpr int EPI_WARPS = 4;                    // (eight with one buffer each: the same bytes)
     static constexpr int EPI_BUF_BYTES = 32 * 32 * 4;      // one 32 x 32 f32 box
     static constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BUF_BYTES;
     static constexpr int CTRL_BYTES = 2048;      // barriers and slots, then the group table
@@ -77,7 +77,6 @@ struct TileCfg {
     static constexpr int SMEM_BYTES = ALIGN_SLACK + STAGES * STAGE_BYTES + EPI_BYTES + CTRL_BYTES;
     // Two accumulators of BN f32 columns each per CTA (a power of two >= 32).
     static constexpr uint32_t TMEM_COLS = 2 * BN;
-    static constexpr uint32_t TEMPTY_ARRIVALS = PAIR ? 2 * EPI_WARPS : EPI_WARPS;
     static_assert(SMEM_BYTES > SMEM_LIMIT / 2, "one CTA per SM keeps TMEM allocation uncontended");
     // The CTA's last unit stages all its output boxes in the idle ring at once.
     static_assert(STAGES * STAGE_BYTES >= EPI_WARPS * (BN / 32) * EPI_BUF_BYTES,
@@ -744,7 +743,7 @@ __device__ __forceinline__ void cluster_sum_epilogue(
 // ------------------------------------------------------------- the GEMM
 
 template <int BN, bool PAIR, bool EPI, bool CLU>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(gemm_threads(EPI, CLU), 1)
     tsm_gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap map_a,
                             const __grid_constant__ CUtensorMap map_b,
                             const __grid_constant__ CUtensorMap map_out,
@@ -754,6 +753,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     using Cfg = TileCfg<BN, PAIR>;
     constexpr int S = Cfg::STAGES;
     static_assert(!(CLU && PAIR), "the cluster split-K sum is built for one CTA per tile");
+    // Epilogue warps: four (one per TMEM lane quarter), or with a fused
+    // epilogue eight -- two per quarter, taking alternate boxes of its rows,
+    // so that one warp's arithmetic latency hides behind the other's (a
+    // single warp per sub-partition issues well below one instruction per
+    // cycle on the activation's dependent chains).  The staging space stays
+    // the same: one box buffer per warp instead of two.
+    constexpr int EW = epilogue_warps(EPI, CLU);
+    constexpr int HW = EW / 4;   // epilogue warps per TMEM lane quarter
+    constexpr int ET = 32 * EW;  // epilogue threads
+    constexpr int NBUF = 2 / HW; // staging buffers per epilogue warp
+    static_assert(EW * NBUF * Cfg::EPI_BUF_BYTES == Cfg::EPI_BYTES, "epilogue staging");
+    constexpr uint32_t TEMPTY = uint32_t((PAIR ? 2 : 1) * EW);  // arrivals that free an accumulator
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -797,7 +808,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(tfull0 + 8u * b, 1);
-            ptx::mbar_init(tempty0 + 8u * b, Cfg::TEMPTY_ARRIVALS);
+            ptx::mbar_init(tempty0 + 8u * b, TEMPTY);
         }
         ptx::mbar_init(done_bar, 1);
         ptx::mbar_init(stall_bar, 1);
@@ -1002,7 +1013,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- epilogue: warps 2..5, TMEM lane quarter = warp % 4
         const int e = warp - 2;
         const int q = warp & 3;
-        const uint32_t bufs = epi0 + uint32_t(e) * 2u * Cfg::EPI_BUF_BYTES;
+        const int h = e >> 2;  // which of the quarter's warps (0 unless HW == 2)
+        const uint32_t bufs = epi0 + uint32_t(e) * uint32_t(NBUF) * Cfg::EPI_BUF_BYTES;
         uint32_t abuf = 0, aphase = 0, sbuf = 0;
         if (p.fused && blockIdx.x == 0 && threadIdx.x == 64)
             publish_counters(p.counters, p.counter_words, p.epoch_tag, p.epoch);
@@ -1023,7 +1035,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint64_t epoch_now = 0;
             if (et == 0)
                 epoch_now = ptx::ld_relaxed_gpu(p.epoch_tag);
-            ptx::named_bar_sync(1, 128);
+            ptx::named_bar_sync(1, ET);
             const int32_t r0 = (w.s * 2 + int32_t(rank)) * p.rows_per;
             const bool active = r0 < Cfg::TILE_M && w.m0 + r0 < p.M;
             if (et == 0) {
@@ -1038,26 +1050,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 *red_ok = okv;
             }
-            ptx::named_bar_sync(1, 128);  // the acquire above orders the reads below
+            ptx::named_bar_sync(1, ET);  // the acquire above orders the reads below
             if (*red_ok && active) {
                 constexpr int U = 4;                                  // chunks in flight per thread
                 const int32_t per_row = BN / 4;                       // float4s of a row
-                const int32_t nf = p.rows_per * per_row;
+                // Only rows inside the tile are read: the last reducer's
+                // share may be short, and past the last partial the
+                // workspace ends (0 <= r0 < tile_m here).
+                const int32_t nf = min(p.rows_per, Cfg::TILE_M - r0) * per_row;
                 const int64_t part = int64_t(Cfg::TILE_M) * per_row;  // float4s of one partial
                 const float4 *src = reinterpret_cast<const float4 *>(p.ws) +
                                     int64_t(w.red_tile) * p.split_k * part + int64_t(r0) * per_row;
                 const float *bias = EPI && p.epi.bias ? p.epi.bias + int64_t(w.z_in) * p.epi.bias_stride : nullptr;
                 auto run = [&](auto act) {
-                    for (int32_t f0 = et; f0 < nf; f0 += 128 * U) {
+                    for (int32_t f0 = et; f0 < nf; f0 += ET * U) {
                         float4 a[U];
 #pragma unroll
                         for (int k = 0; k < U; ++k)
-                            a[k] = f0 + 128 * k < nf ? __ldcg(src + f0 + 128 * k) : make_float4(0.f, 0.f, 0.f, 0.f);
+                            a[k] = f0 + ET * k < nf ? __ldcg(src + f0 + ET * k) : make_float4(0.f, 0.f, 0.f, 0.f);
                         for (int32_t s2 = 1; s2 < p.split_k; ++s2) {
                             float4 v[U];
 #pragma unroll
                             for (int k = 0; k < U; ++k)
-                                v[k] = f0 + 128 * k < nf ? __ldcg(src + s2 * part + f0 + 128 * k) : a[k];
+                                v[k] = f0 + ET * k < nf ? __ldcg(src + s2 * part + f0 + ET * k) : a[k];
 #pragma unroll
                             for (int k = 0; k < U; ++k) {
                                 a[k].x += v[k].x;
@@ -1068,7 +1083,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
 #pragma unroll
                         for (int k = 0; k < U; ++k) {
-                            const int32_t f = f0 + 128 * k;
+                            const int32_t f = f0 + ET * k;
                             const int32_t row = f / per_row;
                             const int32_t gr = w.m0 + r0 + row;
                             const int32_t gc = w.n0 + (f - row * per_row) * 4;
@@ -1107,7 +1122,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     run(ActTag<kActNone>{});
                 }
             }
-            ptx::named_bar_sync(1, 128);
+            ptx::named_bar_sync(1, ET);
             if (et == 0)
                 trace_stamp(p, kTraceReduced);
         };
@@ -1256,19 +1271,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool drain = u + nclusters >= num_units;
             auto take_buf = [&](int c) -> uint32_t {
                 if (drain)
-                    return base + (uint32_t(e) * uint32_t(BN / 32) + uint32_t(c)) * Cfg::EPI_BUF_BYTES;
-                if (lane == 0)
-                    ptx::bulk_wait_group_read<1>();  // the store that used this buffer has read it
-                __syncwarp();
-                const uint32_t b = bufs + sbuf * Cfg::EPI_BUF_BYTES;
-                sbuf ^= 1u;
-                return b;
+                    return base + (uint32_t(e) * uint32_t(BN / 32 / HW) + uint32_t(c / HW)) * Cfg::EPI_BUF_BYTES;
+                if constexpr (NBUF == 2) {
+                    if (lane == 0)
+                        ptx::bulk_wait_group_read<1>();  // the store that used this buffer has read it
+                    __syncwarp();
+                    const uint32_t b = bufs + sbuf * Cfg::EPI_BUF_BYTES;
+                    sbuf ^= 1u;
+                    return b;
+                } else {
+                    if (lane == 0)
+                        ptx::bulk_wait_group_read<0>();  // the warp's previous store has read it
+                    __syncwarp();
+                    return bufs;
+                }
             };
-            for (int c = 0; c < nch; ++c) {
+            // This warp's boxes: all of them, or every HW-th from h.
+            for (int c = h; c < nch; c += HW) {
                 uint32_t r[32];
                 ptx::tmem_ld_32x32b_x32(tm_row + 32u * c, r);
                 ptx::tmem_wait_ld();
-                if (c == nch - 1)
+                if (c + HW >= nch)
                     release_acc();
                 const bool tma = via_tma(c);
                 if constexpr (EPI) {
@@ -1300,7 +1323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tail_box(c, r);
             }
-            if (nch == 0)
+            if (h >= nch)  // no box for this warp
                 release_acc();
             if (++abuf == 2) {
                 abuf = 0;
@@ -1334,7 +1357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the separate reduce kernel, so the sums are bitwise the same) and
             // writes C.  All four epilogue warps pass the three named barriers
             // on every path.
-            const int et = int(threadIdx.x) - 64;  // 0..127
+            const int et = int(threadIdx.x) - 64;  // 0 .. ET - 1
             // The counters belong to this launch once CTA 0 has published the
             // epoch, normally long before now: read it early (relaxed) and
             // check it after the barrier; the GPU-scope fence before the
@@ -1348,7 +1371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // GPU-scope fence (cumulative) before its arrival.
             if (lane == 0)
                 ptx::fence_proxy_async_global();
-            ptx::named_bar_sync(1, 128);
+            ptx::named_bar_sync(1, ET);
             const int64_t bz = w.z_in;
             const int32_t ri = w.s * (PAIR ? 2 : 1) + int32_t(rank);
             const int32_t r0 = ri * p.rows_per;               // first tile row this CTA sums
@@ -1376,7 +1399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 *red_ok = okv;
             }
-            ptx::named_bar_sync(1, 128);
+            ptx::named_bar_sync(1, ET);
             if (*red_ok && active) {
                 // The load is in flight and finishes on its own: wait it out.
                 if (wait_bounded(red_bar, 0, af, kStatusReduce, false)) {
@@ -1429,8 +1452,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // activation is a compile-time constant of the loop (one
                     // dispatch per CTA), so the values' activations overlap.
                     auto sum_all = [&](auto act) {
-                        for (int32_t f0 = et; f0 < per_split; f0 += 256) {
-                            const int32_t f1 = f0 + 128;
+                        for (int32_t f0 = et; f0 < per_split; f0 += 2 * ET) {
+                            const int32_t f1 = f0 + ET;
                             const bool two = f1 < per_split;
                             float4 a0 = stg[f0];
                             float4 a1 = two ? stg[f1] : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1466,7 +1489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            ptx::named_bar_sync(1, 128);
+            ptx::named_bar_sync(1, ET);
             if (et == 0)
                 trace_stamp(p, kTraceReduced);
         }
@@ -1693,7 +1716,7 @@ static cudaError_t launch_bn(const CUtensorMap &a, const CUtensorMap &b, const C
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(grid), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(gemm_threads(EPI, CLU), 1, 1);
     cfg.dynamicSmemBytes = TileCfg<BN, PAIR>::SMEM_BYTES;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -1758,7 +1781,7 @@ static cudaError_t capacity_of(int red_cluster, int *clusters)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(red_cluster), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(gemm_threads(false, true), 1, 1);
     cfg.dynamicSmemBytes = TileCfg<BN, false>::SMEM_BYTES;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
