@@ -1,8 +1,11 @@
 """Build ``libtsm_gemm.so`` in-tree with nvcc for sm_103a only.
 
-Three translation units (the GEMM kernels, the row-reduction kernels, the
-host API) compile in parallel; the kernel units are compiled with ``-Xptxas -v`` and the build fails if ptxas reports any
-spill stores or loads (only ptxas's printed summary is read).
+The translation units compile in parallel: the plain GEMM kernels and the
+cluster split-K sums, the fused-epilogue GEMM kernels once per activation
+(``gemm_epi.cu`` with ``-DTSM_EPI_ACT``), the row-reduction kernels and the
+host API.  The kernel units are compiled with ``-Xptxas -v`` and the build
+fails if ptxas reports any spill stores or loads (only ptxas's printed
+summary is read).
 """
 from __future__ import annotations
 
@@ -21,8 +24,13 @@ LIB_NAME = "libtsm_gemm.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
 PTXAS_LOG = os.path.join(BUILD_DIR, "ptxas.log")
 
-SOURCES = ["gemm_kernels.cu", "rowsum_kernels.cu", "gemm_api.cu"]
-HEADERS = ["gemm_internal.h", "ptx.cuh"]
+# (source, object name, extra nvcc flags); the activations are gemm_internal.h's kAct* values
+ACTIVATIONS = ["none", "relu", "leaky_relu", "gelu", "gelu_tanh", "silu"]
+UNITS = ([("gemm_kernels.cu", "gemm_kernels", [])] +
+         [("gemm_epi.cu", f"gemm_epi_{a}", [f"-DTSM_EPI_ACT={i}"]) for i, a in enumerate(ACTIVATIONS)] +
+         [("rowsum_kernels.cu", "rowsum_kernels", []), ("gemm_api.cu", "gemm_api", [])])
+SOURCES = sorted({u[0] for u in UNITS})
+HEADERS = ["gemm_internal.h", "gemm_kernel.cuh", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -47,8 +55,8 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def _compile(src: str, obj: str, verbose_ptxas: bool) -> str:
-    cmd = [_nvcc(), "-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC",
+def _compile(src: str, obj: str, verbose_ptxas: bool, flags: list[str]) -> str:
+    cmd = [_nvcc(), "-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC", *flags,
            "-I", os.path.join(REPO, "include"), "-c", os.path.join(HERE, src), "-o", obj]
     if verbose_ptxas:
         cmd += ["-Xptxas", "-v"]
@@ -70,13 +78,15 @@ def build(force: bool = False, quiet: bool = True) -> str:
     if not force and up_to_date():
         return LIB_PATH
     os.makedirs(BUILD_DIR, exist_ok=True)
-    objs = [os.path.join(BUILD_DIR, os.path.splitext(s)[0] + ".o") for s in SOURCES]
-    with ThreadPoolExecutor(len(SOURCES)) as ex:
+    objs = [os.path.join(BUILD_DIR, name + ".o") for _, name, _ in UNITS]
+    kernel_unit = [src != "gemm_api.cu" for src, _, _ in UNITS]
+    with ThreadPoolExecutor(len(UNITS)) as ex:
         logs = list(ex.map(lambda a: _compile(*a),
-                           [(s, o, s.endswith("_kernels.cu")) for s, o in zip(SOURCES, objs)]))
+                           [(src, o, k, fl) for (src, _, fl), o, k in zip(UNITS, objs, kernel_unit)]))
+    ptxas = "".join(log for log, k in zip(logs, kernel_unit) if k)
     with open(PTXAS_LOG, "w") as f:
-        f.write(logs[0] + logs[1])
-    check_spills(logs[0] + logs[1])
+        f.write(ptxas)
+    check_spills(ptxas)
     tmp = LIB_PATH + f".tmp{os.getpid()}"
     r = subprocess.run([_nvcc(), *ARCH, "-shared", "-o", tmp, *objs],
                        capture_output=True, text=True)

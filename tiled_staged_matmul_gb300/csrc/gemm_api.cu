@@ -113,7 +113,7 @@ struct DeviceState {
     int sms = 0;
     int cc_major = 0, cc_minor = 0;
     int smem_optin = 0;
-    bool attrs_set[14] = {};  // see attr_index
+    bool attrs_set[39] = {};  // see attr_index
     cudaMemPool_t pool = nullptr;
     uint32_t *status = nullptr;
     // Clusters of 2 and of 4 CTAs of the cluster-sum kernel that fit at once.
@@ -172,12 +172,13 @@ int config_index(int tile_m, int tile_n)
 }
 
 // Slot of DeviceState::attrs_set: the plain kernels 0-4, with the fused
-// epilogue 5-9, the cluster-sum kernels (tile_n 128 / 256, plain or fused) 10-13.
-int attr_index(int tile_m, int tile_n, bool epi, int red_cluster)
+// epilogue 5-34 (five tile shapes for each of the six activations), the
+// cluster-sum kernels (tile_n 128 / 256, plain or fused) 35-38.
+int attr_index(int tile_m, int tile_n, bool epi, int red_cluster, int act)
 {
     if (red_cluster > 1)
-        return 10 + (tile_n == 256 ? 1 : 0) + (epi ? 2 : 0);
-    return config_index(tile_m, tile_n) + (epi ? 5 : 0);
+        return 35 + (tile_n == 256 ? 1 : 0) + (epi ? 2 : 0);
+    return config_index(tile_m, tile_n) + (epi ? 5 + 5 * act : 0);
 }
 
 // Estimated clusters of `n` CTAs (one per SM) that fit at once on a GB300 of
@@ -806,9 +807,9 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
     if (ds->smem_optin < pl.smem_bytes)
         return fail(GEMM_ERR_UNSUPPORTED_DEVICE, "device allows %d bytes of shared memory per block, the kernel needs %lld",
                     ds->smem_optin, (long long)pl.smem_bytes);
-    const int ti = attr_index(pl.tile_m, pl.tile_n, use_epi, pl.red_cluster);
+    const int ti = attr_index(pl.tile_m, pl.tile_n, use_epi, pl.red_cluster, pr.epi.act);
     if (!ds->attrs_set[ti]) {
-        if ((e = set_kernel_attributes(pl.tile_m, pl.tile_n, use_epi, pl.red_cluster)) != cudaSuccess)
+        if ((e = set_kernel_attributes(pl.tile_m, pl.tile_n, use_epi, pl.red_cluster, pr.epi.act)) != cudaSuccess)
             return fail_cuda(e, "cudaFuncSetAttribute(max dynamic shared memory)");
         ds->attrs_set[ti] = true;
     }
@@ -967,11 +968,11 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
     // The GEMM writes raw partials (the plain kernel); the reduce applies
     // the epilogue to the sums.
     kp.epi = Epilogue{};
-    if (st == GEMM_OK && !ds->attrs_set[attr_index(pl.tile_m, pl.tile_n, false, 1)]) {
+    if (st == GEMM_OK && !ds->attrs_set[attr_index(pl.tile_m, pl.tile_n, false, 1, kActNone)]) {
         if ((e = set_kernel_attributes(pl.tile_m, pl.tile_n, false)) != cudaSuccess)
             st = fail_cuda(e, "cudaFuncSetAttribute(max dynamic shared memory)");
         else
-            ds->attrs_set[attr_index(pl.tile_m, pl.tile_n, false, 1)] = true;
+            ds->attrs_set[attr_index(pl.tile_m, pl.tile_n, false, 1, kActNone)] = true;
     }
     if (st == GEMM_OK) {
         if ((e = launch_tcgen05_gemm(pl.tile_m, pl.tile_n, false, 1, map_a, map_b, map_out, map_out,

@@ -162,10 +162,21 @@ SmemBudget smem_budget(int tile_m, int tile_n);
 // plain one (identity Epilogue only).
 // `red_cluster` > 1: the kernel built for the cluster split-K sum, launched in
 // clusters of that many CTAs (one CTA per tile only).
-cudaError_t set_kernel_attributes(int tile_m, int tile_n, bool epi, int red_cluster = 1);
+// `act`: with `epi`, the activation the kernel is built for (the cluster
+// split-K sums read it at run time and take any).
+cudaError_t set_kernel_attributes(int tile_m, int tile_n, bool epi, int red_cluster = 1, int act = kActNone);
 // Clusters of `red_cluster` CTAs of the cluster-sum kernel (tile_n columns)
 // that fit on the device at once (cudaOccupancyMaxActiveClusters).
 cudaError_t cluster_capacity(int tile_n, int red_cluster, int *clusters);
+// The fused-epilogue kernels of one CTA or a pair for activation ACT
+// (gemm_epi.cu, one unit per activation).
+template <int ACT>
+cudaError_t set_epi_attributes(int tile_m, int tile_n);
+template <int ACT>
+cudaError_t launch_epi(int tile_m, int tile_n, const CUtensorMap &map_a, const CUtensorMap &map_b,
+                       const CUtensorMap &map_out, const CUtensorMap &map_ws, const CUtensorMap &map_red,
+                       const KernelParams &p, int grid, cudaStream_t stream);
+// With `epi` and no cluster sum, the kernel of p.epi.act.
 cudaError_t launch_tcgen05_gemm(int tile_m, int tile_n, bool epi, int red_cluster,
                                 const CUtensorMap &map_a,
                                 const CUtensorMap &map_b, const CUtensorMap &map_out,
