@@ -37,6 +37,8 @@ L2_BYTES = 129 * 1024 * 1024
 # The kernels and the host code that plans their launches: recorded DRAM
 # traffic is valid only for the exact code that produced it.
 KERNEL_SOURCES = ["tiled_staged_matmul_gb300/csrc/gemm_kernels.cu",
+                  "tiled_staged_matmul_gb300/csrc/gemm_kernel.cuh",
+                  "tiled_staged_matmul_gb300/csrc/gemm_epi.cu",
                   "tiled_staged_matmul_gb300/csrc/rowsum_kernels.cu",
                   "tiled_staged_matmul_gb300/csrc/gemm_internal.h",
                   "tiled_staged_matmul_gb300/csrc/ptx.cuh",
