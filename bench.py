@@ -348,7 +348,33 @@ def roofline_of(flops, algorithmic_bytes, ms, traffic, kernel, clocks=None):
                                if roofline["bound"] == "tensor" else
                                f"{peaks['source']} (MEASURED_PEAKS.json copy bandwidth)")
     roofline["kernel"] = kernel
+    if roofline["bound"] == "tensor":
+        roofline["per_clock"] = per_clock_peak(tflops_launch, clocks)
     return roofline
+
+
+# Dense f16 tensor rate per SM and clock assumed for the secondary peak
+# (B200's published dense figure divided by its SMs and clock).
+F16_FLOP_PER_CLK_PER_SM = 8192
+
+
+def per_clock_peak(tflops, clocks, sms=None):
+    """The secondary tensor peak: SMs x 8192 dense f16 flop per clock x SM
+    clock, at the maximum clock and at the median clock the timed region ran
+    at, with the achieved rate's fraction of each (SMs: the current device's
+    unless given)."""
+    if sms is None:
+        import torch
+        if not torch.cuda.is_available():
+            return None
+        sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    out = {"sms": sms, "flop_per_clk_per_sm": F16_FLOP_PER_CLK_PER_SM}
+    for key, mhz in (("at_max_clock", (clocks or {}).get("sm_max_mhz")),
+                     ("at_load_clock", (clocks or {}).get("sm_mhz"))):
+        if mhz:
+            peak = sms * F16_FLOP_PER_CLK_PER_SM * mhz * 1e6 / 1e12
+            out[key] = {"mhz": mhz, "tflops": round(peak, 1), "frac": round(tflops / peak, 4)}
+    return out
 
 
 def run_grouped(args, rank, local_rank, world):
@@ -595,6 +621,7 @@ def run_ours(args, rank, local_rank, world):
         result["workloads"] = table
         result["binding_us_per_call"] = ctypes_us_per_call()
         result["gpu_launches"] += len(SIDE_WORKLOADS) * max(args.workload_rounds, 10)
+        result["gpu_launches"] += sum(e["warm_l2"]["steps"] for e in table.values() if "warm_l2" in e)
 
     if not args.no_e2e and not fused:
         result["e2e"] = run_e2e(args, w, A_h, B_h, dev, world)
@@ -706,6 +733,8 @@ def time_workloads(args, names, dev, world, local_rank, rounds: int, headline=No
         roof["frac_best"] = round(roof["frac"] * st["mean"] / st["min"], 4)
         entry["roofline"] = roof
         entry["clocks"] = clocks if call is not None else head_clocks
+        if call is not None and flush:
+            entry["warm_l2"] = warm_l2_steps(call, w, stream, max(rounds // 2, 10))
         if call is not None:
             entry["host_us_per_call"] = host_us_per_call(call)
             span = kernel_span_us(binding, call, plan, flush_l2 if flush else None, dev)
@@ -715,6 +744,25 @@ def time_workloads(args, names, dev, world, local_rank, rounds: int, headline=No
                     roof["frac"] * st["mean"] * 1e3 / span, 4)
         out[w.name] = entry
     return out, clocks
+
+
+def warm_l2_steps(call, w, stream, steps: int) -> dict:
+    """The same workload with no L2 flush between steps (its inputs stay
+    L2-resident): back-to-back steps, each bracketed by CUDA events."""
+    import torch
+    for _ in range(3):
+        call()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for e0, e1 in ev:
+        e0.record(stream)
+        call()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    st = step_stats([e0.elapsed_time(e1) for e0, e1 in ev])
+    return {"label": "warm L2: no flush between steps, inputs L2-resident", "steps": steps,
+            "ms_per_step": st, "value": round(w.flops / (st["mean"] * 1e-3) / 1e12, 3),
+            "unit": "TFLOP/s"}
 
 
 def host_us_per_call(call, calls: int = 200) -> float:

@@ -81,3 +81,14 @@ def test_burst_object_uses_the_burst_peak():
     # a bandwidth-bound shape against the copy bandwidth
     lk = bench.burst_of(2 * 256 * 256 * 65536, 67 * 2 ** 20, 0.027)
     assert lk["bound"] == "hbm" and lk["peak"] == peaks["hbm_gbs"]
+
+
+def test_per_clock_peak():
+    # 152 SMs x 8192 flop/clk: 2577.5 TFLOP/s at 2070 MHz, 1869.7 at 1501.5 MHz
+    r = bench.per_clock_peak(1400.0, {"sm_mhz": 1501.5, "sm_max_mhz": 2070.0}, sms=152)
+    assert r["flop_per_clk_per_sm"] == 8192 and r["sms"] == 152
+    assert r["at_max_clock"]["tflops"] == round(152 * 8192 * 2070e6 / 1e12, 1)
+    assert abs(r["at_max_clock"]["frac"] - 1400.0 / (152 * 8192 * 2070e6 / 1e12)) < 1e-4
+    assert abs(r["at_load_clock"]["frac"] - 1400.0 / (152 * 8192 * 1501.5e6 / 1e12)) < 1e-4
+    # no clocks: only the SM count and rate
+    assert set(bench.per_clock_peak(1.0, None, sms=4)) == {"sms", "flop_per_clk_per_sm"}
