@@ -99,14 +99,21 @@ typedef enum gemm_status {
 typedef struct gemm_options {
     int32_t split_k;    /* 0: planner's choice; S >= 1: split K into S contiguous ranges
                            (clamped to the number of 64-deep k-blocks) */
-    int32_t tile_n;     /* 0: planner's choice; else 64, 128 or 256 output columns per tile */
+    int32_t tile_n;     /* 0: planner's choice; else 64, 128, 256 or 512 output columns per
+                           tile.  512 is a CTA pair's tile (tile_m 0 or 256) holding one
+                           256 x 512 accumulator (all of TMEM) and issuing two 256-column
+                           MMAs per k-step on one A tile: whole tiles only, so split_k must
+                           be 0 or 1 and there is no tail; grouped calls refuse it, and the
+                           planner takes it by itself only for ungrouped calls without a
+                           requested split or tail.  Its sums are bitwise those of 256-wide
+                           whole tiles. */
     int32_t timeout_ms; /* 0: default; else the limit of every device-side wait, in ms */
     int32_t inject_stall; /* test hook, 0 in normal use; 1 makes the epilogue wait on a
                              barrier that nothing signals, so that its bounded wait runs
                              out and the call reports GEMM_ERR_DEVICE_TIMEOUT */
     int32_t tile_m;     /* 0: planner's choice; 128: one CTA per tile; 256: a CTA pair per
                            tile (a 2-CTA cluster issuing tcgen05 cta_group::2 MMAs; needs
-                           tile_n 128 or 256) */
+                           tile_n 128, 256 or 512) */
     int32_t splitk_reduce; /* 0 or 2: sum split-K partials inside the GEMM kernel when the
                               plan allows it (every cluster owns one unit), else in a second
                               kernel; 1: always the second kernel, and no split tail.  Both
@@ -326,6 +333,8 @@ gemm_status_t gemv_f16_f32acc(const uint16_t *A, const uint16_t *x, float *y, in
 
 /* The plan the library would use, computed on the host only (no GPU is
  * touched).  num_sms is the SM count to plan for (0 = the current device's).
+ * It is the plan of an ungrouped call; a grouped call plans with split_k 1,
+ * no tail and without the 512-column tile. */
  * This is the analogue of the pages' footprint check and K_TILE choice
  * ("The PTSS Cliff ...", sections "The SLM Footprint" and "Choosing
  * K_TILE"): the ring holds as many A+B k-block stages as fit the shared

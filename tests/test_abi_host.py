@@ -129,7 +129,8 @@ def test_stage_footprint_matches_the_pages_arithmetic(b):
     assert p["stage_bytes"] == g["total_bytes"]
 
 
-@pytest.mark.parametrize("tile_m,tile_n", [(128, 64), (128, 128), (128, 256), (256, 128), (256, 256)])
+@pytest.mark.parametrize("tile_m,tile_n", [(128, 64), (128, 128), (128, 256), (256, 128), (256, 256),
+                                           (256, 512)])
 def test_ring_fills_the_shared_memory_budget(b, tile_m, tile_n):
     p = b.gemm_plan(4096, 4096, 4096, 1, b._opts(tile_n=tile_n, tile_m=tile_m), SMS)
     assert (p["tile_m"], p["tile_n"]) == (tile_m, tile_n)
@@ -147,6 +148,32 @@ def test_ring_fills_the_shared_memory_budget(b, tile_m, tile_n):
 def test_pair_needs_a_wide_tile(b):
     with pytest.raises(b.GemmError):
         b.gemm_plan(4096, 4096, 4096, 1, b._opts(tile_n=64, tile_m=256), SMS)
+
+
+@pytest.mark.parametrize("M,N,K,wide", [
+    (8192, 8192, 8192, True), (6144, 6144, 6144, True), (3072, 3072, 8192, True),
+    (16384, 16384, 4096, True), (4096, 4096, 4096, False), (1000, 1000, 1000, False),
+    (256, 256, 65536, False), (12288, 12288, 1024, False), (8192, 4096, 8192, False)])
+def test_wide_pair_tile_plans(b, M, N, K, wide):
+    # The planner takes 256 x 512 tiles where their fewer operand bytes
+    # per flop outweigh the unhidden hand-over of the single accumulator
+    # and the coarser waves (long K, whole waves); on request it always does.
+    assert (b.gemm_plan(M, N, K, 1, None, SMS)["tile_n"] == 512) == wide
+    p = b.gemm_plan(M, N, K, 1, b._opts(tile_n=512), SMS)
+    # a CTA pair per 256 x 512 tile, whole tiles only: no K split, no tail
+    assert (p["tile_m"], p["tile_n"], p["split_k"], p["tail_split"]) == (256, 512, 1, 0)
+    tiles = -(-M // 256) * -(-N // 512)
+    assert (p["tiles_m"], p["tiles_n"], p["units"]) == (-(-M // 256), -(-N // 512), tiles)
+    assert p["grid"] == 2 * min(tiles, SMS // 2)
+    assert p["workspace_bytes"] == 0
+
+
+def test_wide_pair_tile_rejects_other_shapes(b):
+    for o in (b._opts(tile_n=512, tile_m=128), b._opts(tile_n=512, split_k=2), b._opts(tile_n=384)):
+        with pytest.raises(b.GemmError):
+            b.gemm_plan(4096, 4096, 4096, 1, o, SMS)
+    with pytest.raises(b.GemmError):
+        b.gemm_plan(4096, 4096, 4096, 1, b._opts(tile_n=512), 1)
 
 
 @pytest.mark.parametrize("M,N,K", [(64, 128, 128), (1000, 1000, 1000), (4096, 4096, 4096),
@@ -217,7 +244,7 @@ def test_long_K_small_output_splits_K(b):
 
 def test_large_square_uses_wide_tiles_without_split(b):
     p = b.gemm_plan(8192, 8192, 8192, 1, None, SMS)
-    assert (p["tile_m"], p["tile_n"], p["split_k"]) == (256, 256, 1)  # CTA pairs
+    assert (p["tile_m"], p["tile_n"], p["split_k"]) == (256, 512, 1)  # CTA pairs
 
 
 def cluster_opts(b, red_cluster, split_k=0, tile_n=0):
@@ -329,14 +356,15 @@ def test_split_tail_by_default_only_when_it_pays(b):
     # the planner's choice (options absent or split_tail 0): long enough tiles
     # split in K ranges ...
     assert tail(4096, 4096, 4096) == (2, "K")
-    assert tail(8192, 8192, 8192) == (2, "K")
+    assert tail(8192, 8192, 8192, 1, b._opts(tile_n=256)) == (2, "K")
+    assert tail(8192, 8192, 8192) == (0, "-")  # 256 x 512 tiles: whole waves, no tail
     assert tail(2304, 2304, 8192) == (15, "K")
     assert tail(6144, 4096, 4096, 1, b.GemmOptions()) == (16, "K")
     # ... short ones in column slices (storing and summing the partials would
     # cost more than the narrower tiles lose), and batches too
     assert tail(4096, 4096, 1024) == (2, "N")
     assert tail(8192, 8192, 2048) == (2, "N")
-    assert tail(8192, 8192, 8192, 3) == (2, "N")
+    assert tail(8192, 8192, 8192, 3, b._opts(tile_n=256)) == (2, "N")
     # a last wave more than half full stays whole
     assert tail(6144, 6144, 6144) == (0, "-")
 

@@ -157,7 +157,7 @@ def test_batched_with_a_bias_per_batch(b):
     assert pad_ok
 
 
-@pytest.mark.parametrize("tile_m,tile_n", [(128, 64), (128, 256), (256, 128), (256, 256)])
+@pytest.mark.parametrize("tile_m,tile_n", [(128, 64), (128, 256), (256, 128), (256, 256), (256, 512)])
 def test_every_tile_shape_with_16_bit_output(b, tile_m, tile_n):
     M, N, K = 520, 333, 300
     A, B = synthetic.operands(M, N, K, "uniform", seed=78)
@@ -166,6 +166,20 @@ def test_every_tile_shape_with_16_bit_output(b, tile_m, tile_n):
                           opts=b.GemmOptions(1, tile_n, 0, 0, tile_m))
     check_epilogue(C, oracle.gemm_f64(A, B, M, N, K), 1.0, bias, "gelu_tanh", "f16", K)
     assert pad_ok
+
+
+@pytest.mark.parametrize("act,out", [("gelu", "bf16"), ("silu", "f32"), ("leaky_relu", "f16")])
+def test_wide_pair_tile_epilogue_matches_the_256_wide_tile_bitwise(b, act, out):
+    # Whole tiles and no K split on both: the same sums and the same
+    # epilogue arithmetic per element, so the same bits.
+    M, N, K = 1000, 1304, 776
+    A, B = synthetic.operands(M, N, K, "normal", seed=79)
+    bias = np.linspace(-1, 1, N).astype(np.float32)
+    outs = [run_fused(b, A, B, alpha=0.5, bias=bias, act=act, out=out, slope=0.1,
+                      opts=b.GemmOptions(1, tile_n, 0, 0, 256)) for tile_n in (256, 512)]
+    assert np.array_equal(outs[0][0], outs[1][0], equal_nan=True)
+    assert outs[1][1]
+    check_epilogue(outs[1][0], oracle.gemm_f64(A, B, M, N, K), 0.5, bias, act, out, K, slope=0.1)
 
 
 def test_repacked_16_bit_output(b):

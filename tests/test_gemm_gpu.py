@@ -30,7 +30,8 @@ def b():
 
 
 # (tile_m, tile_n): one CTA per 128-row tile, or a CTA pair per 256-row tile
-TILES = [(128, 64), (128, 128), (128, 256), (256, 128), (256, 256)]
+# (256 x 512: the pair's single-accumulator tile, two MMAs per k-step)
+TILES = [(128, 64), (128, 128), (128, 256), (256, 128), (256, 256), (256, 512)]
 
 
 def ref_of(A, B):
@@ -173,11 +174,62 @@ def test_pair_tiles_with_many_units_per_cluster(b):
     check_exact(C.numpy(), ref_of(A, B))
 
 
+def test_wide_pair_tile_walks_many_tiles(b):
+    # 4096 x 4096 on 256 x 512 tiles: 128 units over at most 76 clusters, so
+    # the single accumulator is drained and refilled tile after tile.
+    A, B = synthetic.operands(4096, 4096, 512, "int4", seed=29)
+    C, dC = run_gemm(b, A, B, tile_m=256, tile_n=512)
+    check_exact(C.numpy(), ref_of(A, B))
+    assert dC.outside_untouched()
+
+
+def test_wide_pair_tile_batched(b):
+    batch, M, N, K = 3, 600, 1100, 300
+    A, B = synthetic.operands(M, N, K, "int4", seed=31, batch=batch)
+    C, dC = run_gemm(b, A, B, batch=batch, tile_m=256, tile_n=512)
+    for i in range(batch):
+        check_exact(C[i].numpy(), ref_of(A[i], B[i]))
+    assert dC.outside_untouched()
+
+
+@pytest.mark.parametrize("M,N,K", [(1536, 2560, 4096), (1000, 1300, 777)])
+def test_wide_pair_tile_matches_the_256_wide_tile_bitwise(b, M, N, K):
+    # Each output element takes the same MMAs in the same k order in a
+    # 256 x 256 and a 256 x 512 tile (whole tiles, no K split), so the two
+    # plans agree bit for bit on random inputs.
+    A, B = synthetic.operands(M, N, K, "normal", seed=M + 3 * N + K)
+    C256, _ = run_gemm(b, A, B, tile_m=256, tile_n=256, split_k=1)
+    C512, dC = run_gemm(b, A, B, tile_m=256, tile_n=512, split_k=1)
+    assert torch.equal(C256, C512)
+    check_tolerance(C512.numpy(), ref_of(A, B), K)
+    assert dC.outside_untouched()
+
+
+def test_wide_pair_tile_rejects_grouped_calls(b):
+    A = torch.zeros(2, 256, 64, dtype=torch.float16, device="cuda")
+    B = torch.zeros(2, 64, 512, dtype=torch.float16, device="cuda")
+    rows = torch.tensor([200, 256], dtype=torch.int32, device="cuda")
+    with pytest.raises(b.GemmError):
+        b.grouped_gemm(A, B, rows, tile_m=256, tile_n=512)
+    # left to the planner, a grouped call takes another tile
+    out = b.grouped_gemm(A, B, rows)
+    assert torch.equal(out, torch.zeros(2, 256, 512, device="cuda"))
+
+
 def test_8192_cube_every_cell(b, full_8192):
     """The headline workload at full size in its default plan, every cell
     against the fp64 oracle."""
     w, A, B, ref = full_8192
     C, dC = run_gemm(b, A, B)
+    check_tolerance(C.numpy(), ref, w.K)
+    assert dC.outside_untouched()
+
+
+def test_8192_cube_wide_pair_tile_every_cell(b, full_8192):
+    """The headline workload on the opt-in 256 x 512 pair tile, every cell
+    against the fp64 oracle."""
+    w, A, B, ref = full_8192
+    C, dC = run_gemm(b, A, B, tile_m=256, tile_n=512)
     check_tolerance(C.numpy(), ref, w.K)
     assert dC.outside_untouched()
 

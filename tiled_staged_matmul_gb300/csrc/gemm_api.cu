@@ -113,7 +113,7 @@ struct DeviceState {
     int sms = 0;
     int cc_major = 0, cc_minor = 0;
     int smem_optin = 0;
-    bool attrs_set[39] = {};  // see attr_index
+    bool attrs_set[46] = {};  // see attr_index
     cudaMemPool_t pool = nullptr;
     uint32_t *status = nullptr;
     // Clusters of 2 and of 4 CTAs of the cluster-sum kernel that fit at once.
@@ -173,9 +173,12 @@ int config_index(int tile_m, int tile_n)
 
 // Slot of DeviceState::attrs_set: the plain kernels 0-4, with the fused
 // epilogue 5-34 (five tile shapes for each of the six activations), the
-// cluster-sum kernels (tile_n 128 / 256, plain or fused) 35-38.
+// cluster-sum kernels (tile_n 128 / 256, plain or fused) 35-38, the
+// 256 x 512 pair tile 39 (plain) and 40-45 (fused, one per activation).
 int attr_index(int tile_m, int tile_n, bool epi, int red_cluster, int act)
 {
+    if (tile_n == 512)
+        return epi ? 40 + act : 39;
     if (red_cluster > 1)
         return 35 + (tile_n == 256 ? 1 : 0) + (epi ? 2 : 0);
     return config_index(tile_m, tile_n) + (epi ? 5 + 5 * act : 0);
@@ -341,22 +344,32 @@ int ceil_div(int64_t a, int64_t b) { return int((a + b - 1) / b); }
 struct TileChoice {
     int tile_m, tile_n;
 };
-constexpr TileChoice kChoices[] = {{256, 256}, {256, 128}, {128, 256}, {128, 128}, {128, 64}};
+// The 256 x 512 pair tile (one accumulator, two 256-column MMAs per k-step
+// on one A tile) takes whole tiles only: no K split, no tail.
+constexpr TileChoice kChoices[] = {{256, 256}, {256, 128}, {128, 256}, {128, 128}, {128, 64}, {256, 512}};
 
+// `wide`: the planner may pick the 256 x 512 tile by itself (it is always
+// taken when asked for).
 gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const gemm_options_t *o,
-                        int sms, int caps2, int caps4, gemm_plan_info_t *pl)
+                        int sms, int caps2, int caps4, gemm_plan_info_t *pl, bool wide)
 {
     if (sms <= 0)
         return fail(GEMM_ERR_INVALID_VALUE, "SM count must be positive");
     memset(pl, 0, sizeof *pl);
     const int req_n = o ? o->tile_n : 0;
     const int req_m = o ? o->tile_m : 0;
-    if (req_n != 0 && req_n != 64 && req_n != 128 && req_n != 256)
-        return fail(GEMM_ERR_INVALID_VALUE, "tile_n must be 0, 64, 128 or 256 (got %d)", req_n);
+    if (req_n != 0 && req_n != 64 && req_n != 128 && req_n != 256 && req_n != 512)
+        return fail(GEMM_ERR_INVALID_VALUE, "tile_n must be 0, 64, 128, 256 or 512 (got %d)", req_n);
     if (req_m != 0 && req_m != 128 && req_m != 256)
         return fail(GEMM_ERR_INVALID_VALUE, "tile_m must be 0, 128 or 256 (got %d)", req_m);
     if (req_m == 256 && req_n == 64)
         return fail(GEMM_ERR_INVALID_VALUE, "tile_m 256 (a CTA pair) needs tile_n 128 or 256");
+    if (req_n == 512 && req_m == 128)
+        return fail(GEMM_ERR_INVALID_VALUE, "tile_n 512 is a CTA pair's tile: tile_m must be 0 or 256");
+    if (req_n == 512 && o && o->split_k > 1)
+        return fail(GEMM_ERR_INVALID_VALUE, "tile_n 512 takes whole tiles: split_k must be 0 or 1");
+    if (req_n == 512 && sms < 2)
+        return fail(GEMM_ERR_INVALID_VALUE, "a CTA pair needs at least two SMs");
     if (req_m == 256 && sms < 2)
         return fail(GEMM_ERR_INVALID_VALUE, "a CTA pair needs at least two SMs");
     const int req_s = o ? o->split_k : 0;
@@ -375,12 +388,19 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const ge
     auto tiles_of = [&](int tm, int tn) { return int64_t(ceil_div(Mx, tm)) * ceil_div(Nx, tn) * batch; };
     auto slots_of = [&](int tm) { return int64_t(tm == 2 * kTileM ? sms / 2 : sms); };
     auto tile_elems_of = [](int tm, int tn) { return int64_t(tm) * tn; };
+    // The planner's own pick of the 256 x 512 tile: only where no K split
+    // and no tail are asked for, since that tile takes neither.
+    const int req_tail = o ? o->split_tail : 0;
+    const bool wide_auto = wide && req_s <= 1 && req_tail != 1 && req_tail != 3;
     auto allowed = [&](const TileChoice &c) {
-        return (req_m == 0 || req_m == c.tile_m) && (req_n == 0 || req_n == c.tile_n) &&
+        return (req_m == 0 || req_m == c.tile_m) &&
+               (req_n == 0 ? wide_auto || c.tile_n != 512 : req_n == c.tile_n) &&
                (c.tile_m == kTileM || sms >= 2);
     };
     // K ranges that put about one unit on every slot, at least 4 k-blocks each.
     auto split_for = [&](int tm, int tn) -> int {
+        if (tn == 512)
+            return 1;
         if (req_s > 0)
             return std::min(req_s, k_blocks);
         const int64_t tiles = tiles_of(tm, tn);
@@ -404,7 +424,12 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const ge
     // at ~87 GB/s per SM, whichever is longer (measured on GB300: 256 x 256
     // pair tiles run ~15 % over their MMA time, 256 x 128 column slices at
     // three quarters of a whole tile's time).
+    // The 256 x 512 pair tile: its MMAs at ~12.5 TFLOP/s per SM (measured
+    // on GB300 at 8192^3 and 6144^3; a quarter fewer operand bytes per flop
+    // than 256 x 256, so the MMAs bound it).
     auto kb_us = [&](int tm, int w) {
+        if (w == 512)
+            return 2.0 * kTileM * w * kTileK / 12.5e12 * 1e6;
         const double mma = 2.0 * kTileM * w * kTileK / 13.1e12 * 1e6;
         const double bytes = 2.0 * kTileK * (kTileM + (tm == 2 * kTileM ? w / 2 : w));
         return std::max(mma, bytes / 87e9 * 1e6);
@@ -413,7 +438,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const ge
         const int mode = o ? o->split_tail : 0;
         const int req_r0 = o ? o->splitk_reduce : 0;
         Tail none;
-        if (mode == 2 || req_s != 0 || K == 0)
+        if (mode == 2 || req_s != 0 || K == 0 || tn == 512)
             return none;
         const int64_t slots = slots_of(tm), tiles = tiles_of(tm, tn);
         const int64_t rem = tiles % slots;
@@ -491,8 +516,15 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const ge
             const Tail tl = tail_of(c.tile_m, c.tile_n);
             const double waves = tl.pieces ? double(tiles / slots) + tl.frac
                                            : double((tiles + slots - 1) / slots);
-            cost = waves * double(k_blocks) * kb_us(c.tile_m, c.tile_n) +
-                   (c.tile_m == 2 * kTileM ? 8.0 : 0.0);
+            // The 256 x 512 tile's single accumulator is not handed to the
+            // next tile's MMAs until its epilogue has read it all out, which
+            // waits on the stores: about 6.5 us less 0.1 us per k-block per
+            // wave (the stores of short tiles contend most), and 8 us more
+            // for the last epilogue -- fitted on GB300 to 27 shapes timed
+            // both ways, K from 512 to 16384.
+            const double handover = c.tile_n == 512 ? std::max(0.0, 6.5 - 0.1 * k_blocks) : 0.0;
+            cost = waves * (double(k_blocks) * kb_us(c.tile_m, c.tile_n) + handover) +
+                   (c.tile_m == 2 * kTileM ? 8.0 : 0.0) + (c.tile_n == 512 ? 8.0 : 0.0);
         }
         if (!best || cost < best_cost) {
             best = &c;
@@ -802,8 +834,10 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
     }
     gemm_plan_info_t pl;
     if ((st = make_plan(pr.M, pr.N, pr.K, pr.batch, (o || pr.group_rows) ? &og : nullptr, ds->sms,
-                        ds->caps2, ds->caps4, &pl)) != GEMM_OK)
+                        ds->caps2, ds->caps4, &pl, !pr.group_rows)) != GEMM_OK)
         return st;
+    if (pl.tile_n == 512 && pr.group_rows)
+        return fail(GEMM_ERR_INVALID_VALUE, "grouped calls take tile_n 64, 128 or 256");
     if (ds->smem_optin < pl.smem_bytes)
         return fail(GEMM_ERR_UNSUPPORTED_DEVICE, "device allows %d bytes of shared memory per block, the kernel needs %lld",
                     ds->smem_optin, (long long)pl.smem_bytes);
@@ -1307,7 +1341,7 @@ gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const ge
         }
         g_last_error.clear();
     }
-    return make_plan(M, N, K, std::max<int64_t>(batch, 1), opts, sms, caps2, caps4, plan);
+    return make_plan(M, N, K, std::max<int64_t>(batch, 1), opts, sms, caps2, caps4, plan, true);
 }
 
 gemm_status_t gemm_get_device_status(gemm_stream_t stream)
@@ -1482,13 +1516,13 @@ extern "C" gemm_status_t gemm_f16_f32acc_splitk_noalloc(const uint16_t *A, const
     o.split_k = split_k;
     o.splitk_reduce = 1;  // partials in the scratch, summed by the separate reduce kernel
     gemm_plan_info_t pl;
-    if ((st = make_plan(M, N, K, 1, &o, nd->sms, 0, 0, &pl)) != GEMM_OK)
+    if ((st = make_plan(M, N, K, 1, &o, nd->sms, 0, 0, &pl, false)) != GEMM_OK)
         return st;
     if (split_k == 0 && uint64_t(pl.workspace_bytes) > kNoAllocScratchBytes) {
         // The planner's split does not fit: take the largest split that does.
         const int64_t per_split = M * ((N + 3) / 4 * 4) * 4;
         o.split_k = int32_t(std::max<int64_t>(1, int64_t(kNoAllocScratchBytes) / per_split));
-        if ((st = make_plan(M, N, K, 1, &o, nd->sms, 0, 0, &pl)) != GEMM_OK)
+        if ((st = make_plan(M, N, K, 1, &o, nd->sms, 0, 0, &pl, false)) != GEMM_OK)
             return st;
     }
     if (uint64_t(pl.workspace_bytes) > kNoAllocScratchBytes)

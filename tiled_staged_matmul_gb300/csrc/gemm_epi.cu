@@ -18,6 +18,7 @@ cudaError_t set_epi_attributes(int tile_m, int tile_n)
         switch (tile_n) {
         case 128: return set_attr<128, true, true, false, ACT>();
         case 256: return set_attr<256, true, true, false, ACT>();
+        case 512: return set_attr<512, true, true, false, ACT>();
         default: return cudaErrorInvalidValue;
         }
     }
@@ -38,6 +39,7 @@ cudaError_t launch_epi(int tile_m, int tile_n, const CUtensorMap &map_a, const C
         switch (tile_n) {
         case 128: return launch_bn<128, true, true, false, ACT>(map_a, map_b, map_out, map_ws, map_red, p, grid, stream);
         case 256: return launch_bn<256, true, true, false, ACT>(map_a, map_b, map_out, map_ws, map_red, p, grid, stream);
+        case 512: return launch_bn<512, true, true, false, ACT>(map_a, map_b, map_out, map_ws, map_red, p, grid, stream);
         default: return cudaErrorInvalidValue;
         }
     }

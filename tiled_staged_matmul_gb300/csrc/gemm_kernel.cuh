@@ -19,9 +19,12 @@ namespace tsm {
 // 2-CTA cluster) with tcgen05 cta_group::2 -- 256 rows per tile, each CTA
 // staging its own 128 rows of A and its own BN/2 columns of B, and holding
 // its 128 rows of the accumulator.  Without PAIR one CTA does a 128-row tile.
+// A pair's 512-column tile is two 256-column MMAs per k-step on one A tile
+// (a quarter fewer operand bytes per flop); its accumulator takes all of
+// TMEM, so there is one instead of two.
 template <int BN, bool PAIR>
 struct TileCfg {
-    static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
+    static_assert(BN == 64 || BN == 128 || BN == 256 || (BN == 512 && PAIR), "tile width");
     static_assert(!PAIR || BN >= 128, "a CTA pair needs at least 64 B columns per CTA");
     static constexpr int ROWS = kTileM;                    // rows of A / C per CTA
     static constexpr int TILE_M = PAIR ? 2 * kTileM : kTileM;
@@ -47,12 +50,22 @@ struct TileCfg {
                       GROUP_TABLE_OFF + 4 * kMaxGroupsPerLaunch <= CTRL_BYTES,
                   "control block layout");
     static constexpr int SMEM_BYTES = ALIGN_SLACK + STAGES * STAGE_BYTES + EPI_BYTES + CTRL_BYTES;
-    // Two accumulators of BN f32 columns each per CTA (a power of two >= 32).
-    static constexpr uint32_t TMEM_COLS = 2 * BN;
+    // Two accumulators of BN f32 columns each per CTA (a power of two >= 32),
+    // or one when two do not fit the 512 TMEM columns.
+    static constexpr int ACC = 2 * BN <= 512 ? 2 : 1;
+    static constexpr uint32_t TMEM_COLS = uint32_t(ACC * BN);
+    // The MMA width: the tile's, in 256-column halves for a 512-column tile.
+    static constexpr int MMA_N = BN > 256 ? 256 : BN;
+    static constexpr int MMA_HALVES = BN / MMA_N;
+    // B boxes of one MMA in a CTA's stage: a pair's MMA takes each CTA's
+    // half of its columns, so a 512-column tile's CTA stages, of each
+    // 256-column half of the tile, the 128 columns its rank picks.
+    static constexpr int B_BOXES_PER_MMA = B_BOXES / MMA_HALVES;
     static_assert(SMEM_BYTES > SMEM_LIMIT / 2, "one CTA per SM keeps TMEM allocation uncontended");
-    // The CTA's last unit stages all its output boxes in the idle ring at once.
-    static_assert(STAGES * STAGE_BYTES >= EPI_WARPS * (BN / 32) * EPI_BUF_BYTES,
-                  "the ring holds a whole output tile of one CTA");
+    // Whether the CTA's last unit can stage all its output boxes in the idle
+    // ring at once (else it keeps the double-buffered staging).
+    static constexpr bool DRAIN_FITS = STAGES * STAGE_BYTES >= EPI_WARPS * (BN / 32) * EPI_BUF_BYTES;
+    static_assert(BN == 512 || DRAIN_FITS, "the ring holds a whole output tile of one CTA");
 };
 
 // Instruction descriptor of tcgen05.mma.kind::f16: D f32 (bits 4-5 = 1),
@@ -838,10 +851,14 @@ __global__ void __launch_bounds__(gemm_threads(EPI, CLU), 1)
             bool ok = true;
             for (int64_t u = cluster; ok && u < num_units; u += nclusters) {
                 const Unit w = decode_unit(u, p, gtab, Cfg::TILE_M, BN);
-                // This CTA's B columns: half of the unit's in a pair, in
-                // boxes of 64 columns.
+                // This CTA's B columns: half of each MMA's in a pair, in
+                // boxes of 64 columns; box j at bcol(j).
                 const int nbox = w.width / (PAIR ? 128 : 64);
-                const int32_t col_off = PAIR ? int32_t(rank) * (w.width / 2) : 0;
+                const int32_t col_off = PAIR ? int32_t(rank) * (min(w.width, Cfg::MMA_N) / 2) : 0;
+                auto bcol = [&](int j) {
+                    return w.n0 + col_off + (j / Cfg::B_BOXES_PER_MMA) * Cfg::MMA_N +
+                           64 * (j % Cfg::B_BOXES_PER_MMA);
+                };
                 const uint32_t tx = uint32_t(Cfg::A_BYTES + nbox * Cfg::B_BOX_BYTES);
                 if (p.prefetch_l2) {
                     // The unit's whole K range of A and B at once: DRAM sees the
@@ -852,7 +869,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI, CLU), 1)
 #pragma unroll
                         for (int j = 0; j < Cfg::B_BOXES; ++j)
                             if (j < nbox)
-                                ptx::tma_prefetch_l2_3d(&map_b, w.n0 + col_off + 64 * j, kb * kTileK, w.z_in);
+                                ptx::tma_prefetch_l2_3d(&map_b, bcol(j), kb * kTileK, w.z_in);
                     }
                 }
                 for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
@@ -871,7 +888,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI, CLU), 1)
                         for (int j = 0; j < Cfg::B_BOXES; ++j)
                             if (j < nbox)
                                 ptx::tma_load_3d_pair(sa + Cfg::A_BYTES + j * Cfg::B_BOX_BYTES, &map_b,
-                                                      fb, w.n0 + col_off + 64 * j, kb * kTileK, w.z_in);
+                                                      fb, bcol(j), kb * kTileK, w.z_in);
                     } else {
                         const uint32_t fb = full0 + 8u * stage;
                         ptx::mbar_arrive_expect_tx(fb, tx);
@@ -915,9 +932,9 @@ __global__ void __launch_bounds__(gemm_threads(EPI, CLU), 1)
             // ---------------- MMA issuer (one thread; the leader of a pair)
             // Instruction descriptors of a whole tile and of the column
             // slices a narrow tail cuts it into (halves and quarters).
-            constexpr uint32_t idesc = mma_idesc<BN, PAIR>();
-            constexpr uint32_t idesc2 = mma_idesc<BN / 2, PAIR>();
-            constexpr uint32_t idesc4 = mma_idesc<BN / 4, PAIR>();
+            constexpr uint32_t idesc = mma_idesc<Cfg::MMA_N, PAIR>();
+            constexpr uint32_t idesc2 = mma_idesc<Cfg::MMA_N / 2, PAIR>();
+            constexpr uint32_t idesc4 = mma_idesc<Cfg::MMA_N / 4, PAIR>();
             constexpr uint16_t both = PAIR ? 3 : 1;
             uint32_t stage = 0, phase = 0, abuf = 0, aphase = 0;
             bool ok = true;
@@ -943,9 +960,15 @@ __global__ void __launch_bounds__(gemm_threads(EPI, CLU), 1)
 #pragma unroll
                     for (int kk = 0; kk < kTileK / 16; ++kk) {
                         // A: advance 16 f16 = 32 bytes along the swizzled row.
-                        // B: advance 16 K rows = 2048 bytes.
-                        ptx::mma_f16_ss<PAIR>(d, desc_a(sa + 32u * kk), desc_b(sb + 2048u * kk),
-                                              id, (kb > w.kb0 || kk > 0) ? 1u : 0u);
+                        // B: advance 16 K rows = 2048 bytes.  A 512-column tile:
+                        // the second half's B boxes follow the first's.
+#pragma unroll
+                        for (int hh = 0; hh < Cfg::MMA_HALVES; ++hh)
+                            ptx::mma_f16_ss<PAIR>(
+                                d + uint32_t(hh * Cfg::MMA_N),
+                                desc_a(sa + 32u * kk),
+                                desc_b(sb + uint32_t(hh * Cfg::B_BOXES_PER_MMA * Cfg::B_BOX_BYTES) + 2048u * kk),
+                                id, (kb > w.kb0 || kk > 0) ? 1u : 0u);
                     }
                     ptx::mma_commit<PAIR>(empty0 + 8u * stage, both);  // slot free in both CTAs
                     if (++stage == S) {
@@ -956,7 +979,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI, CLU), 1)
                 if (!ok)
                     break;
                 ptx::mma_commit<PAIR>(tfull0 + 8u * abuf, both);  // accumulator ready
-                if (++abuf == 2) {
+                if (++abuf == uint32_t(Cfg::ACC)) {
                     abuf = 0;
                     aphase ^= 1u;
                 }
@@ -1240,7 +1263,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI, CLU), 1)
             };
             // On the CTA's last unit the operand ring is idle: each box gets
             // a buffer of its own there and no store waits for another.
-            const bool drain = u + nclusters >= num_units;
+            const bool drain = Cfg::DRAIN_FITS && u + nclusters >= num_units;
             auto take_buf = [&](int c) -> uint32_t {
                 if (drain)
                     return base + (uint32_t(e) * uint32_t(BN / 32 / HW) + uint32_t(c / HW)) * Cfg::EPI_BUF_BYTES;
@@ -1296,7 +1319,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI, CLU), 1)
             }
             if (h >= nch)  // no box for this warp
                 release_acc();
-            if (++abuf == 2) {
+            if (++abuf == uint32_t(Cfg::ACC)) {
                 abuf = 0;
                 aphase ^= 1u;
             }

@@ -189,7 +189,8 @@ static SmemBudget budget_of()
 SmemBudget smem_budget(int tile_m, int tile_n)
 {
     if (tile_m == 2 * kTileM)
-        return tile_n == 128 ? budget_of<128, true>() : budget_of<256, true>();
+        return tile_n == 128 ? budget_of<128, true>()
+                             : tile_n == 512 ? budget_of<512, true>() : budget_of<256, true>();
     switch (tile_n) {
     case 64: return budget_of<64, false>();
     case 128: return budget_of<128, false>();
@@ -219,6 +220,7 @@ static cudaError_t set_plain_or_cluster_attrs(int tile_m, int tile_n, bool epi, 
         switch (tile_n) {
         case 128: return set_attr<128, true, false, false, kActNone>();
         case 256: return set_attr<256, true, false, false, kActNone>();
+        case 512: return set_attr<512, true, false, false, kActNone>();
         default: return cudaErrorInvalidValue;
         }
     }
@@ -273,6 +275,7 @@ static cudaError_t launch_plain_or_cluster(int tile_m, int tile_n, bool epi, int
         switch (tile_n) {
         case 128: return launch_bn<128, true, false, false, kActNone>(map_a, map_b, map_out, map_ws, map_red, p, grid, stream);
         case 256: return launch_bn<256, true, false, false, kActNone>(map_a, map_b, map_out, map_ws, map_red, p, grid, stream);
+        case 512: return launch_bn<512, true, false, false, kActNone>(map_a, map_b, map_out, map_ws, map_red, p, grid, stream);
         default: return cudaErrorInvalidValue;
         }
     }
