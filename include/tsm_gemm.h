@@ -334,7 +334,7 @@ gemm_status_t gemv_f16_f32acc(const uint16_t *A, const uint16_t *x, float *y, in
 /* The plan the library would use, computed on the host only (no GPU is
  * touched).  num_sms is the SM count to plan for (0 = the current device's).
  * It is the plan of an ungrouped call; a grouped call plans with split_k 1,
- * no tail and without the 512-column tile. */
+ * no tail and without the 512-column tile.
  * This is the analogue of the pages' footprint check and K_TILE choice
  * ("The PTSS Cliff ...", sections "The SLM Footprint" and "Choosing
  * K_TILE"): the ring holds as many A+B k-block stages as fit the shared
