@@ -394,8 +394,8 @@ def run_grouped(args, rank, local_rank, world):
     stream = torch.cuda.current_stream()
     opts = binding.GemmOptions(0, args.tile_n, 0, 0, args.tile_m)
     per_launch = min(w.groups, 256)
-    plan = binding.gemm_plan(w.M, w.N, w.K, per_launch, binding.GemmOptions(1, args.tile_n, 0, 0,
-                                                                            args.tile_m))
+    plan = binding.gemm_plan_grouped(w.M, w.N, w.K, per_launch, binding.GemmOptions(0, args.tile_n, 0, 0,
+                                                                                    args.tile_m))
     launches_per_call = -(-w.groups // 256)
     flops = w.flops(counts_h)
     abytes = w.algorithmic_bytes(counts_h)

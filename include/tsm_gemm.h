@@ -343,6 +343,16 @@ gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int64_t batch,
                         const gemm_options_t *opts, int32_t num_sms,
                         gemm_plan_info_t *plan);
 
+/* The plan of each launch of a grouped call (gemm_f16_f32acc_grouped and its
+ * fused and optioned forms run their groups in launches of at most 256),
+ * computed on the host only like gemm_plan: `groups` is the number of groups
+ * (clamped to 1..256, the groups of one launch), M the rows allotted to each
+ * group.  Whole tiles only (split_k 1, no tail), never the 512-column tile;
+ * opts->tile_n 512 returns GEMM_ERR_INVALID_VALUE. */
+gemm_status_t gemm_plan_grouped(int64_t M, int64_t N, int64_t K, int64_t groups,
+                                const gemm_options_t *opts, int32_t num_sms,
+                                gemm_plan_info_t *plan);
+
 /* C = A . B like gemm_f16_f32acc, for callers that cannot allocate device
  * memory while they run: allocators or memory managers that call into this
  * library and may not re-enter themselves, and hosts that reserved all of

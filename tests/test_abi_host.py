@@ -168,6 +168,22 @@ def test_wide_pair_tile_plans(b, M, N, K, wide):
     assert p["workspace_bytes"] == 0
 
 
+@pytest.mark.parametrize("M,N,K,groups", [(4096, 14336, 4096, 8), (512, 1408, 2048, 64),
+                                          (8192, 8192, 8192, 1), (300, 700, 50, 300)])
+def test_grouped_plan(b, M, N, K, groups):
+    # whole tiles, never the 512-column tile, at most 256 groups per launch;
+    # otherwise the tile the ordinary planner picks among the others
+    p = b.gemm_plan_grouped(M, N, K, groups, None, SMS)
+    assert p["tile_n"] != 512 and p["split_k"] == 1 and p["tail_split"] == 0
+    per_launch = min(groups, 256)
+    assert p["units"] == per_launch * p["tiles_m"] * p["tiles_n"]
+    q = b.gemm_plan(M, N, K, per_launch, b.GemmOptions(1, 0, 0, 0, 0, 0, 0, 2), SMS)
+    if q["tile_n"] != 512:
+        assert (p["tile_m"], p["tile_n"]) == (q["tile_m"], q["tile_n"])
+    with pytest.raises(b.GemmError):
+        b.gemm_plan_grouped(M, N, K, groups, b._opts(tile_n=512), SMS)
+
+
 def test_wide_pair_tile_rejects_other_shapes(b):
     for o in (b._opts(tile_n=512, tile_m=128), b._opts(tile_n=512, split_k=2), b._opts(tile_n=384)):
         with pytest.raises(b.GemmError):

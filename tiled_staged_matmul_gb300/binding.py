@@ -93,6 +93,9 @@ def _load() -> ctypes.CDLL:
     lib.gemm_plan.restype = ctypes.c_int
     lib.gemm_plan.argtypes = [i64, i64, i64, i64, ctypes.POINTER(GemmOptions), i32,
                               ctypes.POINTER(GemmPlanInfo)]
+    lib.gemm_plan_grouped.restype = ctypes.c_int
+    lib.gemm_plan_grouped.argtypes = [i64, i64, i64, i64, ctypes.POINTER(GemmOptions), i32,
+                                      ctypes.POINTER(GemmPlanInfo)]
     lib.gemm_get_device_status.restype = ctypes.c_int
     lib.gemm_get_device_status.argtypes = [vp]
     lib.gemm_last_error_string.restype = ctypes.c_char_p
@@ -203,6 +206,15 @@ def gemm_plan(M, N, K, batch=1, opts: GemmOptions | None = None, num_sms=0) -> d
     info = GemmPlanInfo()
     p = ctypes.byref(opts) if opts is not None else None
     st = _lib.gemm_plan(M, N, K, batch, p, num_sms, ctypes.byref(info))
+    if st != GEMM_OK:
+        raise GemmError(st, gemm_last_error_string())
+    return info.as_dict()
+
+
+def gemm_plan_grouped(M, N, K, groups=1, opts: GemmOptions | None = None, num_sms=0) -> dict:
+    info = GemmPlanInfo()
+    p = ctypes.byref(opts) if opts is not None else None
+    st = _lib.gemm_plan_grouped(M, N, K, groups, p, num_sms, ctypes.byref(info))
     if st != GEMM_OK:
         raise GemmError(st, gemm_last_error_string())
     return info.as_dict()

@@ -1256,6 +1256,38 @@ gemm_status_t grouped(const uint16_t *A, const uint16_t *B, void *C, const int32
     return GEMM_OK;
 }
 
+// The planner on the host: the SM count and cluster capacities of the
+// current device when num_sms <= 0, else the GB300 estimate for num_sms SMs.
+gemm_status_t host_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const gemm_options_t *opts,
+                        int32_t num_sms, gemm_plan_info_t *plan, bool wide)
+{
+    if (!plan)
+        return fail(GEMM_ERR_INVALID_VALUE, "plan is NULL");
+    if (M < 0 || N < 0 || K < 0 || batch < 0 || M > kInt32Max || N > kInt32Max || K > kInt32Max ||
+        batch > kInt32Max)
+        return fail(GEMM_ERR_INVALID_VALUE, "sizes must be in [0, 2^31)");
+    int sms = num_sms;
+    if (sms <= 0) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess)
+            return fail_cuda(e, "cudaGetDevice");
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return fail_cuda(e, "cudaDeviceGetAttribute(SM count)");
+    }
+    int caps2 = estimated_cluster_capacity(sms, 2), caps4 = estimated_cluster_capacity(sms, 4);
+    if (num_sms <= 0) {
+        int dev = 0;
+        DeviceState *ds = nullptr;
+        if (cudaGetDevice(&dev) == cudaSuccess && device_state(dev, &ds) == GEMM_OK) {
+            caps2 = ds->caps2;
+            caps4 = ds->caps4;
+        }
+        g_last_error.clear();
+    }
+    return make_plan(M, N, K, std::max<int64_t>(batch, 1), opts, sms, caps2, caps4, plan, wide);
+}
+
 }  // namespace
 }  // namespace tsm
 
@@ -1315,33 +1347,24 @@ gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const ge
                         int32_t num_sms, gemm_plan_info_t *plan)
 {
     g_last_error.clear();
-    if (!plan)
-        return fail(GEMM_ERR_INVALID_VALUE, "plan is NULL");
-    if (M < 0 || N < 0 || K < 0 || batch < 0 || M > kInt32Max || N > kInt32Max || K > kInt32Max ||
-        batch > kInt32Max)
-        return fail(GEMM_ERR_INVALID_VALUE, "sizes must be in [0, 2^31)");
-    int sms = num_sms;
-    if (sms <= 0) {
-        int dev = 0;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e != cudaSuccess)
-            return fail_cuda(e, "cudaGetDevice");
-        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-            return fail_cuda(e, "cudaDeviceGetAttribute(SM count)");
-    }
-    // Cluster capacities of the current device when planning for it, else
-    // the GB300 estimate for the given SM count.
-    int caps2 = estimated_cluster_capacity(sms, 2), caps4 = estimated_cluster_capacity(sms, 4);
-    if (num_sms <= 0) {
-        int dev = 0;
-        DeviceState *ds = nullptr;
-        if (cudaGetDevice(&dev) == cudaSuccess && device_state(dev, &ds) == GEMM_OK) {
-            caps2 = ds->caps2;
-            caps4 = ds->caps4;
-        }
-        g_last_error.clear();
-    }
-    return make_plan(M, N, K, std::max<int64_t>(batch, 1), opts, sms, caps2, caps4, plan, true);
+    return tsm::host_plan(M, N, K, batch, opts, num_sms, plan, true);
+}
+
+gemm_status_t gemm_plan_grouped(int64_t M, int64_t N, int64_t K, int64_t groups,
+                                const gemm_options_t *opts, int32_t num_sms, gemm_plan_info_t *plan)
+{
+    g_last_error.clear();
+    // What a grouped launch plans with: whole tiles (its units are known
+    // only on the device), never the 512-column tile.
+    gemm_options_t og = {};
+    if (opts)
+        og = *opts;
+    if (og.tile_n == 512)
+        return fail(GEMM_ERR_INVALID_VALUE, "grouped calls take tile_n 64, 128 or 256");
+    og.split_k = 1;
+    og.split_tail = 2;
+    return tsm::host_plan(M, N, K, std::min<int64_t>(std::max<int64_t>(groups, 1), kMaxGroupsPerLaunch),
+                          &og, num_sms, plan, false);
 }
 
 gemm_status_t gemm_get_device_status(gemm_stream_t stream)
