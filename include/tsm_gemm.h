@@ -373,8 +373,7 @@ gemm_status_t gemm_plan_grouped(int64_t M, int64_t N, int64_t K, int64_t groups,
  * multiples of 8, ldc a multiple of 4).
  *
  * The first call on a device resolves the array's device address and
- * queries the device (no allocation); make that first call before any
- * stream capture begins.  Every call on a device shares the one array and
+ * queries the device (no allocation).  Every call on a device shares the one array and
  * it keeps the last call's partials: calls whose work overlaps on the GPU
  * (for example on two streams at once) race on it and must be ordered by the
  * caller.  Nothing in it needs to start at zero -- every partial the reduce
