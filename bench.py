@@ -59,7 +59,7 @@ def parse_args(argv=None):
     p.add_argument("--shape", default=None,
                    help="MxNxK: an ad-hoc shape with N(0, 1/sqrt(K)) operands instead of --workload")
     p.add_argument("--tile-m", type=int, default=0, help="128 or 256 (CTA pair); 0: planner")
-    p.add_argument("--tile-n", type=int, default=0, help="64, 128 or 256; 0: planner")
+    p.add_argument("--tile-n", type=int, default=0, help="64, 128, 256 or 512; 0: planner")
     p.add_argument("--split-k", type=int, default=0, help="K ranges; 0: planner")
     p.add_argument("--splitk-reduce", type=int, default=0,
                    help="0/2: in-kernel split-K sum when possible, 1: separate reduce kernel")

@@ -103,10 +103,9 @@ typedef struct gemm_options {
                            tile.  512 is a CTA pair's tile (tile_m 0 or 256) holding one
                            256 x 512 accumulator (all of TMEM) and issuing two 256-column
                            MMAs per k-step on one A tile: whole tiles only, so split_k must
-                           be 0 or 1 and there is no tail; grouped calls refuse it, and the
-                           planner takes it by itself only for ungrouped calls without a
-                           requested split or tail.  Its sums are bitwise those of 256-wide
-                           whole tiles. */
+                           be 0 or 1 and there is no tail; the planner takes it by itself
+                           only for ungrouped calls where no split or tail is requested.
+                           Its sums are bitwise those of 256-wide whole tiles. */
     int32_t timeout_ms; /* 0: default; else the limit of every device-side wait, in ms */
     int32_t inject_stall; /* test hook, 0 in normal use; 1 makes the epilogue wait on a
                              barrier that nothing signals, so that its bounded wait runs
@@ -333,8 +332,8 @@ gemm_status_t gemv_f16_f32acc(const uint16_t *A, const uint16_t *x, float *y, in
 
 /* The plan the library would use, computed on the host only (no GPU is
  * touched).  num_sms is the SM count to plan for (0 = the current device's).
- * It is the plan of an ungrouped call; a grouped call plans with split_k 1,
- * no tail and without the 512-column tile.
+ * It is the plan of an ungrouped call; a grouped call plans with split_k 1
+ * and no tail (gemm_plan_grouped).
  * This is the analogue of the pages' footprint check and K_TILE choice
  * ("The PTSS Cliff ...", sections "The SLM Footprint" and "Choosing
  * K_TILE"): the ring holds as many A+B k-block stages as fit the shared
@@ -347,8 +346,8 @@ gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int64_t batch,
  * fused and optioned forms run their groups in launches of at most 256),
  * computed on the host only like gemm_plan: `groups` is the number of groups
  * (clamped to 1..256, the groups of one launch), M the rows allotted to each
- * group.  Whole tiles only (split_k 1, no tail), never the 512-column tile;
- * opts->tile_n 512 returns GEMM_ERR_INVALID_VALUE. */
+ * group.  Whole tiles only: split_k 1 and no tail, whatever opts asks; the
+ * 512-column tile only when opts asks for it. */
 gemm_status_t gemm_plan_grouped(int64_t M, int64_t N, int64_t K, int64_t groups,
                                 const gemm_options_t *opts, int32_t num_sms,
                                 gemm_plan_info_t *plan);

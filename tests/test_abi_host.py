@@ -171,17 +171,18 @@ def test_wide_pair_tile_plans(b, M, N, K, wide):
 @pytest.mark.parametrize("M,N,K,groups", [(4096, 14336, 4096, 8), (512, 1408, 2048, 64),
                                           (8192, 8192, 8192, 1), (300, 700, 50, 300)])
 def test_grouped_plan(b, M, N, K, groups):
-    # whole tiles, never the 512-column tile, at most 256 groups per launch;
-    # otherwise the tile the ordinary planner picks among the others
-    p = b.gemm_plan_grouped(M, N, K, groups, None, SMS)
-    assert p["tile_n"] != 512 and p["split_k"] == 1 and p["tail_split"] == 0
-    per_launch = min(groups, 256)
-    assert p["units"] == per_launch * p["tiles_m"] * p["tiles_n"]
-    q = b.gemm_plan(M, N, K, per_launch, b.GemmOptions(1, 0, 0, 0, 0, 0, 0, 2), SMS)
-    if q["tile_n"] != 512:
-        assert (p["tile_m"], p["tile_n"]) == (q["tile_m"], q["tile_n"])
-    with pytest.raises(b.GemmError):
-        b.gemm_plan_grouped(M, N, K, groups, b._opts(tile_n=512), SMS)
+    # whole tiles whatever the options ask, at most 256 groups per launch,
+    # the 512-column tile only on request: otherwise the ordinary plan of
+    # one launch's groups with no split and no tail
+    for o in (None, b._opts(split_k=4), b.GemmOptions(0, 0, 0, 0, 0, 0, 0, 1)):
+        p = b.gemm_plan_grouped(M, N, K, groups, o, SMS)
+        assert p["split_k"] == 1 and p["tail_split"] == 0 and p["tile_n"] != 512
+        per_launch = min(groups, 256)
+        assert p["units"] == per_launch * p["tiles_m"] * p["tiles_n"]
+        q = b.gemm_plan(M, N, K, per_launch, b.GemmOptions(1, 0, 0, 0, 0, 0, 0, 2), SMS)
+        if q["tile_n"] != 512:
+            assert (p["tile_m"], p["tile_n"]) == (q["tile_m"], q["tile_n"])
+    assert b.gemm_plan_grouped(M, N, K, groups, b._opts(tile_n=512), SMS)["tile_n"] == 512
 
 
 def test_wide_pair_tile_rejects_other_shapes(b):

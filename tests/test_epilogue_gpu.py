@@ -191,7 +191,8 @@ def test_repacked_16_bit_output(b):
     assert pad_ok
 
 
-def test_grouped_with_epilogue_keeps_rows_past_the_counts(b):
+@pytest.mark.parametrize("tile_m,tile_n", [(0, 0), (256, 512)])
+def test_grouped_with_epilogue_keeps_rows_past_the_counts(b, tile_m, tile_n):
     G, M, N, K = 4, 160, 72, 128
     rows = [160, 0, 33, 100]
     A, B = synthetic.operands(M, N, K, "uniform", seed=80, batch=G)
@@ -199,7 +200,7 @@ def test_grouped_with_epilogue_keeps_rows_past_the_counts(b):
     out = torch.full((G, M, N), 9.0, dtype=torch.bfloat16, device="cuda")
     counts = torch.tensor(rows, dtype=torch.int32, device="cuda")
     b.grouped_gemm(A.cuda(), B.cuda(), counts, out=out, alpha=0.5,
-                   bias=torch.as_tensor(bias).cuda(), activation="silu")
+                   bias=torch.as_tensor(bias).cuda(), activation="silu", tile_m=tile_m, tile_n=tile_n)
     C = as_f64(out)
     for g, r in enumerate(rows):
         assert np.all(C[g, r:] == 9.0)

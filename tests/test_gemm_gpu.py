@@ -205,17 +205,6 @@ def test_wide_pair_tile_matches_the_256_wide_tile_bitwise(b, M, N, K):
     assert dC.outside_untouched()
 
 
-def test_wide_pair_tile_rejects_grouped_calls(b):
-    A = torch.zeros(2, 256, 64, dtype=torch.float16, device="cuda")
-    B = torch.zeros(2, 64, 512, dtype=torch.float16, device="cuda")
-    rows = torch.tensor([200, 256], dtype=torch.int32, device="cuda")
-    with pytest.raises(b.GemmError):
-        b.grouped_gemm(A, B, rows, tile_m=256, tile_n=512)
-    # left to the planner, a grouped call takes another tile
-    out = b.grouped_gemm(A, B, rows)
-    assert torch.equal(out, torch.zeros(2, 256, 512, device="cuda"))
-
-
 def test_8192_cube_every_cell(b, full_8192):
     """The headline workload at full size in its default plan, every cell
     against the fp64 oracle."""

@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 
 PRIOR = 7.5  # C's rows at or past a group's count must keep this
 
-TILES = [(128, 64), (128, 128), (128, 256), (256, 128), (256, 256)]
+TILES = [(128, 64), (128, 128), (128, 256), (256, 128), (256, 256), (256, 512)]
 
 
 @pytest.fixture(scope="module")
@@ -90,7 +90,7 @@ def test_ragged_counts_every_tile_shape(b, tile_m, tile_n):
     assert dC.outside_untouched()
 
 
-@pytest.mark.parametrize("tile_m,tile_n", [(128, 128), (256, 256)])
+@pytest.mark.parametrize("tile_m,tile_n", [(128, 128), (256, 256), (256, 512)])
 def test_integer_inputs_are_exact(b, tile_m, tile_n):
     G, M, N, K = 5, 257, 130, 96
     rows = [257, 3, 0, 200, 33]

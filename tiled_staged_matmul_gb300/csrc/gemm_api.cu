@@ -836,8 +836,6 @@ gemm_status_t run(const Problem &pr, const gemm_options_t *o, cudaStream_t strea
     if ((st = make_plan(pr.M, pr.N, pr.K, pr.batch, (o || pr.group_rows) ? &og : nullptr, ds->sms,
                         ds->caps2, ds->caps4, &pl, !pr.group_rows)) != GEMM_OK)
         return st;
-    if (pl.tile_n == 512 && pr.group_rows)
-        return fail(GEMM_ERR_INVALID_VALUE, "grouped calls take tile_n 64, 128 or 256");
     if (ds->smem_optin < pl.smem_bytes)
         return fail(GEMM_ERR_UNSUPPORTED_DEVICE, "device allows %d bytes of shared memory per block, the kernel needs %lld",
                     ds->smem_optin, (long long)pl.smem_bytes);
@@ -1355,12 +1353,12 @@ gemm_status_t gemm_plan_grouped(int64_t M, int64_t N, int64_t K, int64_t groups,
 {
     g_last_error.clear();
     // What a grouped launch plans with: whole tiles (its units are known
-    // only on the device), never the 512-column tile.
+    // only on the device), and the 512-column tile only when asked for
+    // (measured 1 % slower on 8 experts of 4096 x 14336, K 4096, whose
+    // routed rows leave the planner's full-M count of tiles too high).
     gemm_options_t og = {};
     if (opts)
         og = *opts;
-    if (og.tile_n == 512)
-        return fail(GEMM_ERR_INVALID_VALUE, "grouped calls take tile_n 64, 128 or 256");
     og.split_k = 1;
     og.split_tail = 2;
     return tsm::host_plan(M, N, K, std::min<int64_t>(std::max<int64_t>(groups, 1), kMaxGroupsPerLaunch),
