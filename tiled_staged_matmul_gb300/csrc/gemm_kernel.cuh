@@ -1281,8 +1281,56 @@ __global__ void __launch_bounds__(gemm_threads(EPI, CLU), 1)
                     return bufs;
                 }
             };
+            // One box of the plain epilogue: staged and stored by TMA, and
+            // the columns the TMA store does not cover by plain stores.
+            auto plain_box = [&](int c, const uint32_t (&r)[32]) {
+                if (via_tma(c)) {
+                    const uint32_t buf = take_buf(c);
+                    stage_box(buf, r);
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        store_box(c, buf);
+                        ptx::bulk_commit_group();
+                    }
+                }
+                tail_box(c, r);
+            };
+            // The 512-column tile's accumulator is the only one, and the
+            // next tile's MMAs wait until it is read out, which the TMA
+            // stores pace (about 43 GB/s per SM): each warp reads its last
+            // four boxes into registers at once and hands the accumulator
+            // back before it stores them.
+            int nloop = nch;
+            if constexpr (BN == 512 && !EPI) {
+                static_assert(HW == 1, "one epilogue warp per TMEM lane quarter");
+                if (!w.split) {
+                    constexpr int R = 4;
+                    const int nreg = nch < R ? nch : R;
+                    for (int c = 0; c < nch - nreg; ++c) {
+                        uint32_t r[32];
+                        ptx::tmem_ld_32x32b_x32(tm_row + 32u * c, r);
+                        ptx::tmem_wait_ld();
+                        plain_box(c, r);
+                    }
+                    if (nreg > 0) {
+                        uint32_t rr[R][32];
+#pragma unroll
+                        for (int i = 0; i < R; ++i)
+                            if (i < nreg)
+                                ptx::tmem_ld_32x32b_x32(tm_row + 32u * uint32_t(nch - nreg + i), rr[i]);
+                        ptx::tmem_wait_ld();
+                        release_acc();
+#pragma unroll
+                        for (int i = 0; i < R; ++i)
+                            if (i < nreg)
+                                plain_box(nch - nreg + i, rr[i]);
+                    }
+                    nloop = 0;
+                }
+            }
             // This warp's boxes: all of them, or every HW-th from h.
-            for (int c = h; c < nch; c += HW) {
+            for (int c = h; c < nloop; c += HW) {
                 uint32_t r[32];
                 ptx::tmem_ld_32x32b_x32(tm_row + 32u * c, r);
                 ptx::tmem_wait_ld();
