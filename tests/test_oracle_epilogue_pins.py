@@ -4,10 +4,12 @@ rounding).
 Each ties ``oracle.activation_f64`` / ``epilogue_f64`` / ``round_to_out`` to
 something other than itself: table values of the standard normal CDF and of
 the logistic function, odd-symmetry identities that a wrong constant or sign
-breaks, limits, a brute-force bfloat16 rounding that decodes candidate bit
-patterns independently, and numpy's float16 on exact tie cases.
+breaks, limits, PyTorch's own float64 GELU (exact and tanh form) and SiLU,
+a brute-force bfloat16 rounding that decodes candidate bit patterns
+independently, and numpy's float16 on exact tie cases.
 ``test_epilogue_pins_catch_planted_mistakes`` plants typical slips in a
 small copy and checks that some pin rejects each."""
+import importlib.util
 import math
 
 import numpy as np
@@ -57,6 +59,20 @@ def test_limits_and_the_tanh_approximation():
     # the tanh form approximates the erf form to within 5e-4 on [-4, 4]
     assert np.max(np.abs(f(x, "gelu_tanh") - f(x, "gelu"))) < 5e-4
     assert np.max(np.abs(f(x, "gelu_tanh") - f(x, "gelu"))) > 1e-5  # and is not the same function
+
+
+def test_activations_match_the_library_routines():
+    # PyTorch's own CPU implementations in float64 (independent code): the
+    # exact GELU, the tanh form (its 0.044715 and sqrt(2/pi) constants
+    # included, which the symmetry and band pins above cannot fix) and SiLU
+    torch = pytest.importorskip("torch")
+    F = torch.nn.functional
+    x = np.linspace(-8, 8, 1601)
+    t = torch.tensor(x, dtype=torch.float64)
+    f = oracle.activation_f64
+    np.testing.assert_allclose(f(x, "gelu"), F.gelu(t).numpy(), rtol=0, atol=1e-15)
+    np.testing.assert_allclose(f(x, "gelu_tanh"), F.gelu(t, approximate="tanh").numpy(), rtol=0, atol=1e-14)
+    np.testing.assert_allclose(f(x, "silu"), F.silu(t).numpy(), rtol=0, atol=1e-14)
 
 
 def _bf16_brute(v: float) -> float:
@@ -162,6 +178,10 @@ def _epi_like(acc, alpha, bias, name, slope=0.01, mistake=None):
     if name == "gelu":
         arg = v if mistake == "erf_no_sqrt2" else v / math.sqrt(2.0)
         v = 0.5 * v * (1 + np.vectorize(math.erf)(arg))
+    elif name == "gelu_tanh":
+        k = 0.04715 if mistake == "tanh_cubic" else 0.044715
+        c = math.sqrt(2.0 * math.pi) if mistake == "tanh_sqrt" else math.sqrt(2.0 / math.pi)
+        v = 0.5 * v * (1 + np.tanh(c * (v + k * v ** 3)))
     elif name == "silu":
         v = v / (1 + np.exp(v if mistake == "silu_sign" else -v))
     elif name == "leaky_relu":
@@ -180,6 +200,13 @@ def _epi_pins_pass(fn):
     ok &= fn(np.array([-1.0]), 1.0, 3.0, "relu")[0] == 2.0
     ok &= fn(np.array([1.0]), 2.0, 1.0, "relu")[0] == 3.0
     ok &= fn(np.array([-2.0]), 1.0, 0.0, "leaky_relu", 0.25)[0] == -0.5
+    try:
+        import torch
+        x = np.array([-3.0, -1.0, 0.5, 2.0])
+        ref = torch.nn.functional.gelu(torch.tensor(x, dtype=torch.float64), approximate="tanh").numpy()
+        ok &= bool(np.all(np.abs(fn(x, 1.0, 0.0, "gelu_tanh") - ref) < 1e-14))
+    except ImportError:
+        pass
     return bool(ok)
 
 
@@ -187,5 +214,8 @@ def test_epilogue_pins_catch_planted_mistakes():
     assert _epi_pins_pass(lambda *a: _epi_like(*a))
     assert _epi_pins_pass(lambda acc, alpha, bias, name, slope=0.01: oracle.epilogue_f64(
         acc, alpha, np.array([bias]) if np.ndim(bias) == 0 else bias, name, slope))
-    for m in ("alpha_on_bias", "bias_after", "erf_no_sqrt2", "silu_sign", "slope_sign"):
+    mistakes = ["alpha_on_bias", "bias_after", "erf_no_sqrt2", "silu_sign", "slope_sign"]
+    if importlib.util.find_spec("torch") is not None:
+        mistakes += ["tanh_cubic", "tanh_sqrt"]
+    for m in mistakes:
         assert not _epi_pins_pass(lambda *a, m=m: _epi_like(*a, mistake=m)), m
