@@ -7,7 +7,8 @@ OUT.pt.  The test runs this file in a child process with
 CUDA_LAUNCH_BLOCKING=1 -- every launch then waits for the previous one to
 finish, so no two kernels, copies or memsets overlap -- and compares with the
 same cases run in its own process without it: the split-K sums (in the
-kernel, in clusters, in a second kernel, over a partial last wave) and the
+kernel, in clusters, in a second kernel, over a partial last wave), the
+256 x 512 tile's single accumulator handed from tile to tile, and the
 grouped call must not depend on how the GPU happened to schedule the work."""
 from __future__ import annotations
 
@@ -31,6 +32,7 @@ CASES = [
     ("k_range_tail", 4096, 4096, 1024, {"split_tail": 1}, 1),
     ("column_slice_tail", 2304, 2304, 512, {"split_tail": 3}, 1),
     ("batched_split", 200, 136, 12000, {}, 3),
+    ("wide_pair_tile", 4096, 4096, 512, {"tile_m": 256, "tile_n": 512}, 1),
 ]
 GROUPED = ("grouped", 6, 300, 256, 1024, [300, 0, 129, 17, 256, 1])
 

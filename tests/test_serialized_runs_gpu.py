@@ -6,9 +6,10 @@ GPU runs the work in its usual order and show only when the launches are
 serialised, or the other way round ("ADR-1501 ...", section "Context": a
 probe raced on an out-of-order queue and only serialising it exposed the
 race).  The cases in serial_cases.py -- split-K summed in the kernel, in
-clusters, in a second kernel and over a partial last wave, a batched split
-and a grouped call -- run once in a child process with CUDA_LAUNCH_BLOCKING=1
-and once here without it, and every C must be bitwise the same."""
+clusters, in a second kernel and over a partial last wave, a batched split,
+the 256 x 512 tile and a grouped call -- run once in a child process with
+CUDA_LAUNCH_BLOCKING=1 and once here without it, and every C must be
+bitwise the same."""
 import os
 import subprocess
 import sys
