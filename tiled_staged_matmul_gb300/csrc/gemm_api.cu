@@ -363,7 +363,7 @@ gemm_status_t make_plan(int64_t M, int64_t N, int64_t K, int64_t batch, const ge
     if (req_m != 0 && req_m != 128 && req_m != 256)
         return fail(GEMM_ERR_INVALID_VALUE, "tile_m must be 0, 128 or 256 (got %d)", req_m);
     if (req_m == 256 && req_n == 64)
-        return fail(GEMM_ERR_INVALID_VALUE, "tile_m 256 (a CTA pair) needs tile_n 128 or 256");
+        return fail(GEMM_ERR_INVALID_VALUE, "tile_m 256 (a CTA pair) needs tile_n 128, 256 or 512");
     if (req_n == 512 && req_m == 128)
         return fail(GEMM_ERR_INVALID_VALUE, "tile_n 512 is a CTA pair's tile: tile_m must be 0 or 256");
     if (req_n == 512 && o && o->split_k > 1)
