@@ -185,6 +185,19 @@ def test_grouped_plan(b, M, N, K, groups):
     assert b.gemm_plan_grouped(M, N, K, groups, b._opts(tile_n=512), SMS)["tile_n"] == 512
 
 
+@pytest.mark.parametrize("M,N,K,batch", [(1, 1, 1, 1), (200, 300, 64, 1), (256, 512, 64, 3),
+                                         (257, 513, 65, 2), (8192, 8192, 8192, 2)])
+def test_wide_pair_tile_small_ragged_and_batched_plans(b, M, N, K, batch):
+    p = b.gemm_plan(M, N, K, batch, b._opts(tile_n=512), SMS)
+    tiles = -(-M // 256) * -(-N // 512) * batch
+    assert (p["tile_m"], p["tile_n"], p["split_k"], p["tail_split"]) == (256, 512, 1, 0)
+    assert p["units"] == tiles and p["grid"] == 2 * min(tiles, SMS // 2)
+    assert (p["stages"], p["stage_bytes"]) == (4, 2 * 128 * 64 + 2 * 64 * 256)
+    # the planner's own choice for a batch of the headline shape
+    if (M, N, K) == (8192, 8192, 8192):
+        assert b.gemm_plan(M, N, K, batch, None, SMS)["tile_n"] == 512
+
+
 def test_wide_pair_tile_rejects_other_shapes(b):
     for o in (b._opts(tile_n=512, tile_m=128), b._opts(tile_n=512, split_k=2), b._opts(tile_n=384)):
         with pytest.raises(b.GemmError):
